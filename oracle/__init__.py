@@ -1,0 +1,189 @@
+"""CPU oracle for the AdamW optimizer step (plain C, loaded with ctypes).
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's CPU
+baseline leg are the only callers.  The CUDA library never imports, links or
+runs anything here, and this package imports nothing from the CUDA library.
+
+The arithmetic lives in ``adamw_ref.c`` (decoupled-weight-decay Adam with bias
+correction, bf16 Kahan mode and fp32-master mixed mode, global-norm clipping);
+this module only compiles it with ``gcc -ffp-contract=off`` and marshals numpy
+arrays into it.  bf16 values travel as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "adamw_ref.c")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "liboracle_adamw.so")
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+          "-shared", "-Wall", "-Wextra"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(src_path: str, out_path: str) -> str:
+    """Compile one oracle C source into a shared library at ``out_path``."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, "-o", tmp, src_path, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``adamw_ref.c`` when the library is missing or older."""
+    if (force or not os.path.exists(LIB_PATH)
+            or os.path.getmtime(LIB_PATH) < os.path.getmtime(SOURCE)):
+        compile_source(SOURCE, LIB_PATH)
+    return LIB_PATH
+
+
+class Hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float),
+                ("max_grad_norm", ctypes.c_float)]
+
+
+class TensorEntry(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("aux", ctypes.c_void_p), ("numel", ctypes.c_int64)]
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(a: np.ndarray, dtype, n: int | None = None):
+    if a.dtype != dtype or not a.flags.c_contiguous:
+        raise TypeError(f"oracle wants contiguous {np.dtype(dtype)}, got {a.dtype}")
+    if n is not None and a.size != n:
+        raise ValueError(f"size {a.size} != {n}")
+
+
+@dataclass
+class Oracle:
+    """Numpy-level wrappers around one loaded oracle library."""
+    lib: ctypes.CDLL
+
+    def __post_init__(self):
+        L = self.lib
+        vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+        hp = ctypes.POINTER(Hparams)
+        L.oracle_f32_to_bf16.argtypes = [vp, vp, i64]
+        L.oracle_bf16_to_f32.argtypes = [vp, vp, i64]
+        L.oracle_step_scalars.argtypes = [hp, i64, vp]
+        L.oracle_adamw_bf16_kahan.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_adamw_bf16_plain.argtypes = [vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_adamw_mixed.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_grad_sumsq.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_int32)]
+        L.oracle_clip_coef.argtypes = [ctypes.c_double, f32,
+                                       ctypes.POINTER(ctypes.c_double)]
+        L.oracle_clip_coef.restype = f32
+        L.oracle_adamw_list_step.argtypes = [ctypes.POINTER(TensorEntry),
+                                             ctypes.c_int32, ctypes.c_int32, hp,
+                                             i64, ctypes.POINTER(ctypes.c_double)]
+        L.oracle_adamw_list_step.restype = ctypes.c_int32
+
+    # -- bf16 conversion -----------------------------------------------------
+    def f32_to_bf16(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_f32_to_bf16(_ptr(x), _ptr(out), x.size)
+        return out
+
+    def bf16_to_f32(self, h: np.ndarray) -> np.ndarray:
+        h = np.ascontiguousarray(h, dtype=np.uint16)
+        out = np.empty(h.shape, dtype=np.float32)
+        self.lib.oracle_bf16_to_f32(_ptr(h), _ptr(out), h.size)
+        return out
+
+    def step_scalars(self, hp: Hparams, t: int) -> np.ndarray:
+        out = np.empty(5, dtype=np.float32)
+        self.lib.oracle_step_scalars(ctypes.byref(hp), t, _ptr(out))
+        return out
+
+    # -- per-tensor steps (arrays updated in place) ----------------------------
+    def bf16_kahan(self, p, g, m, v, c, hp: Hparams, t: int, coef: float = 1.0):
+        n = p.size
+        for a in (p, g, m, v, c):
+            _check(a, np.uint16, n)
+        self.lib.oracle_adamw_bf16_kahan(_ptr(p), _ptr(g), _ptr(m), _ptr(v),
+                                         _ptr(c), n, ctypes.byref(hp), t, coef)
+
+    def bf16_plain(self, p, g, m, v, hp: Hparams, t: int, coef: float = 1.0):
+        n = p.size
+        for a in (p, g, m, v):
+            _check(a, np.uint16, n)
+        self.lib.oracle_adamw_bf16_plain(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n,
+                                         ctypes.byref(hp), t, coef)
+
+    def mixed(self, master, g, m, v, p_out, hp: Hparams, t: int, coef: float = 1.0):
+        n = master.size
+        for a, dt in ((master, np.float32), (g, np.uint16), (m, np.float32),
+                      (v, np.float32), (p_out, np.uint16)):
+            _check(a, dt, n)
+        self.lib.oracle_adamw_mixed(_ptr(master), _ptr(g), _ptr(m), _ptr(v),
+                                    _ptr(p_out), n, ctypes.byref(hp), t, coef)
+
+    # -- norm ------------------------------------------------------------------
+    def grad_sumsq(self, grads) -> tuple[float, bool]:
+        acc = ctypes.c_double(0.0)
+        bad = ctypes.c_int32(0)
+        for g in grads:
+            _check(g, np.uint16)
+            self.lib.oracle_grad_sumsq(_ptr(g), g.size, ctypes.byref(acc),
+                                       ctypes.byref(bad))
+        return acc.value, bool(bad.value)
+
+    def clip_coef(self, sumsq: float, max_norm: float) -> tuple[float, float]:
+        norm = ctypes.c_double(0.0)
+        coef = self.lib.oracle_clip_coef(sumsq, max_norm, ctypes.byref(norm))
+        return float(np.float32(coef)), norm.value
+
+    # -- whole list -------------------------------------------------------------
+    def list_step(self, tensors, mode: int, hp: Hparams, t: int):
+        """``tensors``: list of (param, grad, exp_avg, exp_avg_sq, aux) numpy
+        arrays.  Returns (skipped: bool, norm: float)."""
+        arr = (TensorEntry * max(1, len(tensors)))()
+        wide = np.uint16 if mode == 0 else np.float32
+        for k, (p, g, m, v, a) in enumerate(tensors):
+            n = g.size
+            _check(p, wide, n); _check(g, np.uint16, n); _check(m, wide, n)
+            _check(v, wide, n); _check(a, np.uint16, n)
+            arr[k] = TensorEntry(p.ctypes.data, g.ctypes.data, m.ctypes.data,
+                                 v.ctypes.data, a.ctypes.data, n)
+        norm = ctypes.c_double(0.0)
+        rc = self.lib.oracle_adamw_list_step(arr, len(tensors), mode,
+                                             ctypes.byref(hp), t,
+                                             ctypes.byref(norm))
+        return bool(rc), norm.value
+
+
+def load(path: str | None = None) -> Oracle:
+    """Load the oracle (building it first when ``path`` is None)."""
+    global _lib
+    if path is not None:
+        return Oracle(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(ctypes.CDLL(build()))
+        return _lib
+
+
+def hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+            max_grad_norm=0.0) -> Hparams:
+    return Hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm)
