@@ -1,0 +1,234 @@
+"""Python binding of the adamw_sm C ABI (include/adamw_sm.h).
+
+Argument marshalling only: every step of the optimizer runs in the library's
+CUDA kernels.  The functions keep the C names; a non-zero status raises
+``AdamWError``.  ``Plan`` is a small convenience wrapper that builds the
+tensor table from torch tensors (torch supplies device memory and streams).
+
+The library is built in-tree (``build.build``) on first use when its sources
+are newer than the shared object; if it cannot be built or loaded, every call
+raises -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+MODE_BF16_KAHAN = 0
+MODE_MIXED_FP32_MASTER = 1
+PLAN_NORM = 1
+
+ADAMW_OK = 0
+ADAMW_ERR_INVALID_ARG = -1
+ADAMW_ERR_MISALIGNED = -2
+ADAMW_ERR_CUDA = -3
+ADAMW_ERR_NO_NORM = -4
+ADAMW_ERR_TOO_LARGE = -5
+
+
+class AdamWError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status}: {adamw_status_string(status)}")
+
+
+class adamw_tensor_t(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("aux", ctypes.c_void_p), ("numel", ctypes.c_int64)]
+
+
+class adamw_hparams_t(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("max_grad_norm", ctypes.c_float)]
+
+
+class adamw_plan_info_t(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("n_tensors", ctypes.c_int32),
+                ("total_elems", ctypes.c_int64), ("grid", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("n_chunks", ctypes.c_int64),
+                ("scalar_elems", ctypes.c_int64), ("device", ctypes.c_int32),
+                ("has_norm", ctypes.c_int32)]
+
+
+class adamw_chunk_t(ctypes.Structure):
+    _fields_ = [("tensor", ctypes.c_int32), ("vec", ctypes.c_int32),
+                ("offset", ctypes.c_int64), ("len", ctypes.c_int64),
+                ("cta", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def load() -> ctypes.CDLL:
+    """Build if needed and load the shared library (raises on failure)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            L.adamw_plan_create.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32, i32,
+                                            ctypes.POINTER(vp)]
+            L.adamw_step.argtypes = [vp, ctypes.POINTER(adamw_hparams_t), i64, vp, vp, vp]
+            L.adamw_grad_norm.argtypes = [vp, vp, vp, vp]
+            L.adamw_plan_destroy.argtypes = [vp]
+            L.adamw_plan_get_info.argtypes = [vp, ctypes.POINTER(adamw_plan_info_t)]
+            L.adamw_plan_chunks.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32, i32,
+                                            ctypes.POINTER(adamw_chunk_t), i64,
+                                            ctypes.POINTER(i64)]
+            L.adamw_step_scalars.argtypes = [ctypes.POINTER(adamw_hparams_t), i64,
+                                             ctypes.POINTER(ctypes.c_float)]
+            L.adamw_copy_probe.argtypes = [vp, vp, i64, vp]
+            L.adamw_status_string.argtypes = [ctypes.c_int]
+            L.adamw_status_string.restype = ctypes.c_char_p
+            for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm",
+                         "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
+                         "adamw_step_scalars", "adamw_copy_probe"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != ADAMW_OK:
+        raise AdamWError(rc, where)
+
+
+def _table(entries) -> tuple[ctypes.Array, int]:
+    entries = list(entries)
+    arr = (adamw_tensor_t * max(1, len(entries)))()
+    for i, e in enumerate(entries):
+        arr[i] = e if isinstance(e, adamw_tensor_t) else adamw_tensor_t(*e)
+    return arr, len(entries)
+
+
+# ------------------------------------------------------------ C functions --
+
+def adamw_status_string(status: int) -> str:
+    return load().adamw_status_string(status).decode()
+
+
+def adamw_plan_create(entries, mode: int, flags: int = 0) -> int:
+    """entries: adamw_tensor_t or (param, grad, exp_avg, exp_avg_sq, aux, numel)
+    tuples of device addresses.  Returns the plan handle."""
+    arr, n = _table(entries)
+    out = ctypes.c_void_p()
+    _check(load().adamw_plan_create(arr, n, mode, flags, ctypes.byref(out)), "adamw_plan_create")
+    return out.value
+
+
+def adamw_step(plan: int, hp: adamw_hparams_t, step: int, d_grad_norm: int = 0,
+               d_nonfinite: int = 0, stream: int = 0) -> None:
+    _check(load().adamw_step(plan, ctypes.byref(hp), step, d_grad_norm or None,
+                             d_nonfinite or None, stream or None), "adamw_step")
+
+
+def adamw_grad_norm(plan: int, d_grad_norm: int = 0, d_nonfinite: int = 0,
+                    stream: int = 0) -> None:
+    _check(load().adamw_grad_norm(plan, d_grad_norm or None, d_nonfinite or None,
+                                  stream or None), "adamw_grad_norm")
+
+
+def adamw_plan_destroy(plan: int) -> None:
+    _check(load().adamw_plan_destroy(plan), "adamw_plan_destroy")
+
+
+def adamw_plan_get_info(plan: int) -> adamw_plan_info_t:
+    info = adamw_plan_info_t()
+    _check(load().adamw_plan_get_info(plan, ctypes.byref(info)), "adamw_plan_get_info")
+    return info
+
+
+def adamw_plan_chunks(entries, mode: int, grid: int) -> list[adamw_chunk_t]:
+    arr, n = _table(entries)
+    count = ctypes.c_int64(0)
+    rc = load().adamw_plan_chunks(arr, n, mode, grid, None, 0, ctypes.byref(count))
+    if rc not in (ADAMW_OK, ADAMW_ERR_TOO_LARGE):
+        _check(rc, "adamw_plan_chunks")
+    out = (adamw_chunk_t * max(1, count.value))()
+    _check(load().adamw_plan_chunks(arr, n, mode, grid, out, count.value, ctypes.byref(count)),
+           "adamw_plan_chunks")
+    return list(out[:count.value])
+
+
+def adamw_step_scalars(hp: adamw_hparams_t, step: int) -> list[float]:
+    out = (ctypes.c_float * 5)()
+    _check(load().adamw_step_scalars(ctypes.byref(hp), step, out), "adamw_step_scalars")
+    return list(out)
+
+
+def adamw_copy_probe(dst: int, src: int, nbytes: int, stream: int = 0) -> None:
+    _check(load().adamw_copy_probe(dst, src, nbytes, stream or None), "adamw_copy_probe")
+
+
+def hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+            max_grad_norm=0.0) -> adamw_hparams_t:
+    return adamw_hparams_t(lr, beta1, beta2, eps, weight_decay, max_grad_norm)
+
+
+# --------------------------------------------------------- torch wrapper --
+
+class Plan:
+    """A plan over lists of torch CUDA tensors (one list per buffer kind).
+
+    bf16 Kahan mode: params, exp_avg, exp_avg_sq, aux (= compensation) bf16.
+    Mixed mode: params (= fp32 master), exp_avg, exp_avg_sq fp32; aux = bf16
+    param out.  grads are bf16 in both.  The tensors must stay alive and in
+    place for the plan's lifetime (the plan holds references to them).
+    """
+
+    def __init__(self, params, grads, exp_avgs, exp_avg_sqs, auxs, mode: int,
+                 norm: bool = False):
+        import torch
+        lists = [list(x) for x in (params, grads, exp_avgs, exp_avg_sqs, auxs)]
+        n = len(lists[0])
+        if any(len(x) != n for x in lists):
+            raise ValueError("tensor lists differ in length")
+        wide = torch.bfloat16 if mode == MODE_BF16_KAHAN else torch.float32
+        want = (wide, torch.bfloat16, wide, wide, torch.bfloat16)
+        entries = []
+        for k in range(n):
+            ts = [x[k] for x in lists]
+            numel = ts[0].numel()
+            for t, dt in zip(ts, want):
+                if not t.is_cuda or t.dtype != dt or not t.is_contiguous() or t.numel() != numel:
+                    raise TypeError(f"tensor {k}: want contiguous CUDA {dt} of {numel} elements")
+            entries.append(adamw_tensor_t(*(t.data_ptr() for t in ts), numel))
+        self._keep = lists
+        self.mode = mode
+        dev = lists[0][0].device if n else torch.device("cuda", torch.cuda.current_device())
+        with torch.cuda.device(dev):
+            self.handle = adamw_plan_create(entries, mode, PLAN_NORM if norm else 0)
+        self.device = dev
+        self.info = adamw_plan_get_info(self.handle)
+
+    def step(self, hp: adamw_hparams_t, step: int, grad_norm=None, nonfinite=None,
+             stream=None) -> None:
+        import torch
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        adamw_step(self.handle, hp, step,
+                   grad_norm.data_ptr() if grad_norm is not None else 0,
+                   nonfinite.data_ptr() if nonfinite is not None else 0,
+                   st.cuda_stream)
+
+    def grad_norm(self, grad_norm=None, nonfinite=None, stream=None) -> None:
+        import torch
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        adamw_grad_norm(self.handle, grad_norm.data_ptr() if grad_norm is not None else 0,
+                        nonfinite.data_ptr() if nonfinite is not None else 0, st.cuda_stream)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            adamw_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,79 @@
+// adamw_internal.h -- types shared by the host planner (plan_build.cpp) and
+// the CUDA kernels (adamw_sm.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "adamw_sm.h"
+
+namespace adamw {
+
+// Threads per CTA of the update and norm-partial kernels.
+constexpr int kBlock = 256;
+// Elements per vector: 8 bf16 = one 16-byte load; 8 fp32 = two.
+constexpr int kVec = 8;
+// Fewest elements a CTA is given before the grid is shrunk (one vector per
+// thread), so tiny lists do not launch idle CTAs.
+constexpr int64_t kMinElemsPerCta = int64_t(kBlock) * kVec;
+
+// Device copy of one adamw_tensor_t (same layout).
+struct TensorDev {
+    void* p;
+    const void* g;
+    void* m;
+    void* v;
+    void* a;
+    int64_t numel;
+};
+static_assert(sizeof(TensorDev) == sizeof(adamw_tensor_t), "table layout");
+
+// One piece of one tensor, processed by exactly one CTA.
+struct ChunkDev {
+    int32_t tensor;
+    int32_t vec;     // 1: all five bases 16-byte aligned at `off`
+    int64_t off;
+    int64_t len;
+};
+
+// Output of the norm finalize kernel, read by the clipped update.
+struct NormOut {
+    double norm;
+    float coef;
+    int32_t nonfinite;
+};
+
+// The per-step scalars the kernels take by value.
+struct StepScalars {
+    float beta1, beta2, omb1, omb2;
+    float step_size, sbc2, eps, lrwd;
+    float max_grad_norm;
+};
+
+// ---- host planner (plan_build.cpp) ----
+
+int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode);
+int validate_hparams(const adamw_hparams_t* hp, int64_t step);
+int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out);
+
+// Splits the list over `grid` CTAs.  chunks are ordered by CTA; cta_begin has
+// grid + 1 entries (chunks of CTA b are [cta_begin[b], cta_begin[b+1])).
+struct Partition {
+    std::vector<ChunkDev> chunks;
+    std::vector<int32_t> chunk_cta;
+    std::vector<int32_t> cta_begin;
+    int64_t total = 0;
+    int64_t scalar_elems = 0;
+};
+int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
+                    int32_t grid, Partition* out);
+
+// The grid a list of `total` elements gets when at most `max_grid` CTAs fit.
+int32_t choose_grid(int64_t total, int32_t max_grid);
+
+// Remembers a CUDA error text for adamw_status_string (per host thread).
+void set_cuda_error(const char* where, const char* what);
+const char* last_cuda_error();
+
+}  // namespace adamw

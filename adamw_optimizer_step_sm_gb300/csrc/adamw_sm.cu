@@ -1,0 +1,797 @@
+// adamw_sm.cu -- sm_103a kernels and the device half of the C ABI.
+//
+// The step is a streaming elementwise update: per element it reads p, g, m, v
+// and c (bf16 Kahan mode, 10 B) or master, m, v and g (mixed mode, 14 B) and
+// writes 8 B or 14 B back, with about twenty fp32 operations in between.
+// That is far below the GPU's ridge point, so HBM bandwidth bounds it and the
+// kernels are built for bytes in flight: a persistent grid (SMs x resident
+// CTAs), one contiguous range of the flattened parameter space per CTA,
+// 16-byte vector loads issued U vectors ahead of the arithmetic, fp32 math,
+// 16-byte stores.  No tensor cores: nothing here is a contraction.
+//
+// Arithmetic order follows the definition in include/adamw_sm.h exactly, with
+// the IEEE round-to-nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn,
+// __fsqrt_rn) so that no multiply-add is fused and every result is the one a
+// strict host implementation of the same formula gives.
+//
+// Sources of the method: "[pure bf16 training] w/ AnyPrecisionAdamW and Kahan
+// summation" (transformers PR #21312), "Train from scratch" recipe (bf16
+// momentum / variance / compensation, Kahan summation, betas 0.9/0.95, weight
+// decay 0.1) and "Theoretical memory allocation" (10 vs 16 B/param);
+// "Distributed optimizer support for BERT" (NeMo PR #5305), "Usage"
+// (distributed_fused_adam: the fp32-state per-shard update).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "adamw_internal.h"
+
+using namespace adamw;
+
+namespace {
+
+// ------------------------------------------------------------ helpers ----
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> bf16, round to nearest even, lo in the low half-word.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    uint32_t u;
+    memcpy(&u, &r, sizeof u);
+    return u;
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float from_bf16(uint16_t h) {
+    return __uint_as_float(uint32_t(h) << 16);
+}
+
+// Streaming 16-byte accesses.  Every byte is touched once per step, so loads
+// and stores use the evict-first (.cs) policy and leave L2 to the others.
+__device__ __forceinline__ uint4 ld16(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+__device__ __forceinline__ bool bf16x2_nonfinite(uint32_t w) {
+    return ((w & 0x7f80u) == 0x7f80u) || ((w & 0x7f800000u) == 0x7f800000u);
+}
+
+// Kernel flavours: plain step, clipped step (reads the norm finalize's
+// output, skips on non-finite), plain step that also reports non-finite g.
+enum Kind { kPlain = 0, kClip = 1, kReport = 2 };
+
+// ------------------------------------------------ per-element arithmetic --
+
+// m' and v' of one element (fp32).
+__device__ __forceinline__ void moments(const StepScalars& s, float g, float m0,
+                                        float v0, float& m1, float& v1) {
+    m1 = __fadd_rn(__fmul_rn(s.beta1, m0), __fmul_rn(s.omb1, g));
+    v1 = __fadd_rn(__fmul_rn(s.beta2, v0), __fmul_rn(__fmul_rn(s.omb2, g), g));
+}
+
+// upd = step_size * (m / (sqrt(v)/sbc2 + eps)) + lrwd * p
+__device__ __forceinline__ float update_of(const StepScalars& s, float m, float v,
+                                          float p0) {
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sbc2), s.eps);
+    return __fadd_rn(__fmul_rn(s.step_size, __fdiv_rn(m, den)), __fmul_rn(s.lrwd, p0));
+}
+
+// bf16 Kahan mode on two elements packed in 32-bit words (lo, hi halves).
+template <int K>
+__device__ __forceinline__ void kahan_x2(const StepScalars& s, float coef, uint32_t gw,
+                                         uint32_t& pw, uint32_t& mw, uint32_t& vw,
+                                         uint32_t& cw) {
+    float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+    if (K == kClip) {
+        g0 = __fmul_rn(g0, coef);
+        g1 = __fmul_rn(g1, coef);
+    }
+    const float p0 = bf16_lo(pw), p1 = bf16_hi(pw);
+    float ma, mb, va, vb;
+    moments(s, g0, bf16_lo(mw), bf16_lo(vw), ma, va);
+    moments(s, g1, bf16_hi(mw), bf16_hi(vw), mb, vb);
+    mw = pack_bf16x2(ma, mb);
+    vw = pack_bf16x2(va, vb);
+    // the stored (bf16) moments feed the update
+    const float y0 = __fsub_rn(bf16_lo(cw), update_of(s, bf16_lo(mw), bf16_lo(vw), p0));
+    const float y1 = __fsub_rn(bf16_hi(cw), update_of(s, bf16_hi(mw), bf16_hi(vw), p1));
+    const uint32_t pn = pack_bf16x2(__fadd_rn(p0, y0), __fadd_rn(p1, y1));
+    cw = pack_bf16x2(__fsub_rn(y0, __fsub_rn(bf16_lo(pn), p0)),
+                     __fsub_rn(y1, __fsub_rn(bf16_hi(pn), p1)));
+    pw = pn;
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_x1(const StepScalars& s, float coef, uint16_t gh,
+                                         uint16_t& ph, uint16_t& mh, uint16_t& vh,
+                                         uint16_t& ch) {
+    float g = from_bf16(gh);
+    if (K == kClip) g = __fmul_rn(g, coef);
+    const float p0 = from_bf16(ph);
+    float m1, v1;
+    moments(s, g, from_bf16(mh), from_bf16(vh), m1, v1);
+    mh = to_bf16(m1);
+    vh = to_bf16(v1);
+    const float y = __fsub_rn(from_bf16(ch), update_of(s, from_bf16(mh), from_bf16(vh), p0));
+    const uint16_t pn = to_bf16(__fadd_rn(p0, y));
+    ch = to_bf16(__fsub_rn(y, __fsub_rn(from_bf16(pn), p0)));
+    ph = pn;
+}
+
+// mixed mode on one element; returns the new master.
+template <int K>
+__device__ __forceinline__ float mixed_x1(const StepScalars& s, float coef, float g,
+                                          float p0, float& m, float& v) {
+    if (K == kClip) g = __fmul_rn(g, coef);
+    float m1, v1;
+    moments(s, g, m, v, m1, v1);
+    m = m1;
+    v = v1;
+    return __fsub_rn(p0, update_of(s, m1, v1, p0));
+}
+
+// ------------------------------------------------------- chunk walkers ----
+
+constexpr int kUnroll = 2;  // vectors per thread in flight per stream
+
+template <int K>
+__device__ __forceinline__ void kahan_vec_chunk(const TensorDev& t, int64_t off,
+                                                int64_t len, const StepScalars& s,
+                                                float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p) + off;
+    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
+    uint16_t* m = static_cast<uint16_t*>(t.m) + off;
+    uint16_t* v = static_cast<uint16_t*>(t.v) + off;
+    uint16_t* c = static_cast<uint16_t*>(t.a) + off;
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll], C[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld16(v + i * kVec);
+                C[u] = ld16(c + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(G[u].x) | bf16x2_nonfinite(G[u].y) |
+                           bf16x2_nonfinite(G[u].z) | bf16x2_nonfinite(G[u].w);
+                kahan_x2<K>(s, coef, G[u].x, P[u].x, M[u].x, V[u].x, C[u].x);
+                kahan_x2<K>(s, coef, G[u].y, P[u].y, M[u].y, V[u].y, C[u].y);
+                kahan_x2<K>(s, coef, G[u].z, P[u].z, M[u].z, V[u].z, C[u].z);
+                kahan_x2<K>(s, coef, G[u].w, P[u].w, M[u].w, V[u].w, C[u].w);
+                st16(p + i * kVec, P[u]);
+                st16(m + i * kVec, M[u]);
+                st16(v + i * kVec, V[u]);
+                st16(c + i * kVec, C[u]);
+            }
+        }
+    }
+    // ragged end of a vector body (< kVec elements)
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i], ch = c[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        kahan_x1<K>(s, coef, gh, ph, mh, vh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vh; c[i] = ch;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_elem_chunk(const TensorDev& t, int64_t off,
+                                                 int64_t len, const StepScalars& s,
+                                                 float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p) + off;
+    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
+    uint16_t* m = static_cast<uint16_t*>(t.m) + off;
+    uint16_t* v = static_cast<uint16_t*>(t.v) + off;
+    uint16_t* c = static_cast<uint16_t*>(t.a) + off;
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i], ch = c[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        kahan_x1<K>(s, coef, gh, ph, mh, vh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vh; c[i] = ch;
+    }
+}
+
+// 8 fp32 of a mixed-mode stream = two 16-byte accesses.
+struct F8 { float x[8]; };
+__device__ __forceinline__ F8 ld32(const float* p) {
+    const uint4 a = ld16(p), b = ld16(p + 4);
+    return {{__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w),
+             __uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w)}};
+}
+__device__ __forceinline__ void st32(float* p, const F8& v) {
+    st16(p, make_uint4(__float_as_uint(v.x[0]), __float_as_uint(v.x[1]),
+                       __float_as_uint(v.x[2]), __float_as_uint(v.x[3])));
+    st16(p + 4, make_uint4(__float_as_uint(v.x[4]), __float_as_uint(v.x[5]),
+                           __float_as_uint(v.x[6]), __float_as_uint(v.x[7])));
+}
+
+template <int K>
+__device__ __forceinline__ void mixed_vec_chunk(const TensorDev& t, int64_t off,
+                                                int64_t len, const StepScalars& s,
+                                                float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p) + off;
+    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
+    float* m = static_cast<float*>(t.m) + off;
+    float* v = static_cast<float*>(t.v) + off;
+    uint16_t* o = static_cast<uint16_t*>(t.a) + off;
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll];
+        F8 P[kUnroll], M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld32(p + i * kVec);
+                M[u] = ld32(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t out[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int a = 2 * j, b = 2 * j + 1;
+                    P[u].x[a] = mixed_x1<K>(s, coef, bf16_lo(gw[j]), P[u].x[a], M[u].x[a], V[u].x[a]);
+                    P[u].x[b] = mixed_x1<K>(s, coef, bf16_hi(gw[j]), P[u].x[b], M[u].x[b], V[u].x[b]);
+                    out[j] = pack_bf16x2(P[u].x[a], P[u].x[b]);
+                }
+                st32(p + i * kVec, P[u]);
+                st32(m + i * kVec, M[u]);
+                st32(v + i * kVec, V[u]);
+                st16(o + i * kVec, make_uint4(out[0], out[1], out[2], out[3]));
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), p[i], mi, vi);
+        p[i] = n; m[i] = mi; v[i] = vi; o[i] = to_bf16(n);
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void mixed_elem_chunk(const TensorDev& t, int64_t off,
+                                                 int64_t len, const StepScalars& s,
+                                                 float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p) + off;
+    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
+    float* m = static_cast<float*>(t.m) + off;
+    float* v = static_cast<float*>(t.v) + off;
+    uint16_t* o = static_cast<uint16_t*>(t.a) + off;
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), p[i], mi, vi);
+        p[i] = n; m[i] = mi; v[i] = vi; o[i] = to_bf16(n);
+    }
+}
+
+// --------------------------------------------------------------- kernels --
+
+// The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
+template <int MODE, int K>
+__global__ void __launch_bounds__(kBlock)
+adamw_update_kernel(const TensorDev* __restrict__ tensors,
+                    const ChunkDev* __restrict__ chunks,
+                    const int32_t* __restrict__ cta_begin, StepScalars s,
+                    const NormOut* __restrict__ norm, int32_t* __restrict__ report) {
+    float coef = 1.0f;
+    if (K == kClip) {
+        if (norm->nonfinite) return;  // skipped step: no writes at all
+        coef = norm->coef;
+    }
+    bool bad = false;
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        const ChunkDev ch = chunks[ci];
+        const TensorDev t = tensors[ch.tensor];
+        if (MODE == ADAMW_MODE_BF16_KAHAN) {
+            if (ch.vec) kahan_vec_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+            else kahan_elem_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+        } else {
+            if (ch.vec) mixed_vec_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+            else mixed_elem_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+        }
+    }
+    if (K == kReport) {
+        if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
+    }
+}
+
+// Sum of squares of 8 bf16 in fp32, fixed order; squares of bf16 values are
+// exact in fp32 for |g| in [2^-63, 2^64).
+__device__ __forceinline__ float sumsq8(const uint4& w) {
+    const float a0 = bf16_lo(w.x), a1 = bf16_hi(w.x), a2 = bf16_lo(w.y), a3 = bf16_hi(w.y);
+    const float a4 = bf16_lo(w.z), a5 = bf16_hi(w.z), a6 = bf16_lo(w.w), a7 = bf16_hi(w.w);
+    const float s01 = __fadd_rn(__fmul_rn(a0, a0), __fmul_rn(a1, a1));
+    const float s23 = __fadd_rn(__fmul_rn(a2, a2), __fmul_rn(a3, a3));
+    const float s45 = __fadd_rn(__fmul_rn(a4, a4), __fmul_rn(a5, a5));
+    const float s67 = __fadd_rn(__fmul_rn(a6, a6), __fmul_rn(a7, a7));
+    return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// Compensated (Kahan) fp32 accumulation: s + (-comp) carries the running sum.
+struct KahanF32 {
+    float s = 0.0f, comp = 0.0f;
+    __device__ __forceinline__ void add(float x) {
+        const float y = __fsub_rn(x, comp);
+        const float t = __fadd_rn(s, y);
+        comp = __fsub_rn(__fsub_rn(t, s), y);
+        s = t;
+    }
+    __device__ __forceinline__ double value() const { return double(s) - double(comp); }
+};
+
+// Vectors whose fp32 sum of squares is not below 2^96 (huge, inf or NaN
+// elements) are summed in fp64 one element at a time, which also sets the
+// non-finite flag.
+__device__ __forceinline__ void norm_slow8(const uint4& w, double& acc, bool& bad) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
+        bad |= !isfinite(lo) || !isfinite(hi);
+        acc += lo * lo;
+        acc += hi * hi;
+    }
+}
+
+// Deterministic fixed-tree reduction of one fp64 per thread to thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+    __shared__ double warp_part[kBlock / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+    const int lane_id = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
+    if (lane_id == 0) warp_part[warp_id] = x;
+    __syncthreads();
+    double r = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kBlock / 32; ++w) r += warp_part[w];
+    __syncthreads();
+    return r;
+}
+
+// Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
+// same partition as the update (so the result depends only on the plan).
+__global__ void __launch_bounds__(kBlock)
+norm_partial_kernel(const TensorDev* __restrict__ tensors,
+                    const ChunkDev* __restrict__ chunks,
+                    const int32_t* __restrict__ cta_begin,
+                    double* __restrict__ partial, int32_t* __restrict__ flag) {
+    KahanF32 acc;
+    double slow = 0.0;
+    bool bad = false;
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        const ChunkDev ch = chunks[ci];
+        const uint16_t* g = static_cast<const uint16_t*>(tensors[ch.tensor].g) + ch.off;
+        int64_t done = 0;
+        if (ch.vec) {
+            const int64_t nvec = ch.len / kVec;
+            constexpr int U = 4;
+            for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+                uint4 w[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = base + int64_t(u) * kBlock;
+                    if (i < nvec) w[u] = ld16(g + i * kVec);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = base + int64_t(u) * kBlock;
+                    if (i < nvec) {
+                        const float q = sumsq8(w[u]);
+                        if (q < 0x1p96f) acc.add(q);
+                        else norm_slow8(w[u], slow, bad);
+                    }
+                }
+            }
+            done = nvec * kVec;
+        }
+        for (int64_t i = done + threadIdx.x; i < ch.len; i += kBlock) {
+            const double x = from_bf16(g[i]);
+            bad |= !isfinite(x);
+            slow += x * x;
+        }
+    }
+    const double tot = block_sum(acc.value() + slow);
+    const int any = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        partial[blockIdx.x] = tot;
+        flag[blockIdx.x] = any;
+    }
+}
+
+// Stage 2: fixed-order fp64 sum of the partials, norm, clip coefficient.
+__global__ void __launch_bounds__(kBlock)
+norm_finalize_kernel(const double* __restrict__ partial, const int32_t* __restrict__ flag,
+                     int32_t n, float max_grad_norm, NormOut* __restrict__ out,
+                     double* __restrict__ user_norm, int32_t* __restrict__ user_flag) {
+    double x = 0.0;
+    bool bad = false;
+    for (int32_t i = threadIdx.x; i < n; i += kBlock) {
+        x += partial[i];
+        bad |= flag[i] != 0;
+    }
+    const double tot = block_sum(x);
+    const int any = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(tot);
+        double coef = 1.0;
+        if (max_grad_norm > 0.0f) {
+            coef = double(max_grad_norm) / (norm + 1e-6);
+            if (coef > 1.0) coef = 1.0;
+        }
+        out->norm = norm;
+        out->coef = float(coef);
+        out->nonfinite = any;
+        if (user_norm) *user_norm = norm;
+        if (user_flag) *user_flag = any;
+    }
+}
+
+// Plain 16-byte streaming copy (HBM ceiling probe).
+__global__ void __launch_bounds__(kBlock)
+copy_probe_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n) {
+    constexpr int U = 4;
+    const int64_t stride = int64_t(gridDim.x) * kBlock;
+    for (int64_t base = int64_t(blockIdx.x) * kBlock + threadIdx.x; base < n; base += stride * U) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * stride < n) r[u] = ld16(src + base + u * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * stride < n) st16(dst + base + u * stride, r[u]);
+    }
+}
+
+// ------------------------------------------------------------ host side ----
+
+struct DeviceInfo {
+    int sms = 0;
+    int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};
+    int occ_norm = 0;
+    int occ_copy = 0;
+};
+
+std::mutex g_dev_mu;
+std::vector<DeviceInfo> g_dev;
+
+bool cuda_ok(cudaError_t e, const char* where) {
+    if (e == cudaSuccess) return true;
+    set_cuda_error(where, cudaGetErrorString(e));
+    return false;
+}
+
+template <int MODE, int K>
+const void* update_fn() { return reinterpret_cast<const void*>(&adamw_update_kernel<MODE, K>); }
+
+int device_info(int dev, DeviceInfo* out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev >= int(g_dev.size())) g_dev.resize(dev + 1);
+    DeviceInfo& d = g_dev[dev];
+    if (d.sms == 0) {
+        int sms = 0;
+        if (!cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                     "cudaDeviceGetAttribute"))
+            return ADAMW_ERR_CUDA;
+        const void* fns[2][3] = {
+            {update_fn<0, kPlain>(), update_fn<0, kClip>(), update_fn<0, kReport>()},
+            {update_fn<1, kPlain>(), update_fn<1, kClip>(), update_fn<1, kReport>()}};
+        for (int m = 0; m < 2; ++m)
+            for (int k = 0; k < 3; ++k)
+                if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[m][k], fns[m][k],
+                                                                           kBlock, 0),
+                             "occupancy"))
+                    return ADAMW_ERR_CUDA;
+        if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &d.occ_norm, norm_partial_kernel, kBlock, 0), "occupancy") ||
+            !cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &d.occ_copy, copy_probe_kernel, kBlock, 0), "occupancy"))
+            return ADAMW_ERR_CUDA;
+        d.sms = sms;
+    }
+    *out = d;
+    return ADAMW_OK;
+}
+
+// Makes the plan's device current for the scope, restoring the caller's.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct adamw_plan {
+    int device = 0;
+    int32_t mode = 0;
+    int32_t flags = 0;
+    int32_t n_tensors = 0;
+    int64_t total = 0;
+    int64_t scalar_elems = 0;
+    int32_t grid = 0;
+    int64_t n_chunks = 0;
+    void* block = nullptr;  // one device allocation holding everything below
+    TensorDev* tensors = nullptr;
+    ChunkDev* chunks = nullptr;
+    int32_t* cta_begin = nullptr;
+    double* partial = nullptr;
+    int32_t* flag = nullptr;
+    NormOut* norm = nullptr;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <int MODE, int K>
+cudaError_t launch_update(const adamw_plan* P, const StepScalars& s, int32_t* report,
+                          cudaStream_t st) {
+    adamw_update_kernel<MODE, K><<<P->grid, kBlock, 0, st>>>(P->tensors, P->chunks, P->cta_begin,
+                                                             s, P->norm, report);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& s,
+                              int32_t* report, cudaStream_t st) {
+    if (P->mode == ADAMW_MODE_BF16_KAHAN) {
+        if (kind == kPlain) return launch_update<0, kPlain>(P, s, report, st);
+        if (kind == kClip) return launch_update<0, kClip>(P, s, report, st);
+        return launch_update<0, kReport>(P, s, report, st);
+    }
+    if (kind == kPlain) return launch_update<1, kPlain>(P, s, report, st);
+    if (kind == kClip) return launch_update<1, kClip>(P, s, report, st);
+    return launch_update<1, kReport>(P, s, report, st);
+}
+
+cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
+                        int32_t* user_flag, cudaStream_t st) {
+    norm_partial_kernel<<<P->grid, kBlock, 0, st>>>(P->tensors, P->chunks, P->cta_begin,
+                                                    P->partial, P->flag);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    norm_finalize_kernel<<<1, kBlock, 0, st>>>(P->partial, P->flag, P->grid, max_grad_norm,
+                                               P->norm, user_norm, user_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_tensors,
+                                 int32_t mode, int32_t flags, adamw_plan_t* out) {
+    if (!out) return ADAMW_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (flags & ~ADAMW_PLAN_NORM) return ADAMW_ERR_INVALID_ARG;
+    int rc = validate_table(host_table, n_tensors, mode);
+    if (rc != ADAMW_OK) return rc;
+
+    int dev = 0;
+    if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return ADAMW_ERR_CUDA;
+    DeviceInfo di;
+    rc = device_info(dev, &di);
+    if (rc != ADAMW_OK) return rc;
+
+    int occ = di.occ[mode][kPlain];
+    for (int k = 0; k < 3; ++k) occ = occ < di.occ[mode][k] ? occ : di.occ[mode][k];
+    if (flags & ADAMW_PLAN_NORM) occ = occ < di.occ_norm ? occ : di.occ_norm;
+    if (occ < 1) occ = 1;
+
+    int64_t total = 0;
+    for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;
+    const int32_t grid = choose_grid(total, di.sms * occ);
+
+    Partition part;
+    if (grid > 0) {
+        rc = build_partition(host_table, n_tensors, mode, grid, &part);
+        if (rc != ADAMW_OK) return rc;
+    }
+
+    adamw_plan* P = new adamw_plan();
+    P->device = dev;
+    P->mode = mode;
+    P->flags = flags;
+    P->n_tensors = n_tensors;
+    P->total = total;
+    P->scalar_elems = part.scalar_elems;
+    P->grid = grid;
+    P->n_chunks = int64_t(part.chunks.size());
+
+    // Layout of the single allocation.
+    size_t off = 0;
+    const size_t o_t = off; off = align_up(off + sizeof(TensorDev) * size_t(n_tensors), 256);
+    const size_t o_c = off; off = align_up(off + sizeof(ChunkDev) * part.chunks.size(), 256);
+    const size_t o_b = off; off = align_up(off + sizeof(int32_t) * (size_t(grid) + 1), 256);
+    const size_t o_p = off; off = align_up(off + sizeof(double) * size_t(grid), 256);
+    const size_t o_f = off; off = align_up(off + sizeof(int32_t) * size_t(grid), 256);
+    const size_t o_n = off; off = align_up(off + sizeof(NormOut), 256);
+
+    if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
+        delete P;
+        return ADAMW_ERR_CUDA;
+    }
+    char* b = static_cast<char*>(P->block);
+    P->tensors = reinterpret_cast<TensorDev*>(b + o_t);
+    P->chunks = reinterpret_cast<ChunkDev*>(b + o_c);
+    P->cta_begin = reinterpret_cast<int32_t*>(b + o_b);
+    P->partial = reinterpret_cast<double*>(b + o_p);
+    P->flag = reinterpret_cast<int32_t*>(b + o_f);
+    P->norm = reinterpret_cast<NormOut*>(b + o_n);
+
+    bool ok = cuda_ok(cudaMemset(P->block, 0, off), "cudaMemset");
+    if (ok && n_tensors > 0)
+        ok = cuda_ok(cudaMemcpy(P->tensors, host_table, sizeof(TensorDev) * size_t(n_tensors),
+                                cudaMemcpyHostToDevice), "cudaMemcpy(table)");
+    if (ok && !part.chunks.empty())
+        ok = cuda_ok(cudaMemcpy(P->chunks, part.chunks.data(),
+                                sizeof(ChunkDev) * part.chunks.size(), cudaMemcpyHostToDevice),
+                     "cudaMemcpy(chunks)");
+    if (ok && grid > 0)
+        ok = cuda_ok(cudaMemcpy(P->cta_begin, part.cta_begin.data(),
+                                sizeof(int32_t) * (size_t(grid) + 1), cudaMemcpyHostToDevice),
+                     "cudaMemcpy(cta_begin)");
+    if (!ok) {
+        cudaFree(P->block);
+        delete P;
+        return ADAMW_ERR_CUDA;
+    }
+    *out = P;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t step,
+                          double* d_grad_norm, int32_t* d_nonfinite, adamw_stream_t stream) {
+    if (!plan) return ADAMW_ERR_INVALID_ARG;
+    StepScalars s;
+    int rc = make_scalars(hp, step, &s);
+    if (rc != ADAMW_OK) return rc;
+    const bool clip = hp->max_grad_norm > 0.0f;
+    const bool need_norm = clip || d_grad_norm != nullptr;
+    if (need_norm && !(plan->flags & ADAMW_PLAN_NORM)) return ADAMW_ERR_NO_NORM;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) {
+        set_cuda_error("cudaSetDevice", cudaGetErrorString(cudaGetLastError()));
+        return ADAMW_ERR_CUDA;
+    }
+
+    if (plan->grid == 0) {  // empty list: nothing to update, norm is 0
+        if (d_grad_norm && !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
+            return ADAMW_ERR_CUDA;
+        if (d_nonfinite && !cuda_ok(cudaMemsetAsync(d_nonfinite, 0, sizeof(int32_t), st), "memset"))
+            return ADAMW_ERR_CUDA;
+        return ADAMW_OK;
+    }
+
+    int kind = kPlain;
+    int32_t* report = nullptr;
+    if (need_norm) {
+        if (!cuda_ok(launch_norm(plan, clip ? hp->max_grad_norm : 0.0f, d_grad_norm, d_nonfinite, st),
+                     "norm launch"))
+            return ADAMW_ERR_CUDA;
+        kind = clip ? kClip : kPlain;
+    } else if (d_nonfinite) {
+        if (!cuda_ok(cudaMemsetAsync(d_nonfinite, 0, sizeof(int32_t), st), "cudaMemsetAsync"))
+            return ADAMW_ERR_CUDA;
+        kind = kReport;
+        report = d_nonfinite;
+    }
+    if (!cuda_ok(launch_update_any(plan, kind, s, report, st), "update launch"))
+        return ADAMW_ERR_CUDA;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm, int32_t* d_nonfinite,
+                               adamw_stream_t stream) {
+    if (!plan) return ADAMW_ERR_INVALID_ARG;
+    if (!(plan->flags & ADAMW_PLAN_NORM)) return ADAMW_ERR_NO_NORM;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) {
+        set_cuda_error("cudaSetDevice", cudaGetErrorString(cudaGetLastError()));
+        return ADAMW_ERR_CUDA;
+    }
+    if (plan->grid == 0) {
+        if (d_grad_norm && !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
+            return ADAMW_ERR_CUDA;
+        if (d_nonfinite && !cuda_ok(cudaMemsetAsync(d_nonfinite, 0, sizeof(int32_t), st), "memset"))
+            return ADAMW_ERR_CUDA;
+        return ADAMW_OK;
+    }
+    if (!cuda_ok(launch_norm(plan, 0.0f, d_grad_norm, d_nonfinite, st), "norm launch"))
+        return ADAMW_ERR_CUDA;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_plan_destroy(adamw_plan_t plan) {
+    if (!plan) return ADAMW_OK;
+    int rc = ADAMW_OK;
+    {
+        DeviceGuard guard(plan->device);
+        if (plan->block) {
+            if (!cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) rc = ADAMW_ERR_CUDA;
+            if (!cuda_ok(cudaFree(plan->block), "cudaFree")) rc = ADAMW_ERR_CUDA;
+        }
+    }
+    delete plan;
+    return rc;
+}
+
+extern "C" int adamw_plan_get_info(adamw_plan_t plan, adamw_plan_info_t* out) {
+    if (!plan || !out) return ADAMW_ERR_INVALID_ARG;
+    out->mode = plan->mode;
+    out->n_tensors = plan->n_tensors;
+    out->total_elems = plan->total;
+    out->grid = plan->grid;
+    out->block = kBlock;
+    out->n_chunks = plan->n_chunks;
+    out->scalar_elems = plan->scalar_elems;
+    out->device = plan->device;
+    out->has_norm = (plan->flags & ADAMW_PLAN_NORM) ? 1 : 0;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_copy_probe(void* dst, const void* src, int64_t bytes, adamw_stream_t stream) {
+    if (bytes < 0 || (bytes > 0 && (!dst || !src))) return ADAMW_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) % 16 || bytes % 16)
+        return ADAMW_ERR_MISALIGNED;
+    if (bytes == 0) return ADAMW_OK;
+    int dev = 0;
+    if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return ADAMW_ERR_CUDA;
+    DeviceInfo di;
+    int rc = device_info(dev, &di);
+    if (rc != ADAMW_OK) return rc;
+    const int64_t n = bytes / 16;
+    int64_t grid = int64_t(di.sms) * (di.occ_copy > 0 ? di.occ_copy : 1);
+    const int64_t need = (n + kBlock - 1) / kBlock;
+    if (grid > need) grid = need;
+    copy_probe_kernel<<<int(grid), kBlock, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(dst), static_cast<const uint4*>(src), n);
+    return cuda_ok(cudaGetLastError(), "copy launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
+}

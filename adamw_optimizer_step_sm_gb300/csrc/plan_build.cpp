@@ -1,0 +1,232 @@
+// plan_build.cpp -- host-side planning for the multi-tensor AdamW step:
+// argument validation, the per-step fp32 scalars, and the partition of a
+// tensor list into per-CTA chunks.  Pure host code; needs no GPU.
+//
+// The pages name the multi-tensor optimizer only ("Distributed optimizer
+// support for BERT", NeMo PR #5305, "Usage": fused_adam / distributed_fused_adam
+// update a whole model's parameter list in fused launches); this partition is
+// this library's own design: the flattened element space is cut into `grid`
+// nearly equal contiguous ranges, one per persistent CTA, so that every CTA
+// streams the same number of bytes whatever the tensor sizes.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "adamw_internal.h"
+
+namespace adamw {
+
+namespace {
+
+thread_local std::string g_cuda_error;
+
+bool aligned(const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Elements [0, head) take the element path so that every base is 16-byte
+// aligned at `head`; -1 when no head < kVec does that.
+int vector_head(const adamw_tensor_t& t, int32_t mode) {
+    const uintptr_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    const void* ptrs[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
+    const uintptr_t es[5] = {wide, 2, wide, wide, 2};
+    for (int h = 0; h < kVec; ++h) {
+        bool ok = true;
+        for (int s = 0; s < 5 && ok; ++s)
+            ok = ((reinterpret_cast<uintptr_t>(ptrs[s]) + h * es[s]) % 16) == 0;
+        if (ok) return h;
+    }
+    return -1;
+}
+
+}  // namespace
+
+void set_cuda_error(const char* where, const char* what) {
+    g_cuda_error = std::string(where) + ": " + what;
+}
+
+const char* last_cuda_error() { return g_cuda_error.c_str(); }
+
+int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode) {
+    if (n < 0) return ADAMW_ERR_INVALID_ARG;
+    if (n > 0 && !table) return ADAMW_ERR_INVALID_ARG;
+    if (mode != ADAMW_MODE_BF16_KAHAN && mode != ADAMW_MODE_MIXED_FP32_MASTER)
+        return ADAMW_ERR_INVALID_ARG;
+    const uintptr_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    for (int32_t k = 0; k < n; ++k) {
+        const adamw_tensor_t& t = table[k];
+        if (t.numel < 0) return ADAMW_ERR_INVALID_ARG;
+        if (t.numel == 0) continue;
+        if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq || !t.aux)
+            return ADAMW_ERR_INVALID_ARG;
+        if (!aligned(t.param, wide) || !aligned(t.exp_avg, wide) ||
+            !aligned(t.exp_avg_sq, wide) || !aligned(t.grad, 2) ||
+            !aligned(t.aux, 2))
+            return ADAMW_ERR_MISALIGNED;
+    }
+    return ADAMW_OK;
+}
+
+int validate_hparams(const adamw_hparams_t* hp, int64_t step) {
+    if (!hp || step < 1) return ADAMW_ERR_INVALID_ARG;
+    const float f[6] = {hp->lr, hp->beta1, hp->beta2, hp->eps,
+                        hp->weight_decay, hp->max_grad_norm};
+    for (float x : f)
+        if (!std::isfinite(x)) return ADAMW_ERR_INVALID_ARG;
+    if (hp->lr < 0.0f || hp->eps <= 0.0f || hp->weight_decay < 0.0f)
+        return ADAMW_ERR_INVALID_ARG;
+    if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f)) return ADAMW_ERR_INVALID_ARG;
+    if (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f)) return ADAMW_ERR_INVALID_ARG;
+    return ADAMW_OK;
+}
+
+// Bias corrections of Kingma & Ba and the decoupled decay factor of
+// Loshchilov & Hutter, in fp64 from the fp32 hyperparameters, each rounded
+// once to fp32.
+int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out) {
+    int rc = validate_hparams(hp, step);
+    if (rc != ADAMW_OK) return rc;
+    const double b1 = hp->beta1, b2 = hp->beta2;
+    const double bc1 = 1.0 - std::pow(b1, double(step));
+    const double bc2 = 1.0 - std::pow(b2, double(step));
+    out->beta1 = hp->beta1;
+    out->beta2 = hp->beta2;
+    out->omb1 = float(1.0 - b1);
+    out->omb2 = float(1.0 - b2);
+    out->step_size = float(double(hp->lr) / bc1);
+    out->sbc2 = float(std::sqrt(bc2));
+    out->eps = hp->eps;
+    out->lrwd = float(double(hp->lr) * double(hp->weight_decay));
+    out->max_grad_norm = hp->max_grad_norm;
+    return ADAMW_OK;
+}
+
+int32_t choose_grid(int64_t total, int32_t max_grid) {
+    if (total <= 0) return 0;
+    if (max_grid < 1) max_grid = 1;
+    int64_t want = (total + kMinElemsPerCta - 1) / kMinElemsPerCta;
+    return int32_t(want < max_grid ? want : max_grid);
+}
+
+int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
+                    int32_t grid, Partition* out) {
+    int rc = validate_table(table, n, mode);
+    if (rc != ADAMW_OK) return rc;
+    if (!out || grid < 0) return ADAMW_ERR_INVALID_ARG;
+    Partition& P = *out;
+    P = Partition();
+    for (int32_t k = 0; k < n; ++k) P.total += table[k].numel;
+    if (P.total > 0 && grid == 0) return ADAMW_ERR_INVALID_ARG;
+
+    // Segments: per tensor an optional element-path head, then a vector body
+    // (or the whole tensor on the element path when no head aligns it).
+    struct Seg { int32_t k; int32_t vec; int64_t off, len; };
+    std::vector<Seg> segs;
+    for (int32_t k = 0; k < n; ++k) {
+        const int64_t len = table[k].numel;
+        if (len == 0) continue;
+        int h = vector_head(table[k], mode);
+        if (h < 0 || h >= len) {
+            segs.push_back({k, 0, 0, len});
+            P.scalar_elems += len;
+        } else {
+            if (h > 0) {
+                segs.push_back({k, 0, 0, h});
+                P.scalar_elems += h;
+            }
+            segs.push_back({k, 1, h, len - h});
+        }
+    }
+
+    P.cta_begin.assign(size_t(grid) + 1, 0);
+    if (P.total == 0) return ADAMW_OK;
+
+    // Even split of the flattened element space; cuts inside a vector body
+    // fall on multiples of kVec from the body's start so every chunk of it
+    // starts 16-byte aligned.
+    const int64_t target = ((P.total + grid - 1) / grid + kVec - 1) / kVec * kVec;
+    int32_t cta = 0;
+    int64_t filled = 0;
+    for (const Seg& s : segs) {
+        int64_t pos = 0;
+        while (pos < s.len) {
+            if (filled >= target && cta < grid - 1) {
+                ++cta;
+                filled = 0;
+            }
+            int64_t take = s.len - pos;
+            if (cta < grid - 1 && take > target - filled) {
+                int64_t cap = target - filled;
+                take = s.vec ? (cap + kVec - 1) / kVec * kVec : cap;
+                if (take > s.len - pos) take = s.len - pos;
+            }
+            P.chunks.push_back({s.k, s.vec, s.off + pos, take});
+            P.chunk_cta.push_back(cta);
+            pos += take;
+            filled += take;
+        }
+    }
+    // cta_begin[b] = first chunk of CTA b (chunks are emitted in CTA order).
+    size_t c = 0;
+    for (int32_t b = 0; b <= grid; ++b) {
+        while (c < P.chunks.size() && P.chunk_cta[c] < b) ++c;
+        P.cta_begin[b] = int32_t(c);
+    }
+    return ADAMW_OK;
+}
+
+}  // namespace adamw
+
+// ------------------------------------------------------- host-only ABI ----
+
+extern "C" int adamw_plan_chunks(const adamw_tensor_t* host_table,
+                                 int32_t n_tensors, int32_t mode, int32_t grid,
+                                 adamw_chunk_t* out, int64_t cap,
+                                 int64_t* n_out) {
+    if (!n_out || cap < 0 || (cap > 0 && !out) || grid < 1)
+        return ADAMW_ERR_INVALID_ARG;
+    adamw::Partition P;
+    int rc = adamw::build_partition(host_table, n_tensors, mode, grid, &P);
+    if (rc != ADAMW_OK) return rc;
+    *n_out = int64_t(P.chunks.size());
+    if (int64_t(P.chunks.size()) > cap) return ADAMW_ERR_TOO_LARGE;
+    for (size_t i = 0; i < P.chunks.size(); ++i) {
+        out[i].tensor = P.chunks[i].tensor;
+        out[i].vec = P.chunks[i].vec;
+        out[i].offset = P.chunks[i].off;
+        out[i].len = P.chunks[i].len;
+        out[i].cta = P.chunk_cta[i];
+        out[i].pad_ = 0;
+    }
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step,
+                                  float out5[5]) {
+    if (!out5) return ADAMW_ERR_INVALID_ARG;
+    adamw::StepScalars s;
+    int rc = adamw::make_scalars(hp, step, &s);
+    if (rc != ADAMW_OK) return rc;
+    out5[0] = s.step_size;
+    out5[1] = s.sbc2;
+    out5[2] = s.omb1;
+    out5[3] = s.omb2;
+    out5[4] = s.lrwd;
+    return ADAMW_OK;
+}
+
+extern "C" const char* adamw_status_string(int status) {
+    static thread_local std::string buf;
+    switch (status) {
+        case ADAMW_OK: return "ok";
+        case ADAMW_ERR_INVALID_ARG: return "invalid argument";
+        case ADAMW_ERR_MISALIGNED: return "buffer not aligned to its element size";
+        case ADAMW_ERR_NO_NORM: return "clipping or norm asked of a plan made without ADAMW_PLAN_NORM";
+        case ADAMW_ERR_TOO_LARGE: return "size exceeds a documented limit";
+        case ADAMW_ERR_CUDA:
+            buf = std::string("CUDA error: ") + adamw::last_cuda_error();
+            return buf.c_str();
+        default: return "unknown status";
+    }
+}

@@ -180,9 +180,13 @@ class State:
         return [flat[o:o + n] for o, n in zip(self.offsets, self.workload.numels)]
 
 
-def make_state(w: Workload, device="cpu") -> State:
-    """Initial optimizer state: params drawn, moments and aux zero."""
-    offs, length = tensor_offsets(w.numels)
+def make_state(w: Workload, device="cpu", align_elems: int = 8, skew: int = 0) -> State:
+    """Initial optimizer state: params drawn, moments and aux zero.  Tensors sit
+    in one flat buffer per kind at offsets rounded to ``align_elems`` elements,
+    the first one ``skew`` elements in (ragged layouts use 1 and a skew)."""
+    offs, length = tensor_offsets(w.numels, align_elems)
+    offs = [o + skew for o in offs]
+    length += skew
     p32 = torch.zeros(length, dtype=torch.float32, device=device)
     gen = _gen(device, w.seed, 1)
     for spec, o in zip(w.tensors, offs):
@@ -200,10 +204,14 @@ def make_state(w: Workload, device="cpu") -> State:
     return State(w, param, z(wide), z(wide), z(torch.bfloat16), offs)
 
 
-def make_grad(w: Workload, step: int, device="cpu", length: int | None = None) -> torch.Tensor:
-    """The flat bf16 gradient of ``step`` (1-based), drawn from (seed, step)."""
-    offs, full = tensor_offsets(w.numels)
-    length = full if length is None else length
+def make_grad(w: Workload, step: int, device="cpu", offsets: list[int] | None = None,
+              length: int | None = None) -> torch.Tensor:
+    """The flat bf16 gradient of ``step`` (1-based), drawn from (seed, step),
+    laid out like ``make_state`` (default layout, or the given offsets)."""
+    if offsets is None:
+        offsets, length = tensor_offsets(w.numels)
+    elif length is None:
+        length = max((o + n for o, n in zip(offsets, w.numels)), default=0)
     gen = _gen(device, w.seed, 2, step)
     g = _draw_normal(length, w.g_std, gen, device)
     if w.heavy_tail:
@@ -215,15 +223,14 @@ def make_grad(w: Workload, step: int, device="cpu", length: int | None = None) -
             del u
     gb = g.to(torch.bfloat16)
     del g
-    # zero the alignment padding between tensors so it is never "data"
-    prev_end = 0
-    for o, n in zip(offs, w.numels):
-        if o > prev_end:
-            gb[prev_end:o] = 0
-        prev_end = o + n
+    # zero what lies between tensors so it is never "data"
+    mask = torch.ones(length, dtype=torch.bool, device=device)
+    for o, n in zip(offsets, w.numels):
+        mask[o:o + n] = False
+    gb[mask] = 0
     if w.inf_at is not None and w.inf_at[0] == step:
         _, k, e = w.inf_at
-        gb[offs[k] + e] = float("inf")
+        gb[offsets[k] + e] = float("inf")
     return gb
 
 
@@ -235,3 +242,16 @@ def bf16_bits(t: torch.Tensor):
 
 def f32_array(t: torch.Tensor):
     return t.detach().contiguous().cpu().numpy()
+
+
+def truncated(w: Workload, n_elems: int) -> Workload:
+    """The first ``n_elems`` elements of a workload's tensor list (the last
+    tensor cut short), same recipe: a bounded sample of the same workload."""
+    out, left = [], n_elems
+    for t in w.tensors:
+        if left <= 0:
+            break
+        out.append(TensorSpec(t.name, min(t.numel, left), t.kind))
+        left -= out[-1].numel
+    from dataclasses import replace
+    return replace(w, name=f"{w.name}[:{n_elems}]", tensors=tuple(out), inf_at=None)

@@ -1,0 +1,430 @@
+"""Benchmark of the AdamW optimizer step on one or more GPUs of one node.
+
+One "step" is one optimizer step over the whole tensor list of the workload
+(default: the OPT-1.3b-shaped list, 388 tensors, 1,315,758,080 parameters,
+pure-bf16 AnyPrecisionAdamW with Kahan compensation: 18 bytes moved per
+parameter).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on host cores
+
+With N > 1 (torchrun) every rank runs an independent replica of the same
+workload on its own GPU (the step has no data exchange); value = parameters
+updated by all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from adamw_optimizer_step_sm_gb300 import adamw_sm as A  # noqa: E402
+from adamw_optimizer_step_sm_gb300 import workloads as W  # noqa: E402
+
+METRIC = "params updated/s & achieved HBM GB/s (% of peak), OPT-1.3b-shaped bf16 Kahan step"
+UNIT = "params/s"
+DEFAULT_WORKLOAD = "opt1.3b_bf16_kahan"
+CPU_SAMPLE_ELEMS = 1 << 27
+
+
+def bytes_per_param(w: W.Workload) -> int:
+    """Algorithmic HBM bytes per parameter per step.
+    bf16 Kahan: read p, g, m, v, c (10) + write p, m, v, c (8) = 18.
+    mixed: read master, m, v (12) + g (2), write master, m, v (12) + p_out (2)
+    = 28; with clipping the norm pass reads g once more: 30."""
+    if w.mode == W.MODE_BF16_KAHAN:
+        return 18 + (2 if w.max_grad_norm > 0 else 0)
+    return 28 + (2 if w.max_grad_norm > 0 else 0)
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "adamw_optimizer_step_sm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the update kernel from a committed ncu summary,
+    or None when none exists or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        busy = [x for x in sm if x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int):
+    """The oracle as it stands on host cores, over the first n_elems elements
+    of the workload; returns (params/s, seconds, threads)."""
+    import numpy as np
+    import oracle as O
+    o = O.load()
+    ws = W.truncated(w, n_elems)
+    st = W.make_state(ws, "cpu")
+    to16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    wide = to16 if ws.mode == W.MODE_BF16_KAHAN else (lambda t: t.numpy())
+    p, m, v, a = wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux)
+    hp = O.hparams(**ws.hparams())
+    grads = [to16(W.make_grad(ws, k + 1, "cpu")) for k in range(min(steps, 2))]
+    # split the elementwise work into contiguous pieces, one per thread
+    pieces = []
+    for off, n in zip(st.offsets, ws.numels):
+        step = max(1, -(-n // threads))
+        for s in range(0, n, step):
+            pieces.append((off + s, min(n - s, step)))
+    clip = ws.max_grad_norm > 0
+    t0 = time.perf_counter()
+    for k in range(steps):
+        g = grads[k % len(grads)]
+        coef = 1.0
+        if clip:
+            sumsq, bad = o.grad_sumsq([g[off:off + n] for off, n in zip(st.offsets, ws.numels)])
+            coef, _ = o.clip_coef(sumsq, ws.max_grad_norm)
+
+        def one(pc, t=k + 1):
+            s, n = pc
+            sl = slice(s, s + n)
+            if ws.mode == W.MODE_BF16_KAHAN:
+                o.bf16_kahan(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
+            else:
+                o.mixed(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, pieces))
+    dt = time.perf_counter() - t0
+    return ws.total * steps / dt, dt, threads
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Largest x over ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# -------------------------------------------------------------- GPU arm --
+
+def copy_ceiling(device, nbytes: int = 4 << 30, reps: int = 5) -> dict:
+    """Device-to-device copy bandwidth: cudaMemcpyAsync and the library's
+    16-byte copy kernel (bytes = read + write)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    for name, fn in (("memcpy", lambda: dst.copy_(src)),
+                     ("kernel", lambda: A.adamw_copy_probe(dst.data_ptr(), src.data_ptr(), nbytes,
+                                                           stream.cuda_stream))):
+        fn()
+        torch.cuda.synchronize(device)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        out[name] = 2 * nbytes / best / 1e9
+    del src, dst
+    torch.cuda.empty_cache()
+    out["ceiling"] = max(out["memcpy"], out["kernel"])
+    return out
+
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    A.load()
+    w = W.WORKLOADS[args.workload]
+    from dataclasses import replace
+    w_bench = replace(w, inf_at=None)   # timing steps carry no injected inf
+    clip = w.max_grad_norm > 0
+    bpp = bytes_per_param(w)
+    N = w.total
+
+    ceiling = copy_ceiling(device) if not args.no_ceiling else None
+
+    st = W.make_state(w_bench, device)
+    n_grad = max(1, min(args.steps + args.warmup, args.grad_buffers))
+    grads = [W.make_grad(w_bench, k + 1, device) for k in range(n_grad)]
+    v = st.views
+    plans = [A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode,
+                    norm=clip) for g in grads]
+    hp = A.hparams(**w.hparams())
+    stream = torch.cuda.current_stream(device)
+    norm = torch.zeros(1, dtype=torch.float64, device=device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    launches_per_step = 3 if clip else 1
+
+    t = 0
+    for i in range(args.warmup):
+        plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None)
+        t += 1
+    torch.cuda.synchronize(device)
+    barrier(world)
+
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize(device)
+    barrier(world)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        plans[(args.warmup + i) % n_grad].step(hp, t + 1, grad_norm=norm if clip else None)
+        ev[i][1].record(stream)
+        t += 1
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+
+    per_step = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    span = ev[0][0].elapsed_time(ev[-1][1]) / 1e3
+    span_max = reduce_max(span, world, device)
+    ms_per_step = span_max / args.steps * 1e3
+    value = world * N * args.steps / span_max
+    avg_launch = sum(per_step) / len(per_step)
+    achieved = bpp * N / avg_launch / 1e9
+
+    # end to end through the public API: grads copied in from pinned host
+    # memory every step, the step, and the non-finite flag read back
+    e2e = None
+    if not args.no_e2e:
+        host_g = torch.empty(grads[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+        host_g.copy_(grads[0])
+        host_flag = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        k_e2e = max(1, min(args.steps, 10))
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(k_e2e):
+            grads[0].copy_(host_g, non_blocking=True)
+            plans[0].step(hp, t + 1, grad_norm=norm if clip else None, nonfinite=flag)
+            host_flag.copy_(flag, non_blocking=True)
+            stream.synchronize()
+            if int(host_flag.item()) and clip:
+                continue
+            t += 1
+        e1.record(stream)
+        e1.synchronize()
+        e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, world, device)
+        e2e = {"value": world * N * k_e2e / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": int(grads[0].numel() * 2), "d2h_bytes_per_step": 4,
+               "ms_per_step": e2e_s / k_e2e * 1e3}
+        del host_g
+
+    peaks = load_peaks()
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": w.name, "description": w.description, "n_params": N,
+            "n_tensors": w.n_tensors, "mode": "bf16_kahan" if w.mode == 0 else "mixed_fp32_master",
+            "storage": "bf16" if w.mode == 0 else "fp32 master/m/v, bf16 g and param out",
+            "clip": clip, "bytes_per_param": bpp, "hparams": w.hparams(),
+            "l2": f"inputs larger than L2 ({bpp * N / 1e9:.2f} GB moved per step)"
+                  if bpp * N > 129e6 else "inputs fit in L2 (no flush)",
+            "grads": f"{n_grad} resident grad buffers drawn before timing, cycled",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "traffic": recorded_traffic(w.name),
+                     "kernel": "adamw_update_kernel" if not clip else "whole step (norm + update)",
+                     "algorithmic_bytes_per_launch": bpp * N,
+                     "avg_launch_ms": avg_launch * 1e3},
+        "copy_ceiling_gbs": ceiling,
+        "frac_of_copy_ceiling": (achieved / ceiling["ceiling"]) if ceiling else None,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        thr = host_threads()
+        val, secs, used = oracle_throughput(w, min(CPU_SAMPLE_ELEMS, N), 1, thr)
+        out["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": used, "kind": "oracle",
+                               "sample": f"first {min(CPU_SAMPLE_ELEMS, N)} elements of the "
+                                         f"{w.name} list, 1 step, {secs:.2f} s"}
+    for p in plans:
+        p.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on host cores, each step a bounded sample
+    (the first elements of the same list)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    thr = host_threads()
+    n = min(args.ref_sample, w.total)
+    oracle_throughput(w, min(n, 1 << 20), max(1, min(args.warmup, 3)), thr)  # warm-up
+    val, secs, used = oracle_throughput(w, n, args.steps, thr)
+    out = {
+        "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": w.name, "n_params": w.total, "n_tensors": w.n_tensors,
+                   "bytes_per_param": bytes_per_param(w), "sample_elems_per_step": n},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"first {n} elements of the {w.name} list per step"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--grad-buffers", type=int, default=4)
+    ap.add_argument("--ref-sample", type=int, default=1 << 25)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ceiling", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

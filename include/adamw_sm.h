@@ -1,0 +1,194 @@
+/*
+ * adamw_sm.h -- C ABI of the GB300 (sm_103a) AdamW optimizer-step library.
+ *
+ * One optimizer step of decoupled-weight-decay Adam with bias correction over
+ * a list of parameter tensors, in one of two storage modes:
+ *
+ *   ADAMW_MODE_BF16_KAHAN  pure-bf16 AnyPrecisionAdamW with Kahan summation:
+ *       bf16 param p, grad g, exp_avg m, exp_avg_sq v and compensation c.
+ *       ("[pure bf16 training] w/ AnyPrecisionAdamW and Kahan summation",
+ *       transformers PR #21312, "Train from scratch" run recipe: optim
+ *       adamw_anyprecision, use_kahan_summation=true, bf16 momentum, variance
+ *       and compensation buffers; memory breakdown "bf16 pure" = 10 B/param.)
+ *
+ *   ADAMW_MODE_MIXED_FP32_MASTER  the per-shard update of a distributed
+ *       (ZeRO-style) Adam: fp32 master weights, fp32 m and v, bf16 grad in,
+ *       bf16 param out.  ("Distributed optimizer support for BERT", NeMo PR
+ *       #5305, "Usage": distributed_fused_adam; memory breakdown "bf16 mixed"
+ *       of the transformers PR = 16 B/param.)
+ *
+ * Arithmetic (identical in both modes up to storage; fp32, one IEEE
+ * round-to-nearest per operation, no fused multiply-add):
+ *   host, fp64 rounded once to fp32:  step_size = lr / (1 - beta1^t),
+ *       sbc2 = sqrt(1 - beta2^t), omb1 = 1 - beta1, omb2 = 1 - beta2,
+ *       lrwd = lr * weight_decay
+ *   per element:  g *= coef (only when clipping)
+ *       m' = beta1*m + omb1*g ;  v' = beta2*v + (omb2*g)*g
+ *       (bf16 mode: m', v' rounded to bf16 and used as stored)
+ *       den = sqrt(v')/sbc2 + eps ;  upd = step_size*(m'/den) + lrwd*p
+ *   bf16 mode:  y = c - upd ; p' = bf16(p + y) ; c' = bf16(y - (p' - p))
+ *   mixed mode: master' = master - upd ; p_out = bf16(master')
+ *   clipping:   norm = sqrt(sum g^2) over every tensor of the plan;
+ *       coef = min(1, max_grad_norm / (norm + 1e-6)); a non-finite gradient
+ *       anywhere sets the non-finite flag and the step writes no state.
+ * fp32 -> bf16 rounds to nearest even; subnormals are kept.
+ *
+ * Threading: a plan may be used from one host thread at a time, and steps on
+ * one plan must not overlap on the GPU (they share the plan's workspace).
+ * All entry points are asynchronous on the given stream unless stated.
+ */
+#ifndef ADAMW_SM_H
+#define ADAMW_SM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* adamw_stream_t;
+
+/* Storage modes. */
+#define ADAMW_MODE_BF16_KAHAN 0
+#define ADAMW_MODE_MIXED_FP32_MASTER 1
+
+/* adamw_plan_create flags. */
+#define ADAMW_PLAN_NORM 1 /* allocate the global-norm workspace (clipping) */
+
+/* Status codes (0 = success, negative = error). */
+#define ADAMW_OK 0
+#define ADAMW_ERR_INVALID_ARG (-1) /* NULL or out-of-range argument       */
+#define ADAMW_ERR_MISALIGNED (-2)  /* base not aligned to its element size */
+#define ADAMW_ERR_CUDA (-3)        /* a CUDA call failed; see status string */
+#define ADAMW_ERR_NO_NORM (-4)     /* clipping asked of a plan without norm */
+#define ADAMW_ERR_TOO_LARGE (-5)   /* a size exceeds a documented limit     */
+
+/* One tensor of the list.  Every pointer is a device pointer owned by the
+ * caller; the five buffers of one tensor hold `numel` elements each and must
+ * not overlap one another (different tensors may not overlap either).
+ *   param       bf16 p (read/write)        | fp32 master (read/write)
+ *   grad        bf16 g (read only)         | bf16 g (read only)
+ *   exp_avg     bf16 m (read/write)        | fp32 m (read/write)
+ *   exp_avg_sq  bf16 v (read/write)        | fp32 v (read/write)
+ *   aux         bf16 Kahan c (read/write)  | bf16 param out (write only)
+ * Element alignment is required (2 B for bf16, 4 B for fp32).  Tensors whose
+ * five bases are all 16-byte aligned take the vectorised path; others are
+ * still updated correctly, more slowly.  numel may be 0. */
+typedef struct {
+    void* param;
+    const void* grad;
+    void* exp_avg;
+    void* exp_avg_sq;
+    void* aux;
+    int64_t numel;
+} adamw_tensor_t;
+
+/* Hyperparameters of one step.  beta1, beta2 in [0, 1); eps > 0; lr >= 0;
+ * weight_decay >= 0; all finite.  max_grad_norm <= 0 disables clipping. */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    float max_grad_norm;
+} adamw_hparams_t;
+
+typedef struct adamw_plan* adamw_plan_t;
+
+/* Facts about a plan, for callers that size launches or count bytes. */
+typedef struct {
+    int32_t mode;
+    int32_t n_tensors;
+    int64_t total_elems;   /* sum of numel                                  */
+    int32_t grid;          /* CTAs of the update and norm-partial kernels   */
+    int32_t block;         /* threads per CTA                               */
+    int64_t n_chunks;      /* pieces of tensors handed to CTAs              */
+    int64_t scalar_elems;  /* elements on the unvectorised path             */
+    int32_t device;        /* CUDA device the plan lives on                 */
+    int32_t has_norm;      /* ADAMW_PLAN_NORM was given                     */
+} adamw_plan_info_t;
+
+/* One piece of a tensor assigned to one CTA (host-side view of the plan). */
+typedef struct {
+    int32_t tensor;  /* index into the tensor list                      */
+    int32_t vec;     /* 1: 16-byte vector path, 0: element path          */
+    int64_t offset;  /* first element, relative to the tensor's base     */
+    int64_t len;     /* elements                                         */
+    int32_t cta;     /* CTA that processes the piece                     */
+    int32_t pad_;
+} adamw_chunk_t;
+
+/* Builds a plan on the current CUDA device: validates the list, splits the
+ * flattened element space evenly over a persistent grid (grid = SM count x
+ * resident CTAs per SM, fewer for small lists), uploads the tensor table and
+ * the chunk table, and (with ADAMW_PLAN_NORM) allocates the norm workspace.
+ * Synchronous (it allocates and copies).  host_table is read during the call
+ * only.  On error *out is left NULL and nothing stays allocated.
+ * Errors: INVALID_ARG (NULL out or table with n_tensors > 0, n_tensors < 0,
+ * bad mode, numel < 0, NULL buffer with numel > 0), MISALIGNED, CUDA. */
+int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_tensors,
+                      int32_t mode, int32_t flags, adamw_plan_t* out);
+
+/* One optimizer step over every tensor of the plan, asynchronous on stream.
+ * step = t >= 1, the number of applied updates including this one (a step
+ * skipped for a non-finite gradient does not count).
+ * d_grad_norm (nullable, device fp64): receives the global gradient L2 norm
+ *   when clipping is on.
+ * d_nonfinite (nullable, device int32): receives 1 if any gradient element is
+ *   inf or NaN, else 0.  With clipping on, a 1 means the step wrote nothing.
+ *   Without clipping the state is still updated (non-finite values propagate)
+ *   and the flag only reports it.
+ * Errors: INVALID_ARG (NULL plan/hp, step < 1, hyperparameter out of range),
+ * NO_NORM (clipping on a plan made without ADAMW_PLAN_NORM), CUDA (launch
+ * failure).  An error return launches nothing. */
+int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t step,
+               double* d_grad_norm, int32_t* d_nonfinite,
+               adamw_stream_t stream);
+
+/* The global gradient L2 norm and non-finite flag of the plan's gradients,
+ * without an update (the two-stage reduction the clipped step runs first).
+ * d_grad_norm and d_nonfinite as in adamw_step (either may be NULL).
+ * Errors: INVALID_ARG, NO_NORM, CUDA. */
+int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm,
+                    int32_t* d_nonfinite, adamw_stream_t stream);
+
+/* Releases the plan's device memory (synchronises the plan's device first).
+ * NULL is accepted. */
+int adamw_plan_destroy(adamw_plan_t plan);
+
+/* Fills *out with facts about the plan.  Errors: INVALID_ARG. */
+int adamw_plan_get_info(adamw_plan_t plan, adamw_plan_info_t* out);
+
+/* Host-only (needs no GPU): the partition adamw_plan_create would build for
+ * the given list on a grid of `grid` CTAs.  Writes up to `cap` chunks to out
+ * (out may be NULL when cap is 0) and the full count to *n_out.
+ * Errors: INVALID_ARG, MISALIGNED, TOO_LARGE (cap smaller than the count;
+ * *n_out still holds the count). */
+int adamw_plan_chunks(const adamw_tensor_t* host_table, int32_t n_tensors,
+                      int32_t mode, int32_t grid, adamw_chunk_t* out,
+                      int64_t cap, int64_t* n_out);
+
+/* Host-only: the five per-step fp32 scalars of step t, in the order
+ * step_size, sbc2, omb1, omb2, lrwd.  Errors: INVALID_ARG. */
+int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step, float out5[5]);
+
+/* Measurement aid: copies `bytes` from src to dst (device pointers) with the
+ * library's 16-byte-vector streaming copy kernel, asynchronously.  Used to
+ * measure the HBM copy ceiling the update kernel is compared with.
+ * bytes >= 0; both pointers 16-byte aligned and bytes a multiple of 16.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+int adamw_copy_probe(void* dst, const void* src, int64_t bytes,
+                     adamw_stream_t stream);
+
+/* Text for a status code; for ADAMW_ERR_CUDA it also names the last CUDA
+ * error seen by this thread.  Never NULL; valid until the next call from the
+ * same thread. */
+const char* adamw_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAMW_SM_H */

@@ -1,0 +1,156 @@
+"""Host-side tests of the C ABI: the library loads and exports every symbol
+the header declares, the planner partitions lists correctly, validation
+rejects bad arguments.  No GPU needed (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from adamw_optimizer_step_sm_gb300 import adamw_sm as A
+from adamw_optimizer_step_sm_gb300 import build as B
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            src = open(os.path.join(HEADER_DIR, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(adamw_\w+)\s*\(", src, re.M))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(B.build())
+    names = _declared_functions()
+    assert "adamw_step" in names and "adamw_plan_create" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def _fake(base, n, mode=0, skew=(0, 0, 0, 0, 0)):
+    wide = 2 if mode == 0 else 4
+    es = (wide, 2, wide, wide, 2)
+    return tuple(base + (k + 1) * (1 << 36) + s * e for k, (s, e) in enumerate(zip(skew, es))) + (n,)
+
+
+def _check_partition(entries, mode, grid):
+    chunks = A.adamw_plan_chunks(entries, mode, grid)
+    wide = 2 if mode == 0 else 4
+    es = (wide, 2, wide, wide, 2)
+    covered = {k: np.zeros(e[5], np.int32) for k, e in enumerate(entries)}
+    per_cta = np.zeros(grid, np.int64)
+    last_cta = 0
+    for c in chunks:
+        assert 0 <= c.cta < grid and c.cta >= last_cta, "chunks not in CTA order"
+        last_cta = c.cta
+        covered[c.tensor][c.offset:c.offset + c.len] += 1
+        per_cta[c.cta] += c.len
+        if c.vec:
+            e = entries[c.tensor]
+            for s in range(5):
+                assert (e[s] + c.offset * es[s]) % 16 == 0, "vector chunk start not 16-B aligned"
+    for k, cov in covered.items():
+        assert np.all(cov == 1), f"tensor {k}: elements covered {set(cov.tolist())} times"
+    total = sum(e[5] for e in entries)
+    if total:
+        target = -(-total // grid)
+        assert per_cta.max() <= target + 8 + 8, "CTA load imbalance beyond one vector"
+    return chunks
+
+
+def test_partition_covers_each_element_once_and_balances():
+    sizes = [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257]
+    for mode in (0, 1):
+        entries = [_fake(i << 30, n, mode) for i, n in enumerate(sizes)]
+        for grid in (1, 2, 5, 152, 608, 5000):
+            _check_partition(entries, mode, grid)
+
+
+def test_partition_misaligned_bases_take_head_or_element_path():
+    # same skew on every stream: a short element-path head re-aligns them
+    e_same = [_fake(0, 1000, 0, skew=(3, 3, 3, 3, 3))]
+    ch = _check_partition(e_same, 0, 4)
+    assert ch[0].vec == 0 and ch[0].len == 5 and all(c.vec for c in ch[1:])
+    # different skews: no head works, whole tensor on the element path
+    e_diff = [_fake(0, 1000, 0, skew=(1, 0, 0, 0, 0))]
+    ch = _check_partition(e_diff, 0, 4)
+    assert all(c.vec == 0 for c in ch)
+    # mixed mode: fp32 streams 1 element (4 B) and bf16 streams 5 elements
+    # (10 B) past a 16-B boundary: a 3-element head aligns all five
+    e_mix = [_fake(0, 999, 1, skew=(1, 5, 1, 1, 5))]
+    ch = _check_partition(e_mix, 1, 3)
+    assert ch[0].vec == 0 and ch[0].len == 3 and all(c.vec for c in ch[1:])
+
+
+def test_opt_1_3b_partition():
+    from adamw_optimizer_step_sm_gb300 import workloads as W
+    w = W.WORKLOADS["opt1.3b_bf16_kahan"]
+    offs, _ = W.tensor_offsets(w.numels)
+    entries = [tuple(b + (k + 1) * (1 << 40) for k in range(5)) + (n,)
+               for b, n in zip((2 * o for o in offs), w.numels)]
+    ch = _check_partition(entries, 0, 152 * 3)
+    assert len(ch) < 152 * 3 + 2 * len(entries)
+    assert all(c.vec for c in ch)
+
+
+def test_validation_errors():
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([_fake(0, 10, 0, skew=(0, 0, 0, 0, 0))[:4] + (1,) + (10,)], 0, 2)
+    assert e.value.status == A.ADAMW_ERR_MISALIGNED
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([(0, 0, 0, 0, 0, 10)], 0, 2)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([_fake(0, -1)], 0, 2)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([_fake(0, 10)], 7, 2)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    # fp32 master must be 4-byte aligned in mixed mode
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([_fake(0, 10, 1, skew=(0, 0, 0, 0, 0))[:0] + (2, 16, 32, 64, 96, 10)], 1, 2)
+    assert e.value.status == A.ADAMW_ERR_MISALIGNED
+    # zero-length tensors may have NULL buffers
+    assert A.adamw_plan_chunks([(0, 0, 0, 0, 0, 0)], 0, 2) == []
+
+
+@pytest.mark.parametrize("bad", [dict(beta1=1.0), dict(beta2=-0.1), dict(eps=0.0),
+                                 dict(lr=-1e-3), dict(weight_decay=-0.1),
+                                 dict(lr=float("nan")), dict(max_grad_norm=float("inf"))])
+def test_hparam_validation(bad):
+    hp = A.hparams(**bad)
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_step_scalars(hp, 1)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+
+
+def test_step_zero_rejected():
+    with pytest.raises(A.AdamWError):
+        A.adamw_step_scalars(A.hparams(), 0)
+
+
+@pytest.mark.parametrize("t", [1, 2, 3, 10, 1000, 10**9])
+@pytest.mark.parametrize("betas", [(0.9, 0.95), (0.9, 0.999), (0.0, 0.0), (0.5, 0.25)])
+def test_step_scalars_agree_with_the_oracle(t, betas):
+    """Library and oracle compute the per-step scalars independently from the
+    same definition; they must agree bit for bit."""
+    hp = A.hparams(lr=2e-4, beta1=betas[0], beta2=betas[1], weight_decay=0.1)
+    ohp = oracle.hparams(lr=2e-4, beta1=betas[0], beta2=betas[1], weight_decay=0.1)
+    ours = np.array(A.adamw_step_scalars(hp, t), np.float32)
+    ref = oracle.load().step_scalars(ohp, t)
+    assert np.array_equal(ours.view(np.uint32), ref.view(np.uint32))
+
+
+def test_gpu_entry_points_fail_loudly_without_a_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_create([_fake(0, 64)], 0)
+    assert e.value.status == A.ADAMW_ERR_CUDA

@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU
+oracle on identical seeded bytes.  Tolerances are those stated in
+``parity_harness``: <= 1 bf16 ulp on bf16 state, <= 1e-6 relative on fp32
+state, identical non-finite flags (bit-identical results are expected)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import parity_harness as H
+from adamw_optimizer_step_sm_gb300 import adamw_sm as A
+from adamw_optimizer_step_sm_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert(rep: H.Report, log=None):
+    assert rep.ok(), "\n".join(rep.failures[:20]) + f"\nlog={log}"
+
+
+def _small(name, **kw):
+    """A small list with the shape mix of the paper workloads plus ragged
+    sizes that span several CTAs and leave tails."""
+    sizes = kw.pop("sizes", [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257, 3 * 768, 50272])
+    mode = kw.pop("mode", W.MODE_BF16_KAHAN)
+    tensors = tuple(W.TensorSpec(f"t{i}", n) for i, n in enumerate(sizes))
+    base = dict(steps=6, lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, heavy_tail=True)
+    base.update(kw)
+    return W.Workload(name, mode, tensors, **base)
+
+
+# ------------------------------------------------------------ paper configs --
+
+def test_flat1m_bf16_kahan_bit_exact():
+    rep, log = H.run_parity(W.WORKLOADS["flat1m_bf16_kahan"])
+    _assert(rep, log)
+    assert rep.exact == rep.n, f"{rep.n - rep.exact} of {rep.n} values not bit-identical"
+
+
+def test_bert_shard_mixed():
+    rep, log = H.run_parity(W.WORKLOADS["bert55m_shard_mixed"])
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
+def test_opt125m_bf16_kahan_full_list():
+    rep, log = H.run_parity(W.WORKLOADS["opt125m_bf16_kahan"])
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
+def test_opt1_3b_bf16_kahan_sampled_full_size():
+    rep, log = H.run_sampled(W.WORKLOADS["opt1.3b_bf16_kahan"], per_tensor=1024)
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
+def test_opt1_3b_mixed_clip_inf_skip_sampled_full_size():
+    w = W.WORKLOADS["opt1.3b_mixed_clip"]
+    rep, log = H.run_sampled(w, per_tensor=1024)
+    _assert(rep, log)
+    skipped = [k for (k, s, os_, *_rest) in log if s]
+    assert skipped == [w.inf_at[0]], log
+    # every applied step's norm equals the oracle's to fp64 rounding noise
+    for (k, s, _, flag, bad, gn, on) in log:
+        if not s:
+            assert abs(gn - on) <= 1e-9 * on
+
+
+# ------------------------------------------------------------- edge cases --
+
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED])
+@pytest.mark.parametrize("clip", [0.0, 0.5])
+@pytest.mark.parametrize("layout", [(8, 0), (1, 3), (1, 1)])
+def test_ragged_lists(mode, clip, layout):
+    """Tails, empty tensors, one-element tensors and bases that are not 16-B
+    aligned (element-path heads and whole element-path tensors)."""
+    w = _small("ragged", mode=mode, max_grad_norm=clip)
+    rep, log = H.run_parity(w, align_elems=layout[0], skew=layout[1])
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED])
+def test_clip_skips_step_with_inf_and_writes_nothing(mode):
+    w = _small("skip", mode=mode, max_grad_norm=1.0, inf_at=(2, 8, 777), steps=4)
+    rep, log = H.run_parity(w)
+    _assert(rep, log)
+    assert [k for (k, s, *_r) in log if s] == [2]
+    # the skipped step itself wrote nothing
+    gpu = H.GpuRun(w)
+    hp, _ = H.hp_pair(w)
+    gpu.set_grad(1)
+    gpu.step(hp)
+    before = [t.clone() for t in (gpu.st.param, gpu.st.exp_avg, gpu.st.exp_avg_sq, gpu.st.aux)]
+    gpu.set_grad(2)
+    assert gpu.step(hp) is True
+    after = (gpu.st.param, gpu.st.exp_avg, gpu.st.exp_avg_sq, gpu.st.aux)
+    for b, a in zip(before, after):
+        assert torch.equal(b.view(torch.uint8), a.view(torch.uint8))
+    gpu.plan.close()
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan")])
+def test_nonfinite_reported_without_clip(bad):
+    """Without clipping the step runs and NaN/inf propagate exactly as in the
+    oracle; the flag reports them."""
+    w = _small("report", steps=2)
+    gpu = H.GpuRun(w)
+    ref = H.OracleRun.from_state(gpu.st)
+    hp_g, hp_o = H.hp_pair(w)
+    for k in (1, 2):
+        gpu.set_grad(k)
+        if k == 2:
+            gpu.g[gpu.st.offsets[8] + 12345] = bad
+        gpu.step(hp_g)
+        _, _, obad = ref.step(H.to_u16(gpu.g), hp_o)
+        assert bool(gpu.flag.item()) == obad == (k == 2)
+    rep = H.compare_state(gpu, ref)
+    _assert(rep)
+    gpu.plan.close()
+
+
+def test_grad_norm_deterministic_and_matches_oracle():
+    w = W.WORKLOADS["opt125m_bf16_kahan"]
+    gpu = H.GpuRun(w)
+    gpu.set_grad(1)
+    norms = []
+    for _ in range(3):
+        gpu.plan.grad_norm(gpu.norm, gpu.flag)
+        norms.append(float(gpu.norm.item()))
+    assert norms[0] == norms[1] == norms[2]
+    g = H.to_u16(gpu.g)
+    o = O.load()
+    sumsq, bad = o.grad_sumsq([g[off:off + n] for off, n in zip(gpu.st.offsets, w.numels)])
+    _, onorm = o.clip_coef(sumsq, 1.0)
+    assert not bad and gpu.flag.item() == 0
+    assert abs(norms[0] - onorm) <= 1e-12 * onorm
+    gpu.plan.close()
+
+
+def test_grad_norm_with_huge_and_tiny_values():
+    """Values whose squares leave fp32 range take the fp64 path."""
+    w = _small("huge", sizes=[4096, 100])
+    gpu = H.GpuRun(w)
+    gpu.g.zero_()
+    gpu.g[5] = 3.0e30
+    gpu.g[6] = -2.0e19
+    gpu.g[7] = 1.0e-30
+    gpu.g[4096 + 8] = 0.5
+    gpu.plan.grad_norm(gpu.norm, gpu.flag)
+    g = H.to_u16(gpu.g)
+    o = O.load()
+    sumsq, bad = o.grad_sumsq([g[off:off + n] for off, n in zip(gpu.st.offsets, w.numels)])
+    assert not bad and gpu.flag.item() == 0
+    onorm = float(np.sqrt(sumsq))
+    assert abs(gpu.norm.item() - onorm) <= 1e-12 * onorm
+    gpu.plan.close()
+
+
+def test_empty_plan_and_zero_length_tensors():
+    z = torch.zeros(0, dtype=torch.bfloat16, device="cuda")
+    plan = A.Plan([z], [z], [z], [z], [z], W.MODE_BF16_KAHAN, norm=True)
+    norm = torch.full((1,), 7.0, dtype=torch.float64, device="cuda")
+    flag = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    plan.step(A.hparams(max_grad_norm=1.0), 1, grad_norm=norm, nonfinite=flag)
+    torch.cuda.synchronize()
+    assert norm.item() == 0.0 and flag.item() == 0
+    assert plan.info.grid == 0
+    plan.close()
+    empty = A.adamw_plan_create([], W.MODE_MIXED, 0)
+    A.adamw_step(empty, A.hparams(), 1)
+    A.adamw_plan_destroy(empty)
+
+
+def test_api_errors_on_gpu():
+    w = _small("err", sizes=[1000])
+    st = W.make_state(w, "cuda")
+    g = torch.zeros_like(st.aux)
+    v = st.views
+    plan = A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode, norm=False)
+    with pytest.raises(A.AdamWError) as e:
+        plan.step(A.hparams(max_grad_norm=1.0), 1)
+    assert e.value.status == A.ADAMW_ERR_NO_NORM
+    with pytest.raises(A.AdamWError) as e:
+        plan.step(A.hparams(beta1=1.5), 1)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    with pytest.raises(A.AdamWError) as e:
+        plan.step(A.hparams(), 0)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_create([(st.param.data_ptr() + 1, g.data_ptr(), st.exp_avg.data_ptr(),
+                              st.exp_avg_sq.data_ptr(), st.aux.data_ptr(), 10)], w.mode)
+    assert e.value.status == A.ADAMW_ERR_MISALIGNED
+    plan.close()
+
+
+def test_copy_probe_copies():
+    src = torch.randint(-2**31, 2**31 - 1, (1 << 22,), dtype=torch.int32, device="cuda")
+    dst = torch.zeros_like(src)
+    A.adamw_copy_probe(dst.data_ptr(), src.data_ptr(), src.numel() * 4,
+                       torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(src, dst)
+    with pytest.raises(A.AdamWError):
+        A.adamw_copy_probe(dst.data_ptr() + 4, src.data_ptr(), 64)
+
+
+def test_steps_on_a_side_stream_and_a_second_plan():
+    """Two independent plans on two streams give the same bytes as one run."""
+    w = _small("streams", sizes=[70000, 333])
+    a, b = H.GpuRun(w), H.GpuRun(w)
+    hp, _ = H.hp_pair(w)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for k in (1, 2, 3):
+        a.set_grad(k)
+        b.set_grad(k)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            a.plan.step(hp, k)
+        with torch.cuda.stream(s2):
+            b.plan.step(hp, k)
+    torch.cuda.synchronize()
+    for x, y in zip((a.st.param, a.st.aux), (b.st.param, b.st.aux)):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    a.plan.close()
+    b.plan.close()
