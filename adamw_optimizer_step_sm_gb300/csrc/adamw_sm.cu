@@ -335,41 +335,62 @@ adamw_update_kernel(const TensorDev* __restrict__ tensors,
     }
 }
 
-// Sum of squares of 8 bf16 in fp32, fixed order; squares of bf16 values are
-// exact in fp32 for |g| in [2^-63, 2^64).
-__device__ __forceinline__ float sumsq8(const uint4& w) {
-    const float a0 = bf16_lo(w.x), a1 = bf16_hi(w.x), a2 = bf16_lo(w.y), a3 = bf16_hi(w.y);
-    const float a4 = bf16_lo(w.z), a5 = bf16_hi(w.z), a6 = bf16_lo(w.w), a7 = bf16_hi(w.w);
-    const float s01 = __fadd_rn(__fmul_rn(a0, a0), __fmul_rn(a1, a1));
-    const float s23 = __fadd_rn(__fmul_rn(a2, a2), __fmul_rn(a3, a3));
-    const float s45 = __fadd_rn(__fmul_rn(a4, a4), __fmul_rn(a5, a5));
-    const float s67 = __fadd_rn(__fmul_rn(a6, a6), __fmul_rn(a7, a7));
-    return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
-}
-
-// Compensated (Kahan) fp32 accumulation: s + (-comp) carries the running sum.
-struct KahanF32 {
-    float s = 0.0f, comp = 0.0f;
+// Error-free fp32 accumulation of non-negative terms: s + e is the exact sum
+// of everything added since the last flush, up to the rounding of e itself.
+// Squares of bf16 values are exact in fp32 for |g| in [2^-63, 2^64); for
+// a >= b >= 0 the rounding error of a + b is exactly b - ((a + b) - a)
+// (Dekker's Fast2Sum), so no bit of any square is lost; e collects those
+// errors.  A group of at most 32 terms is flushed to an fp64 accumulator.
+struct Sum2F32 {
+    float s = 0.0f, e = 0.0f;
     __device__ __forceinline__ void add(float x) {
-        const float y = __fsub_rn(x, comp);
-        const float t = __fadd_rn(s, y);
-        comp = __fsub_rn(__fsub_rn(t, s), y);
+        const float a = fmaxf(s, x), b = fminf(s, x);
+        const float t = __fadd_rn(a, b);
+        e = __fadd_rn(e, __fsub_rn(b, __fsub_rn(t, a)));
         s = t;
     }
-    __device__ __forceinline__ double value() const { return double(s) - double(comp); }
+    // Adds the group to acc and restarts it; false when the group left the
+    // range where squares are exact and sums finite.
+    __device__ __forceinline__ bool flush(double& acc) {
+        const bool ok = s < 0x1p100f;   // also false for inf and NaN
+        acc += double(s) + double(e);
+        s = 0.0f;
+        e = 0.0f;
+        return ok;
+    }
 };
 
-// Vectors whose fp32 sum of squares is not below 2^96 (huge, inf or NaN
-// elements) are summed in fp64 one element at a time, which also sets the
-// non-finite flag.
-__device__ __forceinline__ void norm_slow8(const uint4& w, double& acc, bool& bad) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+__device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
+
+// Walks the g elements of one CTA's chunks that belong to this thread, in a
+// fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
+// after every group of U vectors.
+template <int U, typename FV, typename FE, typename FI>
+__device__ __forceinline__ void for_thread_grads(const TensorDev* __restrict__ tensors,
+                                                 const ChunkDev* __restrict__ chunks,
+                                                 int32_t c0, int32_t c1, FV vec, FE elem,
+                                                 FI after_iter) {
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        const ChunkDev ch = chunks[ci];
+        const uint16_t* g = static_cast<const uint16_t*>(tensors[ch.tensor].g) + ch.off;
+        int64_t done = 0;
+        if (ch.vec) {
+            const int64_t nvec = ch.len / kVec;
+            for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+                uint4 w[U];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
-        bad |= !isfinite(lo) || !isfinite(hi);
-        acc += lo * lo;
-        acc += hi * hi;
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = base + int64_t(u) * kBlock;
+                    if (i < nvec) w[u] = ld16(g + i * kVec);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (base + int64_t(u) * kBlock < nvec) vec(w[u]);
+                after_iter();
+            }
+            done = nvec * kVec;
+        }
+        for (int64_t i = done + threadIdx.x; i < ch.len; i += kBlock) elem(g[i]);
     }
 }
 
@@ -390,48 +411,64 @@ __device__ __forceinline__ double block_sum(double x) {
 
 // Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
 // same partition as the update (so the result depends only on the plan).
+// Fast path: error-free fp32 group sums of the exact squares, flushed to fp64
+// every 32 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
+// inf or NaN gradients) recomputes its elements in fp64, which also decides
+// the non-finite flag.
 __global__ void __launch_bounds__(kBlock)
 norm_partial_kernel(const TensorDev* __restrict__ tensors,
                     const ChunkDev* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin,
                     double* __restrict__ partial, int32_t* __restrict__ flag) {
-    KahanF32 acc;
-    double slow = 0.0;
-    bool bad = false;
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
-    for (int32_t ci = c0; ci < c1; ++ci) {
-        const ChunkDev ch = chunks[ci];
-        const uint16_t* g = static_cast<const uint16_t*>(tensors[ch.tensor].g) + ch.off;
-        int64_t done = 0;
-        if (ch.vec) {
-            const int64_t nvec = ch.len / kVec;
-            constexpr int U = 4;
-            for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
-                uint4 w[U];
+    Sum2F32 grp;
+    double tot = 0.0;
+    bool in_range = true;
+    uint32_t nz = 0;
+    for_thread_grads<4>(
+        tensors, chunks, c0, c1,
+        [&](const uint4& w) {
+            nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
+            grp.add(sq(bf16_lo(w.x)));
+            grp.add(sq(bf16_hi(w.x)));
+            grp.add(sq(bf16_lo(w.y)));
+            grp.add(sq(bf16_hi(w.y)));
+            grp.add(sq(bf16_lo(w.z)));
+            grp.add(sq(bf16_hi(w.z)));
+            grp.add(sq(bf16_lo(w.w)));
+            grp.add(sq(bf16_hi(w.w)));
+        },
+        [&](uint16_t h) {
+            nz |= h & 0x7fffu;
+            grp.add(sq(from_bf16(h)));
+            in_range &= grp.flush(tot);
+        },
+        [&]() { in_range &= grp.flush(tot); });
+    in_range &= grp.flush(tot);
+    bool bad = false;
+    if (!in_range || (nz != 0 && tot < 0x1p-100)) {
+        double acc = 0.0;
+        for_thread_grads<1>(
+            tensors, chunks, c0, c1,
+            [&](const uint4& w) {
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t i = base + int64_t(u) * kBlock;
-                    if (i < nvec) w[u] = ld16(g + i * kVec);
+                for (int j = 0; j < 4; ++j) {
+                    const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
+                    bad |= !isfinite(lo) || !isfinite(hi);
+                    acc += lo * lo;
+                    acc += hi * hi;
                 }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t i = base + int64_t(u) * kBlock;
-                    if (i < nvec) {
-                        const float q = sumsq8(w[u]);
-                        if (q < 0x1p96f) acc.add(q);
-                        else norm_slow8(w[u], slow, bad);
-                    }
-                }
-            }
-            done = nvec * kVec;
-        }
-        for (int64_t i = done + threadIdx.x; i < ch.len; i += kBlock) {
-            const double x = from_bf16(g[i]);
-            bad |= !isfinite(x);
-            slow += x * x;
-        }
+            },
+            [&](uint16_t h) {
+                const double x = from_bf16(h);
+                bad |= !isfinite(x);
+                acc += x * x;
+            },
+            [&]() {});
+        tot = acc;
     }
-    const double tot = block_sum(acc.value() + slow);
+    tot = block_sum(tot);
     const int any = __syncthreads_or(bad);
     if (threadIdx.x == 0) {
         partial[blockIdx.x] = tot;

@@ -36,7 +36,6 @@ from adamw_optimizer_step_sm_gb300 import workloads as W  # noqa: E402
 METRIC = "params updated/s & achieved HBM GB/s (% of peak), OPT-1.3b-shaped bf16 Kahan step"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "opt1.3b_bf16_kahan"
-CPU_SAMPLE_ELEMS = 1 << 27
 
 
 def bytes_per_param(w: W.Workload) -> int:
@@ -143,23 +142,31 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int):
+def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arrays=None):
     """The oracle as it stands on host cores, over the first n_elems elements
-    of the workload; returns (params/s, seconds, threads)."""
+    of the workload; returns (params/s, seconds, threads).  ``arrays`` may hold
+    host copies (param, exp_avg, exp_avg_sq, aux, grad, offsets) of the
+    workload's freshly drawn state; otherwise the sample is drawn on the CPU."""
     import numpy as np
     import oracle as O
     o = O.load()
-    ws = W.truncated(w, n_elems)
-    st = W.make_state(ws, "cpu")
     to16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
-    wide = to16 if ws.mode == W.MODE_BF16_KAHAN else (lambda t: t.numpy())
-    p, m, v, a = wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux)
+    if arrays is None:
+        ws = W.truncated(w, n_elems)
+        st = W.make_state(ws, "cpu")
+        wide = to16 if ws.mode == W.MODE_BF16_KAHAN else (lambda t: t.numpy())
+        p, m, v, a = wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux)
+        grads = [to16(W.make_grad(ws, k + 1, "cpu")) for k in range(min(steps, 2))]
+        offsets, numels = st.offsets, ws.numels
+    else:
+        ws = w
+        p, m, v, a, g0, offsets = arrays
+        grads, numels = [g0], w.numels
     hp = O.hparams(**ws.hparams())
-    grads = [to16(W.make_grad(ws, k + 1, "cpu")) for k in range(min(steps, 2))]
-    # split the elementwise work into contiguous pieces, one per thread
+    # split the elementwise work into contiguous pieces, several per thread
     pieces = []
-    for off, n in zip(st.offsets, ws.numels):
-        step = max(1, -(-n // threads))
+    for off, n in zip(offsets, numels):
+        step = max(1 << 16, -(-n // threads))
         for s in range(0, n, step):
             pieces.append((off + s, min(n - s, step)))
     clip = ws.max_grad_norm > 0
@@ -168,7 +175,7 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int):
         g = grads[k % len(grads)]
         coef = 1.0
         if clip:
-            sumsq, bad = o.grad_sumsq([g[off:off + n] for off, n in zip(st.offsets, ws.numels)])
+            sumsq, bad = o.grad_sumsq([g[off:off + n] for off, n in zip(offsets, numels)])
             coef, _ = o.clip_coef(sumsq, ws.max_grad_norm)
 
         def one(pc, t=k + 1):
@@ -182,7 +189,7 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int):
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, pieces))
     dt = time.perf_counter() - t0
-    return ws.total * steps / dt, dt, threads
+    return sum(numels) * steps / dt, dt, threads
 
 
 def host_threads() -> int:
@@ -267,6 +274,15 @@ def run_gpu(args):
     st = W.make_state(w_bench, device)
     n_grad = max(1, min(args.steps + args.warmup, args.grad_buffers))
     grads = [W.make_grad(w_bench, k + 1, device) for k in range(n_grad)]
+    cpu_arrays = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # host copy of the freshly drawn inputs (before any step runs), for
+        # the CPU oracle baseline
+        import numpy as np
+        to16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        wide = to16 if w.mode == W.MODE_BF16_KAHAN else (lambda t: t.cpu().numpy())
+        cpu_arrays = (wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux),
+                      to16(grads[0]), list(st.offsets))
     v = st.views
     plans = [A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode,
                     norm=clip) for g in grads]
@@ -366,12 +382,13 @@ def run_gpu(args):
         "clocks": clk,
         "wall_s_timed": wall,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if cpu_arrays is not None:
         thr = host_threads()
-        val, secs, used = oracle_throughput(w, min(CPU_SAMPLE_ELEMS, N), 1, thr)
+        val, secs, used = oracle_throughput(w_bench, N, 1, thr, cpu_arrays)
         out["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": used, "kind": "oracle",
-                               "sample": f"first {min(CPU_SAMPLE_ELEMS, N)} elements of the "
-                                         f"{w.name} list, 1 step, {secs:.2f} s"}
+                               "sample": f"one step over the whole {w.name} list "
+                                         f"({N} params, the same drawn inputs), {secs:.2f} s "
+                                         f"on {used} threads"}
     for p in plans:
         p.close()
     if rank == 0:
@@ -414,7 +431,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--grad-buffers", type=int, default=4)
-    ap.add_argument("--ref-sample", type=int, default=1 << 25)
+    ap.add_argument("--ref-sample", type=int, default=1 << 28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")

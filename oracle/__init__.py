@@ -89,7 +89,7 @@ class Oracle:
         L.oracle_adamw_bf16_plain.argtypes = [vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_mixed.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_grad_sumsq.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_double),
-                                        ctypes.POINTER(ctypes.c_int32)]
+                                        ctypes.POINTER(ctypes.c_int32)]  # acc[2]
         L.oracle_clip_coef.argtypes = [ctypes.c_double, f32,
                                        ctypes.POINTER(ctypes.c_double)]
         L.oracle_clip_coef.restype = f32
@@ -141,13 +141,14 @@ class Oracle:
 
     # -- norm ------------------------------------------------------------------
     def grad_sumsq(self, grads) -> tuple[float, bool]:
-        acc = ctypes.c_double(0.0)
+        """Sum of squares over the tensors in order (compensated fp64) and
+        whether any element is non-finite."""
+        acc = (ctypes.c_double * 2)(0.0, 0.0)
         bad = ctypes.c_int32(0)
         for g in grads:
             _check(g, np.uint16)
-            self.lib.oracle_grad_sumsq(_ptr(g), g.size, ctypes.byref(acc),
-                                       ctypes.byref(bad))
-        return acc.value, bool(bad.value)
+            self.lib.oracle_grad_sumsq(_ptr(g), g.size, acc, ctypes.byref(bad))
+        return acc[0] + acc[1], bool(bad.value)
 
     def clip_coef(self, sumsq: float, max_norm: float) -> tuple[float, float]:
         norm = ctypes.c_double(0.0)

@@ -48,9 +48,10 @@
  *   mixed mode (fp32 master/m/v, bf16 grad in, bf16 param out):
  *     master' = master - upd ;  p_out = bf16(master')
  *
- *   global-norm clipping (optional): norm = sqrt(sum of g^2) in fp64 over all
- *   tensors in list order; any non-finite g sets the flag and the step writes
- *   nothing; otherwise coef = (float) min(1, max_norm / (norm + 1e-6)).
+ *   global-norm clipping (optional): norm = sqrt(sum of g^2) over all
+ *   tensors in list order, the sum in compensated fp64; any non-finite g
+ *   sets the flag and the step writes nothing; otherwise
+ *   coef = (float) min(1, max_norm / (norm + 1e-6)).
  *
  * fp32 -> bf16 is round-to-nearest-even; NaN stays a (quiet) NaN, overflow
  * goes to +-inf, subnormals are kept (no flush to zero).
@@ -235,19 +236,34 @@ void oracle_adamw_mixed(float* master, const uint16_t* g, float* m, float* v,
 
 /* ------------------------------------------------- global norm and clip -- */
 
-/* Adds sum of g^2 (fp64, element order) of one bf16 tensor to *sumsq and ORs
- * a non-finite test into *nonfinite.  Call once per tensor, in list order. */
-void oracle_grad_sumsq(const uint16_t* g, int64_t n, double* sumsq,
+/* Adds sum of g^2 of one bf16 tensor, in element order, to the running sum
+ * acc[0] + acc[1] and ORs a non-finite test into *nonfinite.  Call once per
+ * tensor, in list order, starting from acc = {0, 0}.
+ *
+ * The definition is the exact sum of squares.  A plain fp64 running sum is
+ * not close enough to it for long lists: squares below half an ulp of the
+ * running sum are dropped every time, which biases the result low (about
+ * 1e-10 relative over 125M terms).  The sum is therefore compensated
+ * (Kahan-Babuska / Neumaier): acc[1] collects, exactly, what each fp64
+ * addition rounds away. */
+void oracle_grad_sumsq(const uint16_t* g, int64_t n, double acc[2],
                        int32_t* nonfinite)
 {
-    double acc = *sumsq;
+    double s = acc[0], comp = acc[1];
     int32_t bad = *nonfinite;
     for (int64_t i = 0; i < n; ++i) {
         double x = (double)bf16_bits_to_f32(g[i]);
         if (!isfinite(x)) bad = 1;
-        acc += x * x;
+        double sq = x * x;
+        double t = s + sq;
+        if (fabs(s) >= fabs(sq))
+            comp += (s - t) + sq;
+        else
+            comp += (sq - t) + s;
+        s = t;
     }
-    *sumsq = acc;
+    acc[0] = s;
+    acc[1] = comp;
     *nonfinite = bad;
 }
 
@@ -285,12 +301,12 @@ int32_t oracle_adamw_list_step(const oracle_tensor_t* list, int32_t n_tensors,
 {
     float coef = 1.0f;
     if (hp->max_grad_norm > 0.0f) {
-        double sumsq = 0.0;
+        double acc[2] = {0.0, 0.0};
         int32_t bad = 0;
         for (int32_t k = 0; k < n_tensors; ++k)
             oracle_grad_sumsq((const uint16_t*)list[k].grad, list[k].numel,
-                              &sumsq, &bad);
-        coef = oracle_clip_coef(sumsq, hp->max_grad_norm, norm_out);
+                              acc, &bad);
+        coef = oracle_clip_coef(acc[0] + acc[1], hp->max_grad_norm, norm_out);
         if (bad) return 1;
     }
     for (int32_t k = 0; k < n_tensors; ++k) {

@@ -346,6 +346,16 @@ def pin_norm(o: O.Oracle):
     ref = torch.linalg.vector_norm(torch.from_numpy(np.concatenate([bf16_to_f64(x) for x in parts])))
     _, norm = o.clip_coef(s, 1.0)
     assert abs(norm - float(ref)) <= 1e-12 * float(ref)
+    # a long heavy-tailed list: the compensated fp64 sum equals the exactly
+    # rounded sum (a plain running sum drifts low by ~1e-10 here)
+    n_long = 20_000_000
+    g32 = (r.standard_normal(n_long) * 1e-2).astype(F32)
+    g32[r.random(n_long) < 0.01] *= 100.0
+    gl = torch_bf16_bits(g32)
+    s, bad = o.grad_sumsq([gl[:7_000_001], gl[7_000_001:]])
+    x = bf16_to_f64(gl)
+    exact = math.fsum(x * x)
+    assert not bad and abs(s - exact) <= 4e-16 * exact, (s, exact)
     # no clipping below max_norm
     assert o.clip_coef(0.25, 1.0)[0] == 1.0
     assert o.clip_coef(4.0, 1.0)[0] == f32(1.0 / (2.0 + 1e-6))

@@ -1,0 +1,108 @@
+"""Host-side pieces of bench.py: byte accounting, the max-over-ranks timing
+reduction on two gloo ranks (the N > 1 replica path), clock-log parsing and
+the reference (CPU oracle) arm on a tiny sample."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from adamw_optimizer_step_sm_gb300 import workloads as W
+
+
+def test_bytes_per_param():
+    assert bench.bytes_per_param(W.WORKLOADS["opt1.3b_bf16_kahan"]) == 18
+    assert bench.bytes_per_param(W.WORKLOADS["bert55m_shard_mixed"]) == 28
+    assert bench.bytes_per_param(W.WORKLOADS["opt1.3b_mixed_clip"]) == 30
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w, r, _ = bench.dist_env()
+    bench.barrier(w)
+    t = bench.reduce_max(1.5 + rank, w, torch.device("cpu"))
+    out[rank] = (w, r, t)
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+            assert p.exitcode == 0
+        assert out[0] == (2, 0, 2.5) and out[1] == (2, 1, 2.5)
+
+
+def test_single_rank_reduce_is_identity():
+    assert bench.reduce_max(3.25, 1, torch.device("cpu")) == 3.25
+
+
+def test_clock_log_parsing():
+    c = bench.ClockSampler(0)
+    c.proc = None
+    assert c.stop() is None
+
+    class FakeProc:
+        def terminate(self): pass
+        def wait(self, timeout=None): return 0
+        def kill(self): pass
+
+    class FakeThread:
+        def join(self, timeout=None): pass
+
+    c.proc, c._t = FakeProc(), FakeThread()
+    c.lines = ["0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1980, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 345, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    r = c.stop()
+    assert r["sm_max_mhz"] == 2070 and r["sm_mhz"] == 1972.5 and r["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_is_dropped_when_kernel_sources_change(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    os.makedirs(tmp_path / "profiles")
+    os.makedirs(tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc")
+    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / "k.cu").write_text("a")
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(
+        {"x": {"kernel_source_hash": h, "dram_bytes_per_launch": 123}}))
+    assert bench.recorded_traffic("x") == 123
+    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / "k.cu").write_text("b")
+    assert bench.recorded_traffic("x") is None
+
+
+def test_reference_arm_prints_one_json_line(capsys):
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1",
+                "--workload", "opt125m_bf16_kahan", "--ref-sample", str(1 << 16)])
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1"])
+    assert capsys.readouterr().out.strip() == ""

@@ -47,7 +47,8 @@ MUTANTS = [
     ("clip_not_clamped", "if (coef > 1.0) coef = 1.0;", "(void)0;"),
     ("clip_no_eps", "double coef = (double)max_norm / (norm + 1e-6);",
      "double coef = (double)max_norm / (norm);"),
-    ("norm_abs_not_square", "acc += x * x;", "acc += fabs(x);"),
+    ("norm_abs_not_square", "double sq = x * x;", "double sq = fabs(x);"),
+    ("norm_uncompensated", "    acc[1] = comp;\n", "    acc[1] = 0.0 * comp;\n"),
     ("nonfinite_missed", "if (!isfinite(x)) bad = 1;", "(void)0;"),
     ("skip_still_writes", "        if (bad) return 1;\n", "        (void)bad;\n"),
     ("clip_scale_ignored_mixed", "float p0 = master[i];\n",
