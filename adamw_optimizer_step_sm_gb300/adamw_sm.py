@@ -6,12 +6,15 @@ CUDA kernels.  The functions keep the C names; a non-zero status raises
 tensor table from torch tensors (torch supplies device memory and streams).
 
 The library is built in-tree (``build.build``) on first use when its sources
-are newer than the shared object; if it cannot be built or loaded, every call
-raises -- there is no fallback implementation.
+are newer than the shared object (or taken from the path in the environment
+variable ADAMW_SM_LIBRARY, for a build made with other tuning constants); if
+it cannot be built or loaded, every call raises -- there is no fallback
+implementation.
 """
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 
 from . import build as _build
@@ -51,7 +54,8 @@ class adamw_plan_info_t(ctypes.Structure):
                 ("total_elems", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("block", ctypes.c_int32), ("n_chunks", ctypes.c_int64),
                 ("scalar_elems", ctypes.c_int64), ("device", ctypes.c_int32),
-                ("has_norm", ctypes.c_int32)]
+                ("has_norm", ctypes.c_int32), ("norm_grid", ctypes.c_int32),
+                ("pad_", ctypes.c_int32)]
 
 
 class adamw_chunk_t(ctypes.Structure):
@@ -69,7 +73,7 @@ def load() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = os.environ.get("ADAMW_SM_LIBRARY") or _build.build()
             L = ctypes.CDLL(path)
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
             L.adamw_plan_create.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32, i32,

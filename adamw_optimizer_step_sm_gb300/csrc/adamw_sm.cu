@@ -4,10 +4,11 @@
 // and c (bf16 Kahan mode, 10 B) or master, m, v and g (mixed mode, 14 B) and
 // writes 8 B or 14 B back, with about twenty fp32 operations in between.
 // That is far below the GPU's ridge point, so HBM bandwidth bounds it and the
-// kernels are built for bytes in flight: a persistent grid (SMs x resident
-// CTAs), one contiguous range of the flattened parameter space per CTA,
-// 16-byte vector loads issued U vectors ahead of the arithmetic, fp32 math,
-// 16-byte stores.  No tensor cores: nothing here is a contraction.
+// kernels are built to keep DRAM streaming: a persistent grid (SMs x resident
+// CTAs) dealt 16K-element tiles of the flattened parameter space round-robin
+// (so the grid sweeps every buffer together), chunk descriptors prefetched one
+// ahead, 16-byte vector loads issued U vectors ahead of the arithmetic, fp32
+// math, 16-byte stores.  No tensor cores: nothing here is a contraction.
 //
 // Arithmetic order follows the definition in include/adamw_sm.h exactly, with
 // the IEEE round-to-nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn,
@@ -54,13 +55,39 @@ __device__ __forceinline__ float from_bf16(uint16_t h) {
     return __uint_as_float(uint32_t(h) << 16);
 }
 
-// Streaming 16-byte accesses.  Every byte is touched once per step, so loads
-// and stores use the evict-first (.cs) policy and leave L2 to the others.
+// Streaming 16-byte accesses.  Every byte is touched once per step.  The
+// cache policy of loads and stores is a build-time constant: 0 = default,
+// 1 = evict-first (.cs), 2 = L1 no-allocate, 3 = last-use (.lu) for loads.
+// Measured on GB300, the default policy is as fast as any hint for lists
+// larger than L2 and keeps L2-resident lists resident between steps.
+#ifndef ADAMW_LD_POLICY
+#define ADAMW_LD_POLICY 0
+#endif
+#ifndef ADAMW_ST_POLICY
+#define ADAMW_ST_POLICY 0
+#endif
 __device__ __forceinline__ uint4 ld16(const void* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#if ADAMW_LD_POLICY == 1
+    return __ldcs(q);
+#elif ADAMW_LD_POLICY == 2
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(q));
+    return r;
+#elif ADAMW_LD_POLICY == 3
+    return __ldlu(q);
+#else
+    return *q;
+#endif
 }
 __device__ __forceinline__ void st16(void* p, uint4 v) {
-    __stcs(reinterpret_cast<uint4*>(p), v);
+    uint4* q = reinterpret_cast<uint4*>(p);
+#if ADAMW_ST_POLICY == 1
+    __stcs(q, v);
+#else
+    *q = v;
+#endif
 }
 
 __device__ __forceinline__ bool bf16x2_nonfinite(uint32_t w) {
@@ -143,17 +170,24 @@ __device__ __forceinline__ float mixed_x1(const StepScalars& s, float coef, floa
 
 // ------------------------------------------------------- chunk walkers ----
 
-constexpr int kUnroll = 2;  // vectors per thread in flight per stream
+// Vectors per thread in flight per stream, and the CTAs per SM the update
+// kernel's register budget is fitted to (0: no constraint).
+#ifndef ADAMW_UNROLL
+#define ADAMW_UNROLL 2
+#endif
+#ifndef ADAMW_MIN_BLOCKS
+#define ADAMW_MIN_BLOCKS 0
+#endif
+constexpr int kUnroll = ADAMW_UNROLL;
 
 template <int K>
-__device__ __forceinline__ void kahan_vec_chunk(const TensorDev& t, int64_t off,
-                                                int64_t len, const StepScalars& s,
-                                                float coef, bool& bad) {
-    uint16_t* p = static_cast<uint16_t*>(t.p) + off;
-    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
-    uint16_t* m = static_cast<uint16_t*>(t.m) + off;
-    uint16_t* v = static_cast<uint16_t*>(t.v) + off;
-    uint16_t* c = static_cast<uint16_t*>(t.a) + off;
+__device__ __forceinline__ void kahan_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
     for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
         uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll], C[kUnroll];
@@ -198,14 +232,13 @@ __device__ __forceinline__ void kahan_vec_chunk(const TensorDev& t, int64_t off,
 }
 
 template <int K>
-__device__ __forceinline__ void kahan_elem_chunk(const TensorDev& t, int64_t off,
-                                                 int64_t len, const StepScalars& s,
-                                                 float coef, bool& bad) {
-    uint16_t* p = static_cast<uint16_t*>(t.p) + off;
-    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
-    uint16_t* m = static_cast<uint16_t*>(t.m) + off;
-    uint16_t* v = static_cast<uint16_t*>(t.v) + off;
-    uint16_t* c = static_cast<uint16_t*>(t.a) + off;
+__device__ __forceinline__ void kahan_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
     for (int64_t i = threadIdx.x; i < len; i += kBlock) {
         uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i], ch = c[i];
         if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
@@ -229,14 +262,13 @@ __device__ __forceinline__ void st32(float* p, const F8& v) {
 }
 
 template <int K>
-__device__ __forceinline__ void mixed_vec_chunk(const TensorDev& t, int64_t off,
-                                                int64_t len, const StepScalars& s,
-                                                float coef, bool& bad) {
-    float* p = static_cast<float*>(t.p) + off;
-    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
-    float* m = static_cast<float*>(t.m) + off;
-    float* v = static_cast<float*>(t.v) + off;
-    uint16_t* o = static_cast<uint16_t*>(t.a) + off;
+__device__ __forceinline__ void mixed_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* o = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
     for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
         uint4 G[kUnroll];
@@ -286,14 +318,13 @@ __device__ __forceinline__ void mixed_vec_chunk(const TensorDev& t, int64_t off,
 }
 
 template <int K>
-__device__ __forceinline__ void mixed_elem_chunk(const TensorDev& t, int64_t off,
-                                                 int64_t len, const StepScalars& s,
-                                                 float coef, bool& bad) {
-    float* p = static_cast<float*>(t.p) + off;
-    const uint16_t* g = static_cast<const uint16_t*>(t.g) + off;
-    float* m = static_cast<float*>(t.m) + off;
-    float* v = static_cast<float*>(t.v) + off;
-    uint16_t* o = static_cast<uint16_t*>(t.a) + off;
+__device__ __forceinline__ void mixed_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* o = static_cast<uint16_t*>(t.a);
     for (int64_t i = threadIdx.x; i < len; i += kBlock) {
         const uint16_t gh = g[i];
         if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
@@ -306,10 +337,31 @@ __device__ __forceinline__ void mixed_elem_chunk(const TensorDev& t, int64_t off
 // --------------------------------------------------------------- kernels --
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
+#if ADAMW_MIN_BLOCKS > 0
+#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock, ADAMW_MIN_BLOCKS)
+#else
+#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock)
+#endif
+
+// One chunk descriptor, read through the read-only path.
+__device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
+    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(c);
+    const ulonglong2 a = __ldg(q), b = __ldg(q + 1), d = __ldg(q + 2);
+    ChunkPtr r;
+    r.p = reinterpret_cast<void*>(a.x);
+    r.g = reinterpret_cast<const void*>(a.y);
+    r.m = reinterpret_cast<void*>(b.x);
+    r.v = reinterpret_cast<void*>(b.y);
+    r.a = reinterpret_cast<void*>(d.x);
+    r.len2 = static_cast<int64_t>(d.y);
+    return r;
+}
+
+// The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]), fetching the
+// next chunk's descriptor before working on the current one.
 template <int MODE, int K>
-__global__ void __launch_bounds__(kBlock)
-adamw_update_kernel(const TensorDev* __restrict__ tensors,
-                    const ChunkDev* __restrict__ chunks,
+__global__ void ADAMW_UPDATE_BOUNDS
+adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
                     const NormOut* __restrict__ norm, int32_t* __restrict__ report) {
     float coef = 1.0f;
@@ -319,16 +371,21 @@ adamw_update_kernel(const TensorDev* __restrict__ tensors,
     }
     bool bad = false;
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    ChunkPtr cur;
+    if (c0 < c1) cur = load_chunk(chunks + c0);
     for (int32_t ci = c0; ci < c1; ++ci) {
-        const ChunkDev ch = chunks[ci];
-        const TensorDev t = tensors[ch.tensor];
+        ChunkPtr nxt = cur;
+        if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
+        const int64_t len = cur.len2 >> 1;
+        const bool vec = cur.len2 & 1;
         if (MODE == ADAMW_MODE_BF16_KAHAN) {
-            if (ch.vec) kahan_vec_chunk<K>(t, ch.off, ch.len, s, coef, bad);
-            else kahan_elem_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+            if (vec) kahan_vec_chunk<K>(cur, len, s, coef, bad);
+            else kahan_elem_chunk<K>(cur, len, s, coef, bad);
         } else {
-            if (ch.vec) mixed_vec_chunk<K>(t, ch.off, ch.len, s, coef, bad);
-            else mixed_elem_chunk<K>(t, ch.off, ch.len, s, coef, bad);
+            if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
+            else mixed_elem_chunk<K>(cur, len, s, coef, bad);
         }
+        cur = nxt;
     }
     if (K == kReport) {
         if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
@@ -340,7 +397,8 @@ adamw_update_kernel(const TensorDev* __restrict__ tensors,
 // Squares of bf16 values are exact in fp32 for |g| in [2^-63, 2^64); for
 // a >= b >= 0 the rounding error of a + b is exactly b - ((a + b) - a)
 // (Dekker's Fast2Sum), so no bit of any square is lost; e collects those
-// errors.  A group of at most 32 terms is flushed to an fp64 accumulator.
+// errors.  A group of at most 64 terms is flushed: s into an fp64 sum, e
+// (at most 2^-18 of s) into an fp32 sum of the errors.
 struct Sum2F32 {
     float s = 0.0f, e = 0.0f;
     __device__ __forceinline__ void add(float x) {
@@ -349,11 +407,12 @@ struct Sum2F32 {
         e = __fadd_rn(e, __fsub_rn(b, __fsub_rn(t, a)));
         s = t;
     }
-    // Adds the group to acc and restarts it; false when the group left the
-    // range where squares are exact and sums finite.
-    __device__ __forceinline__ bool flush(double& acc) {
+    // Adds the group to (acc, err) and restarts it; false when the group left
+    // the range where squares are exact and sums finite.
+    __device__ __forceinline__ bool flush(double& acc, float& err) {
         const bool ok = s < 0x1p100f;   // also false for inf and NaN
-        acc += double(s) + double(e);
+        acc += double(s);
+        err = __fadd_rn(err, e);
         s = 0.0f;
         e = 0.0f;
         return ok;
@@ -366,16 +425,16 @@ __device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
 // fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
 // after every group of U vectors.
 template <int U, typename FV, typename FE, typename FI>
-__device__ __forceinline__ void for_thread_grads(const TensorDev* __restrict__ tensors,
-                                                 const ChunkDev* __restrict__ chunks,
+__device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ chunks,
                                                  int32_t c0, int32_t c1, FV vec, FE elem,
                                                  FI after_iter) {
     for (int32_t ci = c0; ci < c1; ++ci) {
-        const ChunkDev ch = chunks[ci];
-        const uint16_t* g = static_cast<const uint16_t*>(tensors[ch.tensor].g) + ch.off;
+        const ChunkPtr ch = load_chunk(chunks + ci);
+        const uint16_t* g = static_cast<const uint16_t*>(ch.g);
+        const int64_t len = ch.len2 >> 1;
         int64_t done = 0;
-        if (ch.vec) {
-            const int64_t nvec = ch.len / kVec;
+        if (ch.len2 & 1) {
+            const int64_t nvec = len / kVec;
             for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
                 uint4 w[U];
 #pragma unroll
@@ -390,7 +449,7 @@ __device__ __forceinline__ void for_thread_grads(const TensorDev* __restrict__ t
             }
             done = nvec * kVec;
         }
-        for (int64_t i = done + threadIdx.x; i < ch.len; i += kBlock) elem(g[i]);
+        for (int64_t i = done + threadIdx.x; i < len; i += kBlock) elem(g[i]);
     }
 }
 
@@ -411,22 +470,22 @@ __device__ __forceinline__ double block_sum(double x) {
 
 // Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
 // same partition as the update (so the result depends only on the plan).
-// Fast path: error-free fp32 group sums of the exact squares, flushed to fp64
-// every 32 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
+// Fast path: error-free fp32 group sums of the exact squares, flushed every
+// 64 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
 // inf or NaN gradients) recomputes its elements in fp64, which also decides
 // the non-finite flag.
 __global__ void __launch_bounds__(kBlock)
-norm_partial_kernel(const TensorDev* __restrict__ tensors,
-                    const ChunkDev* __restrict__ chunks,
+norm_partial_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin,
                     double* __restrict__ partial, int32_t* __restrict__ flag) {
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
     Sum2F32 grp;
-    double tot = 0.0;
+    double acc = 0.0;
+    float err = 0.0f;
     bool in_range = true;
     uint32_t nz = 0;
-    for_thread_grads<4>(
-        tensors, chunks, c0, c1,
+    for_thread_grads<8>(
+        chunks, c0, c1,
         [&](const uint4& w) {
             nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
             grp.add(sq(bf16_lo(w.x)));
@@ -441,32 +500,33 @@ norm_partial_kernel(const TensorDev* __restrict__ tensors,
         [&](uint16_t h) {
             nz |= h & 0x7fffu;
             grp.add(sq(from_bf16(h)));
-            in_range &= grp.flush(tot);
+            in_range &= grp.flush(acc, err);
         },
-        [&]() { in_range &= grp.flush(tot); });
-    in_range &= grp.flush(tot);
+        [&]() { in_range &= grp.flush(acc, err); });
+    in_range &= grp.flush(acc, err);
+    double tot = acc + double(err);
     bool bad = false;
     if (!in_range || (nz != 0 && tot < 0x1p-100)) {
-        double acc = 0.0;
+        double exact = 0.0;
         for_thread_grads<1>(
-            tensors, chunks, c0, c1,
+            chunks, c0, c1,
             [&](const uint4& w) {
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
                     bad |= !isfinite(lo) || !isfinite(hi);
-                    acc += lo * lo;
-                    acc += hi * hi;
+                    exact += lo * lo;
+                    exact += hi * hi;
                 }
             },
             [&](uint16_t h) {
                 const double x = from_bf16(h);
                 bad |= !isfinite(x);
-                acc += x * x;
+                exact += x * x;
             },
             [&]() {});
-        tot = acc;
+        tot = exact;
     }
     tot = block_sum(tot);
     const int any = __syncthreads_or(bad);
@@ -586,6 +646,15 @@ struct DeviceGuard {
 
 }  // namespace
 
+// One partition of the plan's list on the device: the chunk descriptors of
+// `grid` CTAs and where each CTA's run of chunks begins.
+struct DevPartition {
+    int32_t grid = 0;
+    int64_t n_chunks = 0;
+    ChunkPtr* chunks = nullptr;
+    int32_t* cta_begin = nullptr;
+};
+
 struct adamw_plan {
     int device = 0;
     int32_t mode = 0;
@@ -593,12 +662,10 @@ struct adamw_plan {
     int32_t n_tensors = 0;
     int64_t total = 0;
     int64_t scalar_elems = 0;
-    int32_t grid = 0;
-    int64_t n_chunks = 0;
     void* block = nullptr;  // one device allocation holding everything below
-    TensorDev* tensors = nullptr;
-    ChunkDev* chunks = nullptr;
-    int32_t* cta_begin = nullptr;
+    TensorDev* tensors = nullptr;  // the uploaded tensor table
+    DevPartition upd;              // update kernel
+    DevPartition nrm;              // norm partial kernel (its own grid)
     double* partial = nullptr;
     int32_t* flag = nullptr;
     NormOut* norm = nullptr;
@@ -611,8 +678,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 template <int MODE, int K>
 cudaError_t launch_update(const adamw_plan* P, const StepScalars& s, int32_t* report,
                           cudaStream_t st) {
-    adamw_update_kernel<MODE, K><<<P->grid, kBlock, 0, st>>>(P->tensors, P->chunks, P->cta_begin,
-                                                             s, P->norm, report);
+    adamw_update_kernel<MODE, K><<<P->upd.grid, kBlock, 0, st>>>(P->upd.chunks, P->upd.cta_begin,
+                                                                 s, P->norm, report);
     return cudaGetLastError();
 }
 
@@ -630,11 +697,11 @@ cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& 
 
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
                         int32_t* user_flag, cudaStream_t st) {
-    norm_partial_kernel<<<P->grid, kBlock, 0, st>>>(P->tensors, P->chunks, P->cta_begin,
-                                                    P->partial, P->flag);
+    norm_partial_kernel<<<P->nrm.grid, kBlock, 0, st>>>(P->nrm.chunks, P->nrm.cta_begin,
+                                                        P->partial, P->flag);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    norm_finalize_kernel<<<1, kBlock, 0, st>>>(P->partial, P->flag, P->grid, max_grad_norm,
+    norm_finalize_kernel<<<1, kBlock, 0, st>>>(P->partial, P->flag, P->nrm.grid, max_grad_norm,
                                                P->norm, user_norm, user_flag);
     return cudaGetLastError();
 }
@@ -657,17 +724,26 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int occ = di.occ[mode][kPlain];
     for (int k = 0; k < 3; ++k) occ = occ < di.occ[mode][k] ? occ : di.occ[mode][k];
-    if (flags & ADAMW_PLAN_NORM) occ = occ < di.occ_norm ? occ : di.occ_norm;
     if (occ < 1) occ = 1;
+    const int occ_norm = di.occ_norm > 0 ? di.occ_norm : 1;
 
     int64_t total = 0;
     for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;
     const int32_t grid = choose_grid(total, di.sms * occ);
+    const int32_t grid_norm = (flags & ADAMW_PLAN_NORM) ? choose_grid(total, di.sms * occ_norm) : 0;
 
-    Partition part;
+    Partition part, part_norm;
+    std::vector<ChunkPtr> cp, cp_norm;
     if (grid > 0) {
-        rc = build_partition(host_table, n_tensors, mode, grid, &part);
+        rc = build_partition(host_table, n_tensors, mode, grid, update_tile_elems(total, grid),
+                             &part);
         if (rc != ADAMW_OK) return rc;
+        chunk_pointers(host_table, mode, part, &cp);
+    }
+    if (grid_norm > 0) {
+        rc = build_partition(host_table, n_tensors, mode, grid_norm, 0, &part_norm);
+        if (rc != ADAMW_OK) return rc;
+        chunk_pointers(host_table, mode, part_norm, &cp_norm);
     }
 
     adamw_plan* P = new adamw_plan();
@@ -677,16 +753,20 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->n_tensors = n_tensors;
     P->total = total;
     P->scalar_elems = part.scalar_elems;
-    P->grid = grid;
-    P->n_chunks = int64_t(part.chunks.size());
+    P->upd.grid = grid;
+    P->upd.n_chunks = int64_t(cp.size());
+    P->nrm.grid = grid_norm;
+    P->nrm.n_chunks = int64_t(cp_norm.size());
 
     // Layout of the single allocation.
     size_t off = 0;
     const size_t o_t = off; off = align_up(off + sizeof(TensorDev) * size_t(n_tensors), 256);
-    const size_t o_c = off; off = align_up(off + sizeof(ChunkDev) * part.chunks.size(), 256);
+    const size_t o_c = off; off = align_up(off + sizeof(ChunkPtr) * cp.size(), 256);
     const size_t o_b = off; off = align_up(off + sizeof(int32_t) * (size_t(grid) + 1), 256);
-    const size_t o_p = off; off = align_up(off + sizeof(double) * size_t(grid), 256);
-    const size_t o_f = off; off = align_up(off + sizeof(int32_t) * size_t(grid), 256);
+    const size_t o_cn = off; off = align_up(off + sizeof(ChunkPtr) * cp_norm.size(), 256);
+    const size_t o_bn = off; off = align_up(off + sizeof(int32_t) * (size_t(grid_norm) + 1), 256);
+    const size_t o_p = off; off = align_up(off + sizeof(double) * size_t(grid_norm), 256);
+    const size_t o_f = off; off = align_up(off + sizeof(int32_t) * size_t(grid_norm), 256);
     const size_t o_n = off; off = align_up(off + sizeof(NormOut), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
@@ -695,24 +775,27 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     }
     char* b = static_cast<char*>(P->block);
     P->tensors = reinterpret_cast<TensorDev*>(b + o_t);
-    P->chunks = reinterpret_cast<ChunkDev*>(b + o_c);
-    P->cta_begin = reinterpret_cast<int32_t*>(b + o_b);
+    P->upd.chunks = reinterpret_cast<ChunkPtr*>(b + o_c);
+    P->upd.cta_begin = reinterpret_cast<int32_t*>(b + o_b);
+    P->nrm.chunks = reinterpret_cast<ChunkPtr*>(b + o_cn);
+    P->nrm.cta_begin = reinterpret_cast<int32_t*>(b + o_bn);
     P->partial = reinterpret_cast<double*>(b + o_p);
     P->flag = reinterpret_cast<int32_t*>(b + o_f);
     P->norm = reinterpret_cast<NormOut*>(b + o_n);
 
+    auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
+        return bytes == 0 || cuda_ok(cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice), what);
+    };
     bool ok = cuda_ok(cudaMemset(P->block, 0, off), "cudaMemset");
-    if (ok && n_tensors > 0)
-        ok = cuda_ok(cudaMemcpy(P->tensors, host_table, sizeof(TensorDev) * size_t(n_tensors),
-                                cudaMemcpyHostToDevice), "cudaMemcpy(table)");
-    if (ok && !part.chunks.empty())
-        ok = cuda_ok(cudaMemcpy(P->chunks, part.chunks.data(),
-                                sizeof(ChunkDev) * part.chunks.size(), cudaMemcpyHostToDevice),
-                     "cudaMemcpy(chunks)");
-    if (ok && grid > 0)
-        ok = cuda_ok(cudaMemcpy(P->cta_begin, part.cta_begin.data(),
-                                sizeof(int32_t) * (size_t(grid) + 1), cudaMemcpyHostToDevice),
-                     "cudaMemcpy(cta_begin)");
+    ok = ok && up(P->tensors, host_table, sizeof(TensorDev) * size_t(n_tensors), "cudaMemcpy(table)");
+    ok = ok && up(P->upd.chunks, cp.data(), sizeof(ChunkPtr) * cp.size(), "cudaMemcpy(chunks)");
+    ok = ok && (grid == 0 || up(P->upd.cta_begin, part.cta_begin.data(),
+                                sizeof(int32_t) * (size_t(grid) + 1), "cudaMemcpy(cta_begin)"));
+    ok = ok && up(P->nrm.chunks, cp_norm.data(), sizeof(ChunkPtr) * cp_norm.size(),
+                  "cudaMemcpy(norm chunks)");
+    ok = ok && (grid_norm == 0 || up(P->nrm.cta_begin, part_norm.cta_begin.data(),
+                                     sizeof(int32_t) * (size_t(grid_norm) + 1),
+                                     "cudaMemcpy(norm cta_begin)"));
     if (!ok) {
         cudaFree(P->block);
         delete P;
@@ -738,7 +821,7 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
         return ADAMW_ERR_CUDA;
     }
 
-    if (plan->grid == 0) {  // empty list: nothing to update, norm is 0
+    if (plan->upd.grid == 0) {  // empty list: nothing to update, norm is 0
         if (d_grad_norm && !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
             return ADAMW_ERR_CUDA;
         if (d_nonfinite && !cuda_ok(cudaMemsetAsync(d_nonfinite, 0, sizeof(int32_t), st), "memset"))
@@ -774,7 +857,7 @@ extern "C" int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm, int32_t* 
         set_cuda_error("cudaSetDevice", cudaGetErrorString(cudaGetLastError()));
         return ADAMW_ERR_CUDA;
     }
-    if (plan->grid == 0) {
+    if (plan->nrm.grid == 0) {
         if (d_grad_norm && !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
             return ADAMW_ERR_CUDA;
         if (d_nonfinite && !cuda_ok(cudaMemsetAsync(d_nonfinite, 0, sizeof(int32_t), st), "memset"))
@@ -805,9 +888,10 @@ extern "C" int adamw_plan_get_info(adamw_plan_t plan, adamw_plan_info_t* out) {
     out->mode = plan->mode;
     out->n_tensors = plan->n_tensors;
     out->total_elems = plan->total;
-    out->grid = plan->grid;
+    out->grid = plan->upd.grid;
     out->block = kBlock;
-    out->n_chunks = plan->n_chunks;
+    out->n_chunks = plan->upd.n_chunks;
+    out->norm_grid = plan->nrm.grid;
     out->scalar_elems = plan->scalar_elems;
     out->device = plan->device;
     out->has_norm = (plan->flags & ADAMW_PLAN_NORM) ? 1 : 0;

@@ -5,9 +5,10 @@
 // The pages name the multi-tensor optimizer only ("Distributed optimizer
 // support for BERT", NeMo PR #5305, "Usage": fused_adam / distributed_fused_adam
 // update a whole model's parameter list in fused launches); this partition is
-// this library's own design: the flattened element space is cut into `grid`
-// nearly equal contiguous ranges, one per persistent CTA, so that every CTA
-// streams the same number of bytes whatever the tensor sizes.
+// this library's own design.  Every CTA of a persistent grid gets the same
+// number of elements whatever the tensor sizes: large lists are cut into
+// fixed tiles dealt round-robin (the grid sweeps the buffers together), small
+// lists and the norm pass into one contiguous range per CTA.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -109,11 +110,16 @@ int32_t choose_grid(int64_t total, int32_t max_grid) {
     return int32_t(want < max_grid ? want : max_grid);
 }
 
+int64_t update_tile_elems(int64_t total, int32_t grid) {
+    if (kTileElems <= 0 || grid <= 0) return 0;
+    return (total >= 2 * int64_t(grid) * kTileElems) ? kTileElems : 0;
+}
+
 int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
-                    int32_t grid, Partition* out) {
+                    int32_t grid, int64_t tile_elems, Partition* out) {
     int rc = validate_table(table, n, mode);
     if (rc != ADAMW_OK) return rc;
-    if (!out || grid < 0) return ADAMW_ERR_INVALID_ARG;
+    if (!out || grid < 0 || tile_elems < 0 || tile_elems % kVec) return ADAMW_ERR_INVALID_ARG;
     Partition& P = *out;
     P = Partition();
     for (int32_t k = 0; k < n; ++k) P.total += table[k].numel;
@@ -142,9 +148,35 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
     P.cta_begin.assign(size_t(grid) + 1, 0);
     if (P.total == 0) return ADAMW_OK;
 
-    // Even split of the flattened element space; cuts inside a vector body
-    // fall on multiples of kVec from the body's start so every chunk of it
-    // starts 16-byte aligned.
+    if (tile_elems > 0) {
+        // Interleaved: cut every segment into tiles of tile_elems (a multiple
+        // of kVec, so vector tiles stay 16-byte aligned) and deal the tiles
+        // round-robin to the CTAs in list order, so that at any moment the
+        // whole grid streams one narrow window of each buffer.
+        std::vector<ChunkDev> pieces;
+        for (const Seg& s : segs)
+            for (int64_t pos = 0; pos < s.len; pos += tile_elems)
+                pieces.push_back({s.k, s.vec, s.off + pos,
+                                  (s.len - pos < tile_elems) ? s.len - pos : tile_elems});
+        std::vector<int64_t> count(size_t(grid) + 1, 0);
+        for (size_t j = 0; j < pieces.size(); ++j) ++count[j % grid + 1];
+        for (int32_t b = 0; b < grid; ++b) count[b + 1] += count[b];
+        P.chunks.resize(pieces.size());
+        P.chunk_cta.resize(pieces.size());
+        std::vector<int64_t> fill(count.begin(), count.end() - 1);
+        for (size_t j = 0; j < pieces.size(); ++j) {
+            const int32_t b = int32_t(j % grid);
+            P.chunks[fill[b]] = pieces[j];
+            P.chunk_cta[fill[b]] = b;
+            ++fill[b];
+        }
+        for (int32_t b = 0; b <= grid; ++b) P.cta_begin[b] = int32_t(count[b]);
+        return ADAMW_OK;
+    }
+
+    // Contiguous: an even split of the flattened element space; cuts inside
+    // a vector body fall on multiples of kVec from the body's start so every
+    // chunk of it starts 16-byte aligned.
     const int64_t target = ((P.total + grid - 1) / grid + kVec - 1) / kVec * kVec;
     int32_t cta = 0;
     int64_t filled = 0;
@@ -176,6 +208,26 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
     return ADAMW_OK;
 }
 
+void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& P,
+                    std::vector<ChunkPtr>* out) {
+    const int64_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    out->resize(P.chunks.size());
+    for (size_t i = 0; i < P.chunks.size(); ++i) {
+        const ChunkDev& c = P.chunks[i];
+        const adamw_tensor_t& t = table[c.tensor];
+        auto at = [&](const void* base, int64_t es) {
+            return static_cast<void*>(static_cast<char*>(const_cast<void*>(base)) + c.off * es);
+        };
+        ChunkPtr& d = (*out)[i];
+        d.p = at(t.param, wide);
+        d.g = at(t.grad, 2);
+        d.m = at(t.exp_avg, wide);
+        d.v = at(t.exp_avg_sq, wide);
+        d.a = at(t.aux, 2);
+        d.len2 = 2 * c.len + c.vec;
+    }
+}
+
 }  // namespace adamw
 
 // ------------------------------------------------------- host-only ABI ----
@@ -186,8 +238,13 @@ extern "C" int adamw_plan_chunks(const adamw_tensor_t* host_table,
                                  int64_t* n_out) {
     if (!n_out || cap < 0 || (cap > 0 && !out) || grid < 1)
         return ADAMW_ERR_INVALID_ARG;
+    int rc = adamw::validate_table(host_table, n_tensors, mode);
+    if (rc != ADAMW_OK) return rc;
+    int64_t total = 0;
+    for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;
     adamw::Partition P;
-    int rc = adamw::build_partition(host_table, n_tensors, mode, grid, &P);
+    rc = adamw::build_partition(host_table, n_tensors, mode, grid,
+                                adamw::update_tile_elems(total, grid), &P);
     if (rc != ADAMW_OK) return rc;
     *n_out = int64_t(P.chunks.size());
     if (int64_t(P.chunks.size()) > cap) return ADAMW_ERR_TOO_LARGE;

@@ -131,6 +131,12 @@ WORKLOADS: dict[str, Workload] = {
         max_grad_norm=1.0, g_std=1e-2, inf_at=(3, 200, 12345),
         description="OPT-1.3b tensor list, fp32 master + global-norm clip 1.0, "
                     "+inf injected at step 3"),
+    # profiling-size case of the clipped mixed step (2 GB of state, > L2)
+    "opt125m_mixed_clip": Workload(
+        "opt125m_mixed_clip", MODE_MIXED, OPT_125M, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+        max_grad_norm=1.0, g_std=1e-2, heavy_tail=True,
+        description="OPT-125m tensor list, fp32 master + global-norm clip 1.0"),
 }
 
 

@@ -102,12 +102,14 @@ typedef struct {
     int32_t mode;
     int32_t n_tensors;
     int64_t total_elems;   /* sum of numel                                  */
-    int32_t grid;          /* CTAs of the update and norm-partial kernels   */
+    int32_t grid;          /* CTAs of the update kernel                     */
     int32_t block;         /* threads per CTA                               */
     int64_t n_chunks;      /* pieces of tensors handed to CTAs              */
     int64_t scalar_elems;  /* elements on the unvectorised path             */
     int32_t device;        /* CUDA device the plan lives on                 */
     int32_t has_norm;      /* ADAMW_PLAN_NORM was given                     */
+    int32_t norm_grid;     /* CTAs of the norm-partial kernel (0: no norm)  */
+    int32_t pad_;
 } adamw_plan_info_t;
 
 /* One piece of a tensor assigned to one CTA (host-side view of the plan). */
@@ -121,9 +123,10 @@ typedef struct {
 } adamw_chunk_t;
 
 /* Builds a plan on the current CUDA device: validates the list, splits the
- * flattened element space evenly over a persistent grid (grid = SM count x
- * resident CTAs per SM, fewer for small lists), uploads the tensor table and
- * the chunk table, and (with ADAMW_PLAN_NORM) allocates the norm workspace.
+ * flattened element space over a persistent grid (grid = SM count x resident
+ * CTAs per SM, fewer for small lists), uploads the tensor table and the chunk
+ * table, and (with ADAMW_PLAN_NORM) builds the norm kernel's own partition
+ * and allocates the norm workspace.
  * Synchronous (it allocates and copies).  host_table is read during the call
  * only.  On error *out is left NULL and nothing stays allocated.
  * Errors: INVALID_ARG (NULL out or table with n_tensors > 0, n_tensors < 0,
@@ -134,8 +137,9 @@ int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_tensors,
 /* One optimizer step over every tensor of the plan, asynchronous on stream.
  * step = t >= 1, the number of applied updates including this one (a step
  * skipped for a non-finite gradient does not count).
- * d_grad_norm (nullable, device fp64): receives the global gradient L2 norm
- *   when clipping is on.
+ * d_grad_norm (nullable, device fp64): receives the global gradient L2 norm.
+ *   Clipping computes it anyway; without clipping a non-NULL d_grad_norm
+ *   costs one extra read of every gradient (and needs ADAMW_PLAN_NORM).
  * d_nonfinite (nullable, device int32): receives 1 if any gradient element is
  *   inf or NaN, else 0.  With clipping on, a 1 means the step wrote nothing.
  *   Without clipping the state is still updated (non-finite values propagate)
@@ -162,7 +166,8 @@ int adamw_plan_destroy(adamw_plan_t plan);
 int adamw_plan_get_info(adamw_plan_t plan, adamw_plan_info_t* out);
 
 /* Host-only (needs no GPU): the partition adamw_plan_create would build for
- * the given list on a grid of `grid` CTAs.  Writes up to `cap` chunks to out
+ * the given list on a grid of `grid` CTAs (the update kernel's grid is
+ * adamw_plan_info_t.grid, the norm kernel's norm_grid).  Writes up to `cap` chunks to out
  * (out may be NULL when cap is 0) and the full count to *n_out.
  * Errors: INVALID_ARG, MISALIGNED, TOO_LARGE (cap smaller than the count;
  * *n_out still holds the count). */

@@ -277,7 +277,7 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
         log.append((k, skipped, oskipped, flag, bad, gnorm, norm))
         if skipped != oskipped or flag != bad:
             rep.failures.append(f"step {k}: skip/flag gpu=({skipped},{flag}) oracle=({oskipped},{bad})")
-        if clip and abs(gnorm - norm) > 1e-9 * norm:
+        if clip and abs(gnorm - norm) > 1e-12 * norm:
             rep.failures.append(f"step {k}: norm gpu {gnorm!r} oracle {norm!r}")
     got = dict(param=wide(st.param[it]), exp_avg=wide(st.exp_avg[it]),
                exp_avg_sq=wide(st.exp_avg_sq[it]), aux=to_u16(st.aux[it]))
