@@ -88,11 +88,12 @@ def load() -> ctypes.CDLL:
             L.adamw_step_scalars.argtypes = [ctypes.POINTER(adamw_hparams_t), i64,
                                              ctypes.POINTER(ctypes.c_float)]
             L.adamw_copy_probe.argtypes = [vp, vp, i64, vp]
+            L.adamw_grad_norm_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, vp, vp, vp]
             L.adamw_status_string.argtypes = [ctypes.c_int]
             L.adamw_status_string.restype = ctypes.c_char_p
             for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm",
                          "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
-                         "adamw_step_scalars", "adamw_copy_probe"):
+                         "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -136,6 +137,19 @@ def adamw_grad_norm(plan: int, d_grad_norm: int = 0, d_nonfinite: int = 0,
                     stream: int = 0) -> None:
     _check(load().adamw_grad_norm(plan, d_grad_norm or None, d_nonfinite or None,
                                   stream or None), "adamw_grad_norm")
+
+
+NOALLOC_MAX_TENSORS = 4096
+
+
+def adamw_grad_norm_noalloc(entries, d_grad_norm: int = 0, d_nonfinite: int = 0,
+                            stream: int = 0) -> None:
+    """Global gradient norm of a tensor list without any device allocation
+    (no plan; only .grad and .numel of each entry are read).  For callers
+    that cannot call cudaMalloc; see include/adamw_sm.h."""
+    arr, n = _table(entries)
+    _check(load().adamw_grad_norm_noalloc(arr, n, d_grad_norm or None, d_nonfinite or None,
+                                          stream or None), "adamw_grad_norm_noalloc")
 
 
 def adamw_plan_destroy(plan: int) -> None:

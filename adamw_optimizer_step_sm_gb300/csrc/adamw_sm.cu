@@ -916,3 +916,191 @@ extern "C" int adamw_copy_probe(void* dst, const void* src, int64_t bytes, adamw
         static_cast<uint4*>(dst), static_cast<const uint4*>(src), n);
     return cuda_ok(cudaGetLastError(), "copy launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
 }
+
+// ------------------------------------------- global norm without allocation --
+//
+// adamw_grad_norm_noalloc is adamw_grad_norm for callers that cannot allocate
+// device memory.  Instead of a plan's cudaMalloc'd workspace it uses one
+// file-scope __device__ array (the uploaded tensor list, the per-CTA partials
+// and flags, and the finalize record), so a call allocates nothing.  Every GPU
+// that loads this library holds the array until the process exits.
+
+namespace {
+
+constexpr int kNoAllocMaxCtas = 1024;
+constexpr size_t kNoAllocTableOff = 0;
+constexpr size_t kNoAllocPartialOff =
+    (sizeof(adamw_tensor_t) * ADAMW_NOALLOC_MAX_TENSORS + 255) / 256 * 256;
+constexpr size_t kNoAllocFlagOff = kNoAllocPartialOff + sizeof(double) * kNoAllocMaxCtas;
+constexpr size_t kNoAllocOutOff = kNoAllocFlagOff + sizeof(int32_t) * kNoAllocMaxCtas;
+constexpr size_t kNoAllocBytes = (kNoAllocOutOff + sizeof(NormOut) + 255) / 256 * 256;
+
+// The scratch (about 208 KiB).  Host code never uses this name as an address:
+// on the host it is only a stand-in; noalloc_device() asks the runtime for the
+// device address.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char* base = nullptr;  // device address of g_noalloc_scratch
+    int grid = 0;
+};
+
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Stage 1 without a chunk table: tensor by tensor in list order, every thread
+// of the grid takes a fixed share of each tensor (an element of the head that
+// 16-byte aligns g, vectors strided by the whole grid, an element of the
+// tail).  Sums as in norm_partial_kernel: error-free fp32 groups of exact
+// squares, an fp64 recomputation for threads whose groups leave the safe range.
+__global__ void __launch_bounds__(kBlock)
+norm_partial_noalloc_kernel(const adamw_tensor_t* __restrict__ table, int32_t n,
+                            double* __restrict__ partial, int32_t* __restrict__ flag) {
+    const int64_t gt = int64_t(blockIdx.x) * kBlock + threadIdx.x;
+    const int64_t T = int64_t(gridDim.x) * kBlock;
+    constexpr int U = 4;
+
+    auto walk = [&](auto vec, auto elem, auto after_iter) {
+        for (int32_t k = 0; k < n; ++k) {
+            const uint16_t* g = static_cast<const uint16_t*>(table[k].grad);
+            const int64_t len = table[k].numel;
+            if (len <= 0) continue;
+            int64_t h = int64_t((16 - (reinterpret_cast<uintptr_t>(g) & 15)) & 15) >> 1;
+            if (h > len) h = len;
+            if (gt < h) elem(g[gt]);
+            const uint16_t* gv = g + h;
+            const int64_t nvec = (len - h) / kVec;
+            for (int64_t base = gt; base < nvec; base += T * U) {
+                uint4 w[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (base + u * T < nvec) w[u] = ld16(gv + (base + u * T) * kVec);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (base + u * T < nvec) vec(w[u]);
+                after_iter();
+            }
+            const int64_t t0 = h + nvec * kVec;
+            if (gt < len - t0) elem(g[t0 + gt]);
+        }
+    };
+
+    Sum2F32 grp;
+    double acc = 0.0;
+    float err = 0.0f;
+    bool in_range = true;
+    uint32_t nz = 0;
+    walk(
+        [&](const uint4& w) {
+            nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
+            grp.add(sq(bf16_lo(w.x)));
+            grp.add(sq(bf16_hi(w.x)));
+            grp.add(sq(bf16_lo(w.y)));
+            grp.add(sq(bf16_hi(w.y)));
+            grp.add(sq(bf16_lo(w.z)));
+            grp.add(sq(bf16_hi(w.z)));
+            grp.add(sq(bf16_lo(w.w)));
+            grp.add(sq(bf16_hi(w.w)));
+        },
+        [&](uint16_t hb) {
+            nz |= hb & 0x7fffu;
+            grp.add(sq(from_bf16(hb)));
+            in_range &= grp.flush(acc, err);
+        },
+        [&]() { in_range &= grp.flush(acc, err); });
+    in_range &= grp.flush(acc, err);
+    double tot = acc + double(err);
+    bool bad = false;
+    if (!in_range || (nz != 0 && tot < 0x1p-100)) {
+        double exact = 0.0;
+        walk(
+            [&](const uint4& w) {
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
+                    bad |= !isfinite(lo) || !isfinite(hi);
+                    exact += lo * lo;
+                    exact += hi * hi;
+                }
+            },
+            [&](uint16_t hb) {
+                const double x = from_bf16(hb);
+                bad |= !isfinite(x);
+                exact += x * x;
+            },
+            [&]() {});
+        tot = exact;
+    }
+    tot = block_sum(tot);
+    const int any = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        partial[blockIdx.x] = tot;
+        flag[blockIdx.x] = any;
+    }
+}
+
+// Set-up, once per device, with that device current: the scratch's device
+// address and the grid size.
+int noalloc_device(int dev, NoAllocDevice* out) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return ADAMW_ERR_TOO_LARGE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        if (!cuda_ok(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress"))
+            return ADAMW_ERR_CUDA;
+        int sms = 0, occ = 0;
+        if (!cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                     "cudaDeviceGetAttribute") ||
+            !cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &occ, norm_partial_noalloc_kernel, kBlock, 0), "occupancy"))
+            return ADAMW_ERR_CUDA;
+        const int grid = sms * (occ > 0 ? occ : 1);
+        d.base = static_cast<unsigned char*>(ptr);
+        d.grid = grid < kNoAllocMaxCtas ? grid : kNoAllocMaxCtas;
+        d.ready = true;
+    }
+    *out = d;
+    return ADAMW_OK;
+}
+
+}  // namespace
+
+extern "C" int adamw_grad_norm_noalloc(const adamw_tensor_t* host_table, int32_t n_tensors,
+                                       double* d_grad_norm, int32_t* d_nonfinite,
+                                       adamw_stream_t stream) {
+    if (n_tensors < 0 || (n_tensors > 0 && !host_table)) return ADAMW_ERR_INVALID_ARG;
+    if (n_tensors > ADAMW_NOALLOC_MAX_TENSORS) return ADAMW_ERR_TOO_LARGE;
+    for (int32_t k = 0; k < n_tensors; ++k) {
+        const adamw_tensor_t& t = host_table[k];
+        if (t.numel < 0 || (t.numel > 0 && !t.grad)) return ADAMW_ERR_INVALID_ARG;
+        if (t.numel > 0 && (reinterpret_cast<uintptr_t>(t.grad) & 1)) return ADAMW_ERR_MISALIGNED;
+    }
+    int dev = 0;
+    if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return ADAMW_ERR_CUDA;
+    NoAllocDevice d;
+    int rc = noalloc_device(dev, &d);
+    if (rc != ADAMW_OK) return rc;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    adamw_tensor_t* table = reinterpret_cast<adamw_tensor_t*>(d.base + kNoAllocTableOff);
+    double* partial = reinterpret_cast<double*>(d.base + kNoAllocPartialOff);
+    int32_t* flag = reinterpret_cast<int32_t*>(d.base + kNoAllocFlagOff);
+    NormOut* out = reinterpret_cast<NormOut*>(d.base + kNoAllocOutOff);
+    // Every CTA writes its partial and flag and the finalize writes the
+    // record on every call, so nothing in the scratch has to start at zero.
+    if (n_tensors > 0 &&
+        !cuda_ok(cudaMemcpyAsync(table, host_table, sizeof(adamw_tensor_t) * size_t(n_tensors),
+                                 cudaMemcpyHostToDevice, st), "cudaMemcpyAsync(table)"))
+        return ADAMW_ERR_CUDA;
+    norm_partial_noalloc_kernel<<<d.grid, kBlock, 0, st>>>(table, n_tensors, partial, flag);
+    if (!cuda_ok(cudaGetLastError(), "norm launch")) return ADAMW_ERR_CUDA;
+    norm_finalize_kernel<<<1, kBlock, 0, st>>>(partial, flag, d.grid, 0.0f, out, d_grad_norm,
+                                               d_nonfinite);
+    if (!cuda_ok(cudaGetLastError(), "finalize launch")) return ADAMW_ERR_CUDA;
+    return ADAMW_OK;
+}

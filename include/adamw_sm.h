@@ -187,6 +187,36 @@ int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step, float out5[5]);
 int adamw_copy_probe(void* dst, const void* src, int64_t bytes,
                      adamw_stream_t stream);
 
+/* Largest tensor list adamw_grad_norm_noalloc accepts. */
+#define ADAMW_NOALLOC_MAX_TENSORS 4096
+
+/* The global gradient L2 norm and non-finite flag of a tensor list, like
+ * adamw_grad_norm, for callers that cannot allocate device memory: code whose
+ * device memory is all handed to a caching allocator (a raw cudaMalloc then
+ * fails or fragments that pool), and code that must not synchronise the
+ * device (cudaMalloc and cudaFree may).  It needs no plan (plan creation
+ * allocates) and allocates nothing: its scratch is a fixed file-scope device
+ * array of about 208 KiB in this library, which every GPU that loads the
+ * library keeps until the process exits.  The source pages have no
+ * counterpart; this is a utility of this library.
+ * host_table: host array of n_tensors entries, read during the call only; only
+ *   .grad (device bf16, 2-byte aligned) and .numel are used.
+ * d_grad_norm (nullable, device fp64) and d_nonfinite (nullable, device
+ *   int32) receive the norm and the flag, as in adamw_grad_norm.
+ * The first call on a device sets that device up (looks up the scratch
+ * address and the grid size) with it current; make that first call before
+ * any stream capture.  All calls share the one scratch array, which keeps the
+ * last call's contents (nothing in it needs to start at zero): calls that
+ * overlap on the GPU, on any streams, race.  The sum runs in a fixed order
+ * for a given device, but not the order of adamw_grad_norm, so the two norms
+ * agree to fp64 rounding, not bit for bit.
+ * Errors: INVALID_ARG (n_tensors < 0, NULL table or grad with numel > 0,
+ * numel < 0), TOO_LARGE (n_tensors > ADAMW_NOALLOC_MAX_TENSORS, or a device
+ * index of 64 or more), MISALIGNED (odd grad address), CUDA. */
+int adamw_grad_norm_noalloc(const adamw_tensor_t* host_table, int32_t n_tensors,
+                            double* d_grad_norm, int32_t* d_nonfinite,
+                            adamw_stream_t stream);
+
 /* Text for a status code; for ADAMW_ERR_CUDA it also names the last CUDA
  * error seen by this thread.  Never NULL; valid until the next call from the
  * same thread. */
