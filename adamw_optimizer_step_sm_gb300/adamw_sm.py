@@ -29,6 +29,7 @@ ADAMW_ERR_MISALIGNED = -2
 ADAMW_ERR_CUDA = -3
 ADAMW_ERR_NO_NORM = -4
 ADAMW_ERR_TOO_LARGE = -5
+ADAMW_ERR_NOT_ACCESSIBLE = -6
 
 
 class AdamWError(RuntimeError):
@@ -213,9 +214,13 @@ class Plan:
         for k in range(n):
             ts = [x[k] for x in lists]
             numel = ts[0].numel()
-            for t, dt in zip(ts, want):
-                if not t.is_cuda or t.dtype != dt or not t.is_contiguous() or t.numel() != numel:
-                    raise TypeError(f"tensor {k}: want contiguous CUDA {dt} of {numel} elements")
+            for j, (t, dt) in enumerate(zip(ts, want)):
+                # gradients may live in pinned host memory (read over the
+                # CPU-GPU link); everything else on the device
+                where_ok = t.is_cuda or (j == 1 and t.is_pinned())
+                if not where_ok or t.dtype != dt or not t.is_contiguous() or t.numel() != numel:
+                    raise TypeError(f"tensor {k}: want contiguous CUDA {dt} of {numel} elements"
+                                    + (" (or pinned host memory)" if j == 1 else ""))
             entries.append(adamw_tensor_t(*(t.data_ptr() for t in ts), numel))
         self._keep = lists
         self.mode = mode

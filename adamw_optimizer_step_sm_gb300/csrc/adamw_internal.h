@@ -106,6 +106,9 @@ int32_t choose_grid(int64_t total, int32_t max_grid);
 // on `grid` CTAs (0: contiguous ranges).
 int64_t update_tile_elems(int64_t total, int32_t grid);
 
+// Every buffer of the list can be dereferenced by `device` (device_access.cpp).
+int check_device_access(const adamw_tensor_t* table, int32_t n, int device);
+
 // Remembers a CUDA error text for adamw_status_string (per host thread).
 void set_cuda_error(const char* where, const char* what);
 const char* last_cuda_error();

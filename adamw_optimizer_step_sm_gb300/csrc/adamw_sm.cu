@@ -718,6 +718,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int dev = 0;
     if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return ADAMW_ERR_CUDA;
+    rc = check_device_access(host_table, n_tensors, dev);
+    if (rc != ADAMW_OK) return rc;
     DeviceInfo di;
     rc = device_info(dev, &di);
     if (rc != ADAMW_OK) return rc;

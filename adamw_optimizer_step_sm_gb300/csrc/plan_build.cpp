@@ -281,6 +281,7 @@ extern "C" const char* adamw_status_string(int status) {
         case ADAMW_ERR_MISALIGNED: return "buffer not aligned to its element size";
         case ADAMW_ERR_NO_NORM: return "clipping or norm asked of a plan made without ADAMW_PLAN_NORM";
         case ADAMW_ERR_TOO_LARGE: return "size exceeds a documented limit";
+        case ADAMW_ERR_NOT_ACCESSIBLE: return "a buffer is not accessible from the plan's device";
         case ADAMW_ERR_CUDA:
             buf = std::string("CUDA error: ") + adamw::last_cuda_error();
             return buf.c_str();

@@ -254,6 +254,96 @@ def copy_ceiling(device, nbytes: int = 4 << 30, reps: int = 5) -> dict:
     return out
 
 
+def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
+    """The same metric end to end: every step copies that step's bf16
+    gradients from pinned host memory, runs the step and reads the non-finite
+    flag (4 bytes) back to the host, which decides whether the step counted.
+
+    Paths, all through the library's C ABI:
+      overlapped  two device gradient buffers; step k+1's host-to-device copy
+                  runs on a side stream while step k updates (the reported e2e)
+      serial      copy, then step, on one stream
+      zero_copy   the plan's gradient pointers are the pinned host buffer
+                  itself; the kernels read it over NVLink-C2C
+    """
+    N = w.total
+    k_e2e = max(2, min(args.steps, 10))
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    host_g = [torch.empty(grads[0].numel(), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    host_g[0].copy_(grads[0])
+    host_g[1].copy_(grads[1 % len(grads)])
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    host_flag = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    norm = torch.zeros(1, dtype=torch.float64, device=device)
+    state = {"t": t}
+    bufs = [grads[0], grads[1 % len(grads)]]
+    bplans = [plans[0], plans[1 % len(plans)]]
+
+    def finish_step():
+        host_flag.copy_(flag, non_blocking=True)
+        stream.synchronize()
+        if not (clip and int(host_flag.item())):
+            state["t"] += 1
+
+    def serial(i):
+        bufs[0].copy_(host_g[i % 2], non_blocking=True)
+        bplans[0].step(hp, state["t"] + 1, grad_norm=norm if clip else None, nonfinite=flag)
+        finish_step()
+
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def overlap_prime():
+        used[1].record(stream)
+        with torch.cuda.stream(side):
+            bufs[0].copy_(host_g[0], non_blocking=True)
+            copied[0].record(side)
+
+    def overlapped(i):
+        b, nb = i % 2, 1 - i % 2
+        side.wait_event(used[nb])            # buffer nb is free once step i-1 ended
+        with torch.cuda.stream(side):
+            bufs[nb].copy_(host_g[nb], non_blocking=True)
+            copied[nb].record(side)
+        stream.wait_event(copied[b])
+        bplans[b].step(hp, state["t"] + 1, grad_norm=norm if clip else None, nonfinite=flag)
+        used[b].record(stream)
+        finish_step()
+
+    v = st.views
+    zc_plan = A.Plan(v(st.param), v(host_g[0]), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux),
+                     w.mode, norm=clip)
+
+    def zero_copy(i):
+        zc_plan.step(hp, state["t"] + 1, grad_norm=norm if clip else None, nonfinite=flag)
+        finish_step()
+
+    out = {}
+    for name, fn, prime in (("overlapped", overlapped, overlap_prime), ("serial", serial, None),
+                            ("zero_copy", zero_copy, None)):
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if prime:
+            prime()
+        for i in range(k_e2e):
+            fn(i)
+        e1.record(stream)
+        e1.synchronize()
+        secs = reduce_max(e0.elapsed_time(e1) / 1e3, world, device)
+        out[name] = {"value": world * N * k_e2e / secs, "ms_per_step": secs / k_e2e * 1e3}
+    zc_plan.close()
+    torch.cuda.synchronize(device)
+    best = out["overlapped"]
+    return {"value": best["value"], "unit": UNIT, "h2d_bytes_per_step": int(N * 2),
+            "d2h_bytes_per_step": 4, "ms_per_step": best["ms_per_step"], "steps": k_e2e,
+            "path": "bf16 grads in pinned host memory, copied to the device on a side stream "
+                    "while the previous step runs (double-buffered); flag read back every step",
+            "paths": out, "_t": state["t"]}
+
+
 def run_gpu(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -324,33 +414,12 @@ def run_gpu(args):
     avg_launch = sum(per_step) / len(per_step)
     achieved = bpp * N / avg_launch / 1e9
 
-    # end to end through the public API: grads copied in from pinned host
-    # memory every step, the step, and the non-finite flag read back
+    # end to end through the public API, gradients arriving in pinned host
+    # memory every step and the non-finite flag read back every step
     e2e = None
     if not args.no_e2e:
-        host_g = torch.empty(grads[0].numel(), dtype=torch.bfloat16, pin_memory=True)
-        host_g.copy_(grads[0])
-        host_flag = torch.zeros(1, dtype=torch.int32, pin_memory=True)
-        k_e2e = max(1, min(args.steps, 10))
-        torch.cuda.synchronize(device)
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(k_e2e):
-            grads[0].copy_(host_g, non_blocking=True)
-            plans[0].step(hp, t + 1, grad_norm=norm if clip else None, nonfinite=flag)
-            host_flag.copy_(flag, non_blocking=True)
-            stream.synchronize()
-            if int(host_flag.item()) and clip:
-                continue
-            t += 1
-        e1.record(stream)
-        e1.synchronize()
-        e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, world, device)
-        e2e = {"value": world * N * k_e2e / e2e_s, "unit": UNIT,
-               "h2d_bytes_per_step": int(grads[0].numel() * 2), "d2h_bytes_per_step": 4,
-               "ms_per_step": e2e_s / k_e2e * 1e3}
-        del host_g
+        e2e = run_e2e(args, w, st, grads, plans, hp, clip, t, world, device)
+        t = e2e.pop("_t")
 
     peaks = load_peaks()
     out = {

@@ -63,10 +63,17 @@ typedef struct CUstream_st* adamw_stream_t;
 #define ADAMW_ERR_CUDA (-3)        /* a CUDA call failed; see status string */
 #define ADAMW_ERR_NO_NORM (-4)     /* clipping asked of a plan without norm */
 #define ADAMW_ERR_TOO_LARGE (-5)   /* a size exceeds a documented limit     */
+#define ADAMW_ERR_NOT_ACCESSIBLE (-6) /* a buffer the device cannot reach   */
 
-/* One tensor of the list.  Every pointer is a device pointer owned by the
- * caller; the five buffers of one tensor hold `numel` elements each and must
- * not overlap one another (different tensors may not overlap either).
+/* One tensor of the list.  Every pointer is owned by the caller and must be
+ * dereferenceable by the plan's device: device memory of that device, managed
+ * memory, pinned host memory mapped at the same address (cudaHostAlloc under
+ * unified addressing), or pageable host memory on devices with pageable-memory
+ * access (Grace systems).  Host-resident buffers are read and written by the
+ * kernels over the CPU-GPU link (NVLink-C2C on GB300): a gradient list kept in
+ * pinned host memory needs no separate host-to-device copy.  The five buffers
+ * of one tensor hold `numel` elements each and must not overlap one another
+ * (different tensors may not overlap either).
  *   param       bf16 p (read/write)        | fp32 master (read/write)
  *   grad        bf16 g (read only)         | bf16 g (read only)
  *   exp_avg     bf16 m (read/write)        | fp32 m (read/write)
@@ -130,7 +137,9 @@ typedef struct {
  * Synchronous (it allocates and copies).  host_table is read during the call
  * only.  On error *out is left NULL and nothing stays allocated.
  * Errors: INVALID_ARG (NULL out or table with n_tensors > 0, n_tensors < 0,
- * bad mode, numel < 0, NULL buffer with numel > 0), MISALIGNED, CUDA. */
+ * bad mode, numel < 0, NULL buffer with numel > 0), MISALIGNED,
+ * NOT_ACCESSIBLE (a buffer the current device cannot dereference: another
+ * device's memory, unmapped host memory), CUDA. */
 int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_tensors,
                       int32_t mode, int32_t flags, adamw_plan_t* out);
 

@@ -228,3 +228,54 @@ def test_steps_on_a_side_stream_and_a_second_plan():
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     a.plan.close()
     b.plan.close()
+
+
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_MIXED, 1.0)])
+def test_gradients_in_pinned_host_memory(mode, clip):
+    """A plan whose gradients live in pinned host memory (read by the kernels
+    over the CPU-GPU link) gives the same bytes as one with device gradients."""
+    w = _small("hostgrad", mode=mode, max_grad_norm=clip, steps=3)
+    a = H.GpuRun(w)
+    b_state = W.make_state(w, "cuda")
+    host_g = torch.zeros(a.g.numel(), dtype=torch.bfloat16, pin_memory=True)
+    v = b_state.views
+    plan_b = A.Plan(v(b_state.param), v(host_g), v(b_state.exp_avg), v(b_state.exp_avg_sq),
+                    v(b_state.aux), mode, norm=True)
+    hp, _ = H.hp_pair(w)
+    norm_a = torch.zeros(1, dtype=torch.float64, device="cuda")
+    norm_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    for k in (1, 2, 3):
+        a.set_grad(k)
+        host_g.copy_(a.g)
+        a.plan.step(hp, k, grad_norm=norm_a if clip else None)
+        plan_b.step(hp, k, grad_norm=norm_b if clip else None)
+    torch.cuda.synchronize()
+    for x, y in zip((a.st.param, a.st.exp_avg, a.st.exp_avg_sq, a.st.aux),
+                    (b_state.param, b_state.exp_avg, b_state.exp_avg_sq, b_state.aux)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    if clip:
+        assert norm_a.item() == norm_b.item()
+    a.plan.close()
+    plan_b.close()
+
+
+def test_buffers_of_another_kind_are_refused_before_any_launch():
+    """Unpinned host memory on a device without pageable access, or any
+    pointer the device cannot dereference, is an error code, not a fault.
+    (On devices with pageable-memory access, unpinned host memory is valid.)"""
+    st = W.make_state(_small("acc", sizes=[64]), "cuda")
+    g = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    cpu_g = torch.zeros(64, dtype=torch.bfloat16)          # pageable host memory
+    entry = (st.param.data_ptr(), cpu_g.data_ptr(), st.exp_avg.data_ptr(),
+             st.exp_avg_sq.data_ptr(), st.aux.data_ptr(), 64)
+    pageable = getattr(torch.cuda.get_device_properties(0), "pageable_memory_access", None)
+    try:
+        plan = A.adamw_plan_create([entry], W.MODE_BF16_KAHAN)
+        A.adamw_plan_destroy(plan)
+        accepted = True
+    except A.AdamWError as e:
+        assert e.status == A.ADAMW_ERR_NOT_ACCESSIBLE
+        accepted = False
+    if pageable is not None:
+        assert accepted == bool(pageable)
+    del g
