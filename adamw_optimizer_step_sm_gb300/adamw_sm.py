@@ -90,11 +90,15 @@ def load() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_float)]
             L.adamw_copy_probe.argtypes = [vp, vp, i64, vp]
             L.adamw_grad_norm_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, vp, vp, vp]
+            L.adamw_step_table.argtypes = [vp, i32, i32, ctypes.POINTER(adamw_hparams_t), i64,
+                                           vp, vp, vp]
+            L.adamw_step_table_cache_clear.argtypes = []
             L.adamw_status_string.argtypes = [ctypes.c_int]
             L.adamw_status_string.restype = ctypes.c_char_p
             for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm",
                          "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
-                         "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc"):
+                         "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc",
+                         "adamw_step_table", "adamw_step_table_cache_clear"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -151,6 +155,19 @@ def adamw_grad_norm_noalloc(entries, d_grad_norm: int = 0, d_nonfinite: int = 0,
     arr, n = _table(entries)
     _check(load().adamw_grad_norm_noalloc(arr, n, d_grad_norm or None, d_nonfinite or None,
                                           stream or None), "adamw_grad_norm_noalloc")
+
+
+def adamw_step_table(d_table: int, n_tensors: int, mode: int, hp: adamw_hparams_t, step: int,
+                     d_grad_norm: int = 0, d_nonfinite: int = 0, stream: int = 0) -> None:
+    """One step over a tensor table held in device memory at address d_table
+    (n_tensors adamw_tensor_t entries); plans are cached by table contents."""
+    _check(load().adamw_step_table(d_table, n_tensors, mode, ctypes.byref(hp), step,
+                                   d_grad_norm or None, d_nonfinite or None, stream or None),
+           "adamw_step_table")
+
+
+def adamw_step_table_cache_clear() -> int:
+    return load().adamw_step_table_cache_clear()
 
 
 def adamw_plan_destroy(plan: int) -> None:

@@ -188,6 +188,23 @@ int adamw_plan_chunks(const adamw_tensor_t* host_table, int32_t n_tensors,
  * step_size, sbc2, omb1, omb2, lrwd.  Errors: INVALID_ARG. */
 int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step, float out5[5]);
 
+/* One step over a tensor table the caller already holds in DEVICE memory
+ * (d_table: n_tensors adamw_tensor_t entries, read during the call).  The
+ * table is copied to the host (the call waits for `stream` to reach that
+ * copy) and the plan built for it is kept in a cache of up to 8 plans keyed
+ * by the table's bytes, the mode and the current device, so passing the same
+ * table every step builds the plan (and allocates) once.  Other arguments and
+ * errors as adamw_plan_create and adamw_step (cached plans carry the norm
+ * workspace, so clipping is always available).  Thread-safe with respect to
+ * the cache; the buffers named by a cached table must outlive its use. */
+int adamw_step_table(const adamw_tensor_t* d_table, int32_t n_tensors, int32_t mode,
+                     const adamw_hparams_t* hp, int64_t step, double* d_grad_norm,
+                     int32_t* d_nonfinite, adamw_stream_t stream);
+
+/* Destroys every plan adamw_step_table cached (synchronising their devices)
+ * and returns how many there were. */
+int adamw_step_table_cache_clear(void);
+
 /* Measurement aid: copies `bytes` from src to dst (device pointers) with the
  * library's 16-byte-vector streaming copy kernel, asynchronously.  Used to
  * measure the HBM copy ceiling the update kernel is compared with.

@@ -82,12 +82,13 @@ def test_traffic_is_dropped_when_kernel_sources_change(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     os.makedirs(tmp_path / "profiles")
     os.makedirs(tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc")
-    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / "k.cu").write_text("a")
+    for f in bench.KERNEL_SOURCES:
+        (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / f).write_text("a")
     h = bench.kernel_source_hash()
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(
         {"x": {"kernel_source_hash": h, "dram_bytes_per_launch": 123}}))
     assert bench.recorded_traffic("x") == 123
-    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / "k.cu").write_text("b")
+    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / bench.KERNEL_SOURCES[0]).write_text("b")
     assert bench.recorded_traffic("x") is None
 
 

@@ -279,3 +279,35 @@ def test_buffers_of_another_kind_are_refused_before_any_launch():
     if pageable is not None:
         assert accepted == bool(pageable)
     del g
+
+
+def test_step_table_over_a_device_table_matches_a_plan():
+    """adamw_step_table takes the tensor table from device memory, caches one
+    plan for it, and updates exactly like an explicit plan."""
+    import ctypes
+    w = _small("table", mode=W.MODE_MIXED, max_grad_norm=0.5, steps=3)
+    a = H.GpuRun(w)
+    b = W.make_state(w, "cuda")
+    g = torch.zeros_like(a.g)
+    v = b.views
+    entries = [A.adamw_tensor_t(*(t.data_ptr() for t in ts), ts[0].numel())
+               for ts in zip(v(b.param), v(g), v(b.exp_avg), v(b.exp_avg_sq), v(b.aux))]
+    raw = bytes((A.adamw_tensor_t * len(entries))(*entries))
+    d_table = torch.frombuffer(bytearray(raw), dtype=torch.uint8).cuda()
+    hp, _ = H.hp_pair(w)
+    A.adamw_step_table_cache_clear()
+    norm_a = torch.zeros(1, dtype=torch.float64, device="cuda")
+    norm_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for k in (1, 2, 3):
+        a.set_grad(k)
+        g.copy_(a.g)
+        a.plan.step(hp, k, grad_norm=norm_a)
+        A.adamw_step_table(d_table.data_ptr(), len(entries), w.mode, hp, k, norm_b.data_ptr(), 0, stream)
+    torch.cuda.synchronize()
+    assert A.adamw_step_table_cache_clear() == 1
+    for x, y in zip((a.st.param, a.st.exp_avg, a.st.exp_avg_sq, a.st.aux),
+                    (b.param, b.exp_avg, b.exp_avg_sq, b.aux)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    assert norm_a.item() == norm_b.item()
+    a.plan.close()
