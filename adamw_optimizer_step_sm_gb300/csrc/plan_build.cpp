@@ -82,6 +82,17 @@ int validate_hparams(const adamw_hparams_t* hp, int64_t step) {
     return ADAMW_OK;
 }
 
+// beta^t by binary exponentiation (fp64 multiplications only, lowest bit of
+// t first), so the device-resident step path reproduces it exactly.
+double beta_power(double beta, int64_t t) {
+    double result = 1.0, square = beta;
+    for (; t > 0; t >>= 1) {
+        if (t & 1) result *= square;
+        square *= square;
+    }
+    return result;
+}
+
 // Bias corrections of Kingma & Ba and the decoupled decay factor of
 // Loshchilov & Hutter, in fp64 from the fp32 hyperparameters, each rounded
 // once to fp32.
@@ -89,8 +100,8 @@ int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out) {
     int rc = validate_hparams(hp, step);
     if (rc != ADAMW_OK) return rc;
     const double b1 = hp->beta1, b2 = hp->beta2;
-    const double bc1 = 1.0 - std::pow(b1, double(step));
-    const double bc2 = 1.0 - std::pow(b2, double(step));
+    const double bc1 = 1.0 - beta_power(b1, step);
+    const double bc2 = 1.0 - beta_power(b2, step);
     out->beta1 = hp->beta1;
     out->beta2 = hp->beta2;
     out->omb1 = float(1.0 - b1);

@@ -400,7 +400,25 @@ def pin_skip_on_nonfinite(o: O.Oracle):
         assert changed
 
 
+def pin_bias_correction_powers(o: O.Oracle):
+    """The per-step scalars against the closed forms with the library's fp64
+    pow: step_size = lr/(1-b1^t), sbc2 = sqrt(1-b2^t), 1-b1, 1-b2, lr*wd,
+    each rounded once to fp32.  Binary exponentiation is within a few fp64
+    ulps of pow, so the fp32 scalars agree to at most one fp32 ulp (and
+    exactly at t = 1, 2 where both are exact products)."""
+    for b1, b2 in ((0.9, 0.95), (0.9, 0.999), (0.5, 0.25), (0.0, 0.0), (0.99, 0.9999)):
+        hp = O.hparams(lr=2e-4, beta1=b1, beta2=b2, weight_decay=0.1)
+        fb1, fb2, lr, wd = f32(b1), f32(b2), f32(2e-4), f32(0.1)
+        for t in (1, 2, 3, 7, 10, 100, 1000, 12345, 10**6, 10**9):
+            got = o.step_scalars(hp, t).astype(np.float64)
+            want = np.array([lr / (1 - math.pow(fb1, t)), math.sqrt(1 - math.pow(fb2, t)),
+                             1 - fb1, 1 - fb2, lr * wd], dtype=np.float32).astype(np.float64)
+            tol = np.zeros(5) if t <= 2 else ulp_f32(want)
+            assert np.all(np.abs(got - want) <= tol), (b1, b2, t, got, want)
+
+
 ALL_PINS = [
+    pin_bias_correction_powers,
     pin_bf16_rne_vs_torch,
     pin_bf16_rne_definition,
     pin_first_step_mixed,

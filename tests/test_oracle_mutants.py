@@ -20,8 +20,12 @@ MUTANTS = [
     ("no_bias_correction1", "s.step_size = (float)((double)hp->lr / bc1);",
      "s.step_size = (float)((double)hp->lr); (void)bc1;"),
     ("no_bias_correction2", "s.sbc2 = (float)sqrt(bc2);", "s.sbc2 = 1.0f; (void)bc2;"),
-    ("bc2_uses_beta1", "double bc2 = 1.0 - pow(b2, (double)t);",
-     "double bc2 = 1.0 - pow(b1, (double)t);"),
+    ("bc2_uses_beta1", "double bc2 = 1.0 - power_by_squaring(b2, t);",
+     "double bc2 = 1.0 - power_by_squaring(b1, t);"),
+    ("power_off_by_one", "    double result = 1.0, square = b;\n",
+     "    double result = b, square = b;\n"),
+    ("power_skips_odd_bits", "        if (t & 1) result = result * square;\n",
+     "        if (t & 2) result = result * square;\n"),
     ("v_not_squared_mixed", "float v1 = (b2 * v[i]) + ((s.omb2 * gi) * gi);",
      "float v1 = (b2 * v[i]) + (s.omb2 * gi);"),
     ("v_not_squared_bf16", "float v1 = (b2 * v0) + ((s.omb2 * gi) * gi);",
