@@ -22,6 +22,8 @@ from . import build as _build
 MODE_BF16_KAHAN = 0
 MODE_MIXED_FP32_MASTER = 1
 PLAN_NORM = 1
+STEP_CLIP = 1
+STEP_NORM = 2
 
 ADAMW_OK = 0
 ADAMW_ERR_INVALID_ARG = -1
@@ -81,6 +83,7 @@ def load() -> ctypes.CDLL:
                                             ctypes.POINTER(vp)]
             L.adamw_step.argtypes = [vp, ctypes.POINTER(adamw_hparams_t), i64, vp, vp, vp]
             L.adamw_grad_norm.argtypes = [vp, vp, vp, vp]
+            L.adamw_step_device.argtypes = [vp, vp, vp, i32, vp, vp, vp]
             L.adamw_plan_destroy.argtypes = [vp]
             L.adamw_plan_get_info.argtypes = [vp, ctypes.POINTER(adamw_plan_info_t)]
             L.adamw_plan_chunks.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32, i32,
@@ -95,7 +98,7 @@ def load() -> ctypes.CDLL:
             L.adamw_step_table_cache_clear.argtypes = []
             L.adamw_status_string.argtypes = [ctypes.c_int]
             L.adamw_status_string.restype = ctypes.c_char_p
-            for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm",
+            for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm", "adamw_step_device",
                          "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
                          "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc",
                          "adamw_step_table", "adamw_step_table_cache_clear"):
@@ -136,6 +139,14 @@ def adamw_step(plan: int, hp: adamw_hparams_t, step: int, d_grad_norm: int = 0,
                d_nonfinite: int = 0, stream: int = 0) -> None:
     _check(load().adamw_step(plan, ctypes.byref(hp), step, d_grad_norm or None,
                              d_nonfinite or None, stream or None), "adamw_step")
+
+
+def adamw_step_device(plan: int, d_hp: int, d_step: int, flags: int = 0, d_grad_norm: int = 0,
+                      d_nonfinite: int = 0, stream: int = 0) -> None:
+    """A step whose hyperparameters (device adamw_hparams_t at d_hp) and
+    applied-step counter (device int64 at d_step) live on the device."""
+    _check(load().adamw_step_device(plan, d_hp, d_step, flags, d_grad_norm or None,
+                                    d_nonfinite or None, stream or None), "adamw_step_device")
 
 
 def adamw_grad_norm(plan: int, d_grad_norm: int = 0, d_nonfinite: int = 0,
@@ -256,6 +267,16 @@ class Plan:
                    nonfinite.data_ptr() if nonfinite is not None else 0,
                    st.cuda_stream)
 
+    def step_device(self, d_hp, d_step, flags: int = 0, grad_norm=None, nonfinite=None,
+                    stream=None) -> None:
+        """d_hp: CUDA uint8 tensor holding one adamw_hparams_t (see
+        ``device_hparams``); d_step: CUDA int64 tensor, the applied-step count."""
+        import torch
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        adamw_step_device(self.handle, d_hp.data_ptr(), d_step.data_ptr(), flags,
+                          grad_norm.data_ptr() if grad_norm is not None else 0,
+                          nonfinite.data_ptr() if nonfinite is not None else 0, st.cuda_stream)
+
     def grad_norm(self, grad_norm=None, nonfinite=None, stream=None) -> None:
         import torch
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -272,3 +293,10 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def device_hparams(hp: adamw_hparams_t, device="cuda"):
+    """An adamw_hparams_t as a CUDA uint8 tensor, for adamw_step_device."""
+    import torch
+    raw = bytes(hp)
+    return torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)

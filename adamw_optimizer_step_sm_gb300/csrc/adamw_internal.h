@@ -77,6 +77,17 @@ struct StepScalars {
     float max_grad_norm;
 };
 
+// What the device-resident step path (adamw_step_device) decides before the
+// update runs: the scalars of t = *d_step + 1, the clip coefficient, and
+// whether the step is skipped (1: non-finite gradient under clipping,
+// 2: invalid hyperparameters).
+struct StepRecord {
+    StepScalars s;
+    float coef;
+    int32_t skip;
+    int32_t pad_[2];
+};
+
 // ---- host planner (plan_build.cpp) ----
 
 int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode);

@@ -359,13 +359,20 @@ __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]), fetching the
 // next chunk's descriptor before working on the current one.
-template <int MODE, int K>
+// DEV: the scalars, clip coefficient and skip decision come from the
+// StepRecord the device-resident step path's prologue wrote.
+template <int MODE, int K, bool DEV>
 __global__ void ADAMW_UPDATE_BOUNDS
 adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
-                    const NormOut* __restrict__ norm, int32_t* __restrict__ report) {
+                    const NormOut* __restrict__ norm, int32_t* __restrict__ report,
+                    const StepRecord* __restrict__ rec) {
     float coef = 1.0f;
-    if (K == kClip) {
+    if (DEV) {
+        if (rec->skip) return;        // skipped step: no writes at all
+        s = rec->s;
+        coef = rec->coef;
+    } else if (K == kClip) {
         if (norm->nonfinite) return;  // skipped step: no writes at all
         coef = norm->coef;
     }
@@ -564,6 +571,92 @@ norm_finalize_kernel(const double* __restrict__ partial, const int32_t* __restri
     }
 }
 
+// ---- device-resident step path ----
+
+// beta^t by binary exponentiation, lowest bit of t first, one IEEE fp64
+// rounding per multiplication: the same operations as the host planner's.
+__device__ double beta_power_dev(double beta, int64_t t) {
+    double result = 1.0, square = beta;
+    for (; t > 0; t >>= 1) {
+        if (t & 1) result = __dmul_rn(result, square);
+        square = __dmul_rn(square, square);
+    }
+    return result;
+}
+
+__device__ bool hparams_valid_dev(const adamw_hparams_t& hp) {
+    const float f[6] = {hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm};
+    for (float x : f)
+        if (!isfinite(x)) return false;
+    return hp.lr >= 0.0f && hp.eps > 0.0f && hp.weight_decay >= 0.0f && hp.beta1 >= 0.0f &&
+           hp.beta1 < 1.0f && hp.beta2 >= 0.0f && hp.beta2 < 1.0f;
+}
+
+// The host planner's make_scalars, operation for operation.
+__device__ void make_scalars_dev(const adamw_hparams_t& hp, int64_t t, StepScalars* out) {
+    const double b1 = hp.beta1, b2 = hp.beta2;
+    const double bc1 = __dsub_rn(1.0, beta_power_dev(b1, t));
+    const double bc2 = __dsub_rn(1.0, beta_power_dev(b2, t));
+    out->beta1 = hp.beta1;
+    out->beta2 = hp.beta2;
+    out->omb1 = __double2float_rn(__dsub_rn(1.0, b1));
+    out->omb2 = __double2float_rn(__dsub_rn(1.0, b2));
+    out->step_size = __double2float_rn(__ddiv_rn(double(hp.lr), bc1));
+    out->sbc2 = __double2float_rn(__dsqrt_rn(bc2));
+    out->eps = hp.eps;
+    out->lrwd = __double2float_rn(__dmul_rn(double(hp.lr), double(hp.weight_decay)));
+    out->max_grad_norm = hp.max_grad_norm;
+}
+
+// One CTA, before the update: finalises the norm when n_partials > 0 (the
+// same fixed-order reduction as norm_finalize_kernel), reads the
+// hyperparameters and the applied-step counter from device memory, decides
+// whether the step is skipped, writes the StepRecord, advances the counter
+// for an applied step, and fills the caller's outputs (flag -1 for invalid
+// hyperparameters).
+__global__ void __launch_bounds__(kBlock)
+step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
+                     StepRecord* __restrict__ rec, const double* __restrict__ partial,
+                     const int32_t* __restrict__ flag, int32_t n_partials, int32_t clip,
+                     NormOut* __restrict__ nout, double* __restrict__ user_norm,
+                     int32_t* __restrict__ user_flag) {
+    double x = 0.0;
+    bool bad = false;
+    for (int32_t i = threadIdx.x; i < n_partials; i += kBlock) {
+        x += partial[i];
+        bad |= flag[i] != 0;
+    }
+    const double tot = block_sum(x);
+    const int any = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        const adamw_hparams_t hp = *d_hp;
+        const bool valid = hparams_valid_dev(hp);
+        const double norm = sqrt(tot);
+        float coef = 1.0f;
+        if (clip && valid && hp.max_grad_norm > 0.0f) {
+            double c = double(hp.max_grad_norm) / (norm + 1e-6);
+            if (c > 1.0) c = 1.0;
+            coef = float(c);
+        }
+        StepRecord r{};
+        r.skip = !valid ? 2 : (clip && any) ? 1 : 0;
+        r.coef = coef;
+        if (!r.skip) {
+            const int64_t t = *d_step + 1;
+            make_scalars_dev(hp, t, &r.s);
+            *d_step = t;
+        }
+        *rec = r;
+        if (n_partials > 0) {
+            nout->norm = norm;
+            nout->coef = coef;
+            nout->nonfinite = any;
+            if (user_norm) *user_norm = norm;
+        }
+        if (user_flag) *user_flag = !valid ? -1 : (n_partials > 0 ? any : 0);
+    }
+}
+
 // Plain 16-byte streaming copy (HBM ceiling probe).
 __global__ void __launch_bounds__(kBlock)
 copy_probe_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n) {
@@ -599,7 +692,7 @@ bool cuda_ok(cudaError_t e, const char* where) {
 }
 
 template <int MODE, int K>
-const void* update_fn() { return reinterpret_cast<const void*>(&adamw_update_kernel<MODE, K>); }
+const void* update_fn() { return reinterpret_cast<const void*>(&adamw_update_kernel<MODE, K, false>); }
 
 int device_info(int dev, DeviceInfo* out) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -669,30 +762,32 @@ struct adamw_plan {
     double* partial = nullptr;
     int32_t* flag = nullptr;
     NormOut* norm = nullptr;
+    StepRecord* rec = nullptr;     // device-resident step path
 };
 
 namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-template <int MODE, int K>
+template <int MODE, int K, bool DEV>
 cudaError_t launch_update(const adamw_plan* P, const StepScalars& s, int32_t* report,
                           cudaStream_t st) {
-    adamw_update_kernel<MODE, K><<<P->upd.grid, kBlock, 0, st>>>(P->upd.chunks, P->upd.cta_begin,
-                                                                 s, P->norm, report);
+    adamw_update_kernel<MODE, K, DEV><<<P->upd.grid, kBlock, 0, st>>>(
+        P->upd.chunks, P->upd.cta_begin, s, P->norm, report, P->rec);
     return cudaGetLastError();
 }
 
+template <bool DEV>
 cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& s,
                               int32_t* report, cudaStream_t st) {
     if (P->mode == ADAMW_MODE_BF16_KAHAN) {
-        if (kind == kPlain) return launch_update<0, kPlain>(P, s, report, st);
-        if (kind == kClip) return launch_update<0, kClip>(P, s, report, st);
-        return launch_update<0, kReport>(P, s, report, st);
+        if (kind == kPlain) return launch_update<0, kPlain, DEV>(P, s, report, st);
+        if (kind == kClip) return launch_update<0, kClip, DEV>(P, s, report, st);
+        return launch_update<0, kReport, DEV>(P, s, report, st);
     }
-    if (kind == kPlain) return launch_update<1, kPlain>(P, s, report, st);
-    if (kind == kClip) return launch_update<1, kClip>(P, s, report, st);
-    return launch_update<1, kReport>(P, s, report, st);
+    if (kind == kPlain) return launch_update<1, kPlain, DEV>(P, s, report, st);
+    if (kind == kClip) return launch_update<1, kClip, DEV>(P, s, report, st);
+    return launch_update<1, kReport, DEV>(P, s, report, st);
 }
 
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
@@ -770,6 +865,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_p = off; off = align_up(off + sizeof(double) * size_t(grid_norm), 256);
     const size_t o_f = off; off = align_up(off + sizeof(int32_t) * size_t(grid_norm), 256);
     const size_t o_n = off; off = align_up(off + sizeof(NormOut), 256);
+    const size_t o_r = off; off = align_up(off + sizeof(StepRecord), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;
@@ -784,6 +880,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->partial = reinterpret_cast<double*>(b + o_p);
     P->flag = reinterpret_cast<int32_t*>(b + o_f);
     P->norm = reinterpret_cast<NormOut*>(b + o_n);
+    P->rec = reinterpret_cast<StepRecord*>(b + o_r);
 
     auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
         return bytes == 0 || cuda_ok(cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice), what);
@@ -844,7 +941,7 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
         kind = kReport;
         report = d_nonfinite;
     }
-    if (!cuda_ok(launch_update_any(plan, kind, s, report, st), "update launch"))
+    if (!cuda_ok(launch_update_any<false>(plan, kind, s, report, st), "update launch"))
         return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }
@@ -867,6 +964,41 @@ extern "C" int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm, int32_t* 
         return ADAMW_OK;
     }
     if (!cuda_ok(launch_norm(plan, 0.0f, d_grad_norm, d_nonfinite, st), "norm launch"))
+        return ADAMW_ERR_CUDA;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
+                                 int64_t* d_step, int32_t flags, double* d_grad_norm,
+                                 int32_t* d_nonfinite, adamw_stream_t stream) {
+    if (!plan || !d_hp || !d_step || (flags & ~(ADAMW_STEP_CLIP | ADAMW_STEP_NORM)))
+        return ADAMW_ERR_INVALID_ARG;
+    const bool clip = (flags & ADAMW_STEP_CLIP) != 0;
+    const bool want_norm = clip || (flags & ADAMW_STEP_NORM) || d_grad_norm != nullptr;
+    if (want_norm && !(plan->flags & ADAMW_PLAN_NORM)) return ADAMW_ERR_NO_NORM;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) {
+        set_cuda_error("cudaSetDevice", cudaGetErrorString(cudaGetLastError()));
+        return ADAMW_ERR_CUDA;
+    }
+    const bool norm_pass = want_norm && plan->nrm.grid > 0;
+    if (norm_pass) {
+        norm_partial_kernel<<<plan->nrm.grid, kBlock, 0, st>>>(plan->nrm.chunks, plan->nrm.cta_begin,
+                                                               plan->partial, plan->flag);
+        if (!cuda_ok(cudaGetLastError(), "norm launch")) return ADAMW_ERR_CUDA;
+    }
+    step_prologue_kernel<<<1, kBlock, 0, st>>>(d_hp, d_step, plan->rec, plan->partial, plan->flag,
+                                               norm_pass ? plan->nrm.grid : 0, clip ? 1 : 0,
+                                               plan->norm, d_grad_norm, d_nonfinite);
+    if (!cuda_ok(cudaGetLastError(), "prologue launch")) return ADAMW_ERR_CUDA;
+    if (want_norm && !norm_pass && d_grad_norm &&
+        !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
+        return ADAMW_ERR_CUDA;
+    if (plan->upd.grid == 0) return ADAMW_OK;
+    const int kind = clip ? kClip : (!want_norm && d_nonfinite) ? kReport : kPlain;
+    int32_t* report = (kind == kReport) ? d_nonfinite : nullptr;
+    if (!cuda_ok(launch_update_any<true>(plan, kind, StepScalars{}, report, st), "update launch"))
         return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }

@@ -160,6 +160,30 @@ int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t step,
                double* d_grad_norm, int32_t* d_nonfinite,
                adamw_stream_t stream);
 
+/* adamw_step_device flags. */
+#define ADAMW_STEP_CLIP 1 /* clip by d_hp->max_grad_norm (needs ADAMW_PLAN_NORM) */
+#define ADAMW_STEP_NORM 2 /* compute the norm into d_grad_norm, no clipping      */
+
+/* adamw_step with every per-step input in device memory, so a sequence of
+ * calls can be captured in a CUDA graph and replayed:
+ * d_hp (device adamw_hparams_t) is read when the step runs (write a new lr
+ * there between replays for a schedule); d_step (device int64) holds the
+ * number of updates applied so far: the step uses t = *d_step + 1 and stores
+ * t back unless it is skipped.  The step is skipped (nothing written, counter
+ * unchanged) when ADAMW_STEP_CLIP is set and a gradient is non-finite, or when
+ * the hyperparameters in d_hp are out of range (then *d_nonfinite = -1).
+ * d_grad_norm, d_nonfinite: as in adamw_step.  The scalars are computed on
+ * the device with the same fp64 operations as the host path, so results are
+ * bit-identical to adamw_step with the same t.  Launches: a one-CTA prologue
+ * and the update, plus the norm pass when clipping or the norm is asked.
+ * No host synchronisation and no allocation; all pointers are device-
+ * accessible memory the caller owns (not checked here).
+ * Errors: INVALID_ARG (NULL plan, d_hp or d_step, unknown flag), NO_NORM,
+ * CUDA. */
+int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp, int64_t* d_step,
+                      int32_t flags, double* d_grad_norm, int32_t* d_nonfinite,
+                      adamw_stream_t stream);
+
 /* The global gradient L2 norm and non-finite flag of the plan's gradients,
  * without an update (the two-stage reduction the clipped step runs first).
  * d_grad_norm and d_nonfinite as in adamw_step (either may be NULL).

@@ -311,3 +311,100 @@ def test_step_table_over_a_device_table_matches_a_plan():
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
     assert norm_a.item() == norm_b.item()
     a.plan.close()
+
+
+# ----------------------------------------------- device-resident step path --
+
+def _twin(w):
+    """Two identical states of workload w: one stepped by the host path, one
+    by the device-resident path."""
+    a = H.GpuRun(w)
+    b_state = W.make_state(w, "cuda")
+    v = b_state.views
+    b_plan = A.Plan(v(b_state.param), v(a.g), v(b_state.exp_avg), v(b_state.exp_avg_sq),
+                    v(b_state.aux), w.mode, norm=True)
+    return a, b_state, b_plan
+
+
+def _same_state(x, y):
+    for p, q in zip((x.param, x.exp_avg, x.exp_avg_sq, x.aux), (y.param, y.exp_avg, y.exp_avg_sq, y.aux)):
+        assert torch.equal(p.view(torch.uint8), q.view(torch.uint8))
+
+
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_BF16_KAHAN, 0.5),
+                                       (W.MODE_MIXED, 0.0), (W.MODE_MIXED, 1.0)])
+def test_device_step_matches_host_step(mode, clip):
+    """Hyperparameters and the step counter in device memory give the same
+    bytes as the host path, including a skipped step (inf at step 3)."""
+    w = _small("dev", mode=mode, max_grad_norm=clip, steps=5,
+               inf_at=(3, 8, 777) if clip else None)
+    a, b_state, b_plan = _twin(w)
+    hp, _ = H.hp_pair(w)
+    d_hp = A.device_hparams(hp)
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    n_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    f_b = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = A.STEP_CLIP if clip else 0
+    for k in range(1, 6):
+        a.set_grad(k)                  # the twin plan reads the same buffer
+        skipped = a.step(hp)
+        b_plan.step_device(d_hp, d_step, flags, grad_norm=n_b if clip else None, nonfinite=f_b)
+        torch.cuda.synchronize()
+        assert int(f_b.item()) == int(a.flag.item())
+        assert int(d_step.item()) == a.t
+        if clip:
+            assert n_b.item() == a.norm.item()
+        assert skipped == (clip > 0 and k == 3)
+    _same_state(a.st, b_state)
+    a.plan.close()
+    b_plan.close()
+
+
+def test_device_step_refuses_invalid_hparams_on_device():
+    w = _small("devbad", sizes=[4096, 77], steps=1)
+    a, b_state, b_plan = _twin(w)
+    a.set_grad(1)
+    before = [t.clone() for t in (b_state.param, b_state.exp_avg, b_state.exp_avg_sq, b_state.aux)]
+    d_hp = A.device_hparams(A.hparams(beta1=1.5))
+    d_step = torch.full((1,), 7, dtype=torch.int64, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b_plan.step_device(d_hp, d_step, 0, nonfinite=flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == -1 and int(d_step.item()) == 7
+    for x, y in zip(before, (b_state.param, b_state.exp_avg, b_state.exp_avg_sq, b_state.aux)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    a.plan.close()
+    b_plan.close()
+
+
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_MIXED, 1.0)])
+def test_device_step_replayed_from_a_cuda_graph(mode, clip):
+    """One device-resident step captured in a CUDA graph and replayed with a
+    changing learning rate (written to the device hyperparameters between
+    replays) equals the host path with the same per-step lr."""
+    w = _small("graph", mode=mode, max_grad_norm=clip, steps=6)
+    a, b_state, b_plan = _twin(w)
+    flags = A.STEP_CLIP if clip else 0
+    hps = [A.hparams(**{**w.hparams(), "lr": 2e-4 * (k + 1) / 6}) for k in range(6)]
+    d_hp = A.device_hparams(hps[0])
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    norm = torch.zeros(1, dtype=torch.float64, device="cuda")
+    # load the kernels once outside the capture (a throwaway list)
+    warm = _small("warm", mode=mode, sizes=[64], steps=1)
+    wa, wb_state, wb_plan = _twin(warm)
+    wb_plan.step_device(A.device_hparams(hps[0]), torch.zeros(1, dtype=torch.int64, device="cuda"),
+                        flags, grad_norm=norm if clip else None)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        b_plan.step_device(d_hp, d_step, flags, grad_norm=norm if clip else None)
+    for k in range(6):
+        a.set_grad(k + 1)
+        a.step(hps[k], want_flag=False)
+        d_hp.copy_(A.device_hparams(hps[k]))
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(d_step.item()) == 6
+    _same_state(a.st, b_state)
+    for p in (a.plan, b_plan, wa.plan, wb_plan):
+        p.close()
