@@ -93,7 +93,7 @@ def compare(rep: Report, name: str, gpu: np.ndarray, ref: np.ndarray):
 
 # -------------------------------------------------------------- the GPU side --
 
-class GpuRun:
+class GpuSide:
     """A workload's state on the GPU plus a plan over its tensor list."""
 
     def __init__(self, w: W.Workload, device="cuda", state: W.State | None = None):
@@ -173,7 +173,7 @@ class OracleRun:
         return False, norm, bad
 
 
-def compare_state(gpu: GpuRun, ref: OracleRun, rep: Report | None = None) -> Report:
+def compare_state(gpu: GpuSide, ref: OracleRun, rep: Report | None = None) -> Report:
     rep = rep or Report()
     st = gpu.st
     wide = to_u16 if gpu.w.mode == W.MODE_BF16_KAHAN else to_f32
@@ -191,7 +191,7 @@ def run_parity(w: W.Workload, steps: int | None = None, device="cuda",
                align_elems: int = 8, skew: int = 0) -> tuple[Report, list]:
     """Full-list parity: every element of every tensor after every step."""
     steps = steps or w.steps
-    gpu = GpuRun(w, device, W.make_state(w, device, align_elems, skew))
+    gpu = GpuSide(w, device, W.make_state(w, device, align_elems, skew))
     ref = OracleRun.from_state(gpu.st)
     hp_g, hp_o = hp_pair(w)
     log = []
@@ -211,7 +211,7 @@ def run_parity(w: W.Workload, steps: int | None = None, device="cuda",
 
 # --------------------------------------------------- sampled (full size) --
 
-def sample_indices(gpu: GpuRun, per_tensor: int, seed: int = 0) -> np.ndarray:
+def sample_indices(gpu: GpuSide, per_tensor: int, seed: int = 0) -> np.ndarray:
     """Flat-buffer indices to check: per tensor its first and last 9
     elements, ``per_tensor`` random ones, and the elements around every chunk
     boundary of the plan (where CTAs hand over and vector bodies start)."""
@@ -243,7 +243,7 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
     own norm over the full gradient) and the GPU's values at those elements
     must match."""
     steps = steps or w.steps
-    gpu = GpuRun(w, device)
+    gpu = GpuSide(w, device)
     idx = sample_indices(gpu, per_tensor)
     it = torch.from_numpy(idx).to(device)
     wide = to_u16 if w.mode == W.MODE_BF16_KAHAN else to_f32

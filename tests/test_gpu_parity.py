@@ -19,7 +19,7 @@ def _assert(rep: H.Report, log=None):
 
 
 def _small(name, **kw):
-    """A small list with the shape mix of the paper workloads plus ragged
+    """A small list with the shape mix of the workloads on the pages plus ragged
     sizes that span several CTAs and leave tails."""
     sizes = kw.pop("sizes", [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257, 3 * 768, 50272])
     mode = kw.pop("mode", W.MODE_BF16_KAHAN)
@@ -29,7 +29,7 @@ def _small(name, **kw):
     return W.Workload(name, mode, tensors, **base)
 
 
-# ------------------------------------------------------------ paper configs --
+# ---------------------------------------------------- the pages' workloads --
 
 def test_flat1m_bf16_kahan_bit_exact():
     rep, log = H.run_parity(W.WORKLOADS["flat1m_bf16_kahan"])
@@ -90,7 +90,7 @@ def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     _assert(rep, log)
     assert [k for (k, s, *_r) in log if s] == [2]
     # the skipped step itself wrote nothing
-    gpu = H.GpuRun(w)
+    gpu = H.GpuSide(w)
     hp, _ = H.hp_pair(w)
     gpu.set_grad(1)
     gpu.step(hp)
@@ -108,7 +108,7 @@ def test_nonfinite_reported_without_clip(bad):
     """Without clipping the step runs and NaN/inf propagate exactly as in the
     oracle; the flag reports them."""
     w = _small("report", steps=2)
-    gpu = H.GpuRun(w)
+    gpu = H.GpuSide(w)
     ref = H.OracleRun.from_state(gpu.st)
     hp_g, hp_o = H.hp_pair(w)
     for k in (1, 2):
@@ -125,7 +125,7 @@ def test_nonfinite_reported_without_clip(bad):
 
 def test_grad_norm_deterministic_and_matches_oracle():
     w = W.WORKLOADS["opt125m_bf16_kahan"]
-    gpu = H.GpuRun(w)
+    gpu = H.GpuSide(w)
     gpu.set_grad(1)
     norms = []
     for _ in range(3):
@@ -145,7 +145,7 @@ def test_grad_norm_deterministic_and_matches_oracle():
 def test_grad_norm_with_huge_and_tiny_values():
     """Values whose squares leave fp32 range take the fp64 path."""
     w = _small("huge", sizes=[4096, 100])
-    gpu = H.GpuRun(w)
+    gpu = H.GpuSide(w)
     gpu.g.zero_()
     gpu.g[5] = 3.0e30
     gpu.g[6] = -2.0e19
@@ -212,7 +212,7 @@ def test_copy_probe_copies():
 def test_steps_on_a_side_stream_and_a_second_plan():
     """Two independent plans on two streams give the same bytes as one run."""
     w = _small("streams", sizes=[70000, 333])
-    a, b = H.GpuRun(w), H.GpuRun(w)
+    a, b = H.GpuSide(w), H.GpuSide(w)
     hp, _ = H.hp_pair(w)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     for k in (1, 2, 3):
@@ -235,7 +235,7 @@ def test_gradients_in_pinned_host_memory(mode, clip):
     """A plan whose gradients live in pinned host memory (read by the kernels
     over the CPU-GPU link) gives the same bytes as one with device gradients."""
     w = _small("hostgrad", mode=mode, max_grad_norm=clip, steps=3)
-    a = H.GpuRun(w)
+    a = H.GpuSide(w)
     b_state = W.make_state(w, "cuda")
     host_g = torch.zeros(a.g.numel(), dtype=torch.bfloat16, pin_memory=True)
     v = b_state.views
@@ -286,7 +286,7 @@ def test_step_table_over_a_device_table_matches_a_plan():
     plan for it, and updates exactly like an explicit plan."""
     import ctypes
     w = _small("table", mode=W.MODE_MIXED, max_grad_norm=0.5, steps=3)
-    a = H.GpuRun(w)
+    a = H.GpuSide(w)
     b = W.make_state(w, "cuda")
     g = torch.zeros_like(a.g)
     v = b.views
@@ -318,7 +318,7 @@ def test_step_table_over_a_device_table_matches_a_plan():
 def _twin(w):
     """Two identical states of workload w: one stepped by the host path, one
     by the device-resident path."""
-    a = H.GpuRun(w)
+    a = H.GpuSide(w)
     b_state = W.make_state(w, "cuda")
     v = b_state.views
     b_plan = A.Plan(v(b_state.param), v(a.g), v(b_state.exp_avg), v(b_state.exp_avg_sq),

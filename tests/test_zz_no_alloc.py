@@ -27,7 +27,7 @@ def _list(align_elems, skew):
     sizes = [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257, 3 * 768, 50272, 4_000_000]
     w = W.Workload("noalloc", W.MODE_BF16_KAHAN, tuple(W.TensorSpec(f"t{i}", n) for i, n in enumerate(sizes)),
                    2, lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, heavy_tail=True)
-    return H.GpuRun(w, "cuda", W.make_state(w, "cuda", align_elems, skew))
+    return H.GpuSide(w, "cuda", W.make_state(w, "cuda", align_elems, skew))
 
 
 def _norms(gpu):
