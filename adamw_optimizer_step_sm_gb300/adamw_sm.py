@@ -21,6 +21,7 @@ from . import build as _build
 
 MODE_BF16_KAHAN = 0
 MODE_MIXED_FP32_MASTER = 1
+MODE_MIXED_BF16_REMAINDER = 2
 PLAN_NORM = 1
 STEP_CLIP = 1
 STEP_NORM = 2
@@ -225,7 +226,8 @@ class Plan:
 
     bf16 Kahan mode: params, exp_avg, exp_avg_sq, aux (= compensation) bf16.
     Mixed mode: params (= fp32 master), exp_avg, exp_avg_sq fp32; aux = bf16
-    param out.  grads are bf16 in both.  The tensors must stay alive and in
+    param out.  Remainder mode: params bf16, exp_avg, exp_avg_sq fp32, aux =
+    int16 remainder of the fp32 master.  grads are bf16 in all modes.  The tensors must stay alive and in
     place for the plan's lifetime (the plan holds references to them).
     """
 
@@ -236,8 +238,11 @@ class Plan:
         n = len(lists[0])
         if any(len(x) != n for x in lists):
             raise ValueError("tensor lists differ in length")
-        wide = torch.bfloat16 if mode == MODE_BF16_KAHAN else torch.float32
-        want = (wide, torch.bfloat16, wide, wide, torch.bfloat16)
+        want = {MODE_BF16_KAHAN: (torch.bfloat16,) * 5,
+                MODE_MIXED_FP32_MASTER: (torch.float32, torch.bfloat16, torch.float32,
+                                         torch.float32, torch.bfloat16),
+                MODE_MIXED_BF16_REMAINDER: (torch.bfloat16, torch.bfloat16, torch.float32,
+                                            torch.float32, torch.int16)}[mode]
         entries = []
         for k in range(n):
             ts = [x[k] for x in lists]

@@ -90,6 +90,11 @@ struct StepRecord {
 
 // ---- host planner (plan_build.cpp) ----
 
+constexpr int kModes = 3;
+bool valid_mode(int32_t mode);
+// Bytes per element of param, grad, exp_avg, exp_avg_sq, aux in a mode.
+void element_sizes(int32_t mode, int64_t es[5]);
+
 int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode);
 int validate_hparams(const adamw_hparams_t* hp, int64_t step);
 int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out);

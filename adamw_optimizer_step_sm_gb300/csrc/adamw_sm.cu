@@ -1,8 +1,9 @@
 // adamw_sm.cu -- sm_103a kernels and the device half of the C ABI.
 //
 // The step is a streaming elementwise update: per element it reads p, g, m, v
-// and c (bf16 Kahan mode, 10 B) or master, m, v and g (mixed mode, 14 B) and
-// writes 8 B or 14 B back, with about twenty fp32 operations in between.
+// and c (bf16 Kahan mode, 10 B), master, m, v and g (mixed mode, 14 B) or p,
+// remainder, m, v and g (remainder mode, 14 B) and writes 8, 14 or 12 B back,
+// with about twenty fp32 operations in between.
 // That is far below the GPU's ridge point, so HBM bandwidth bounds it and the
 // kernels are built to keep DRAM streaming: a persistent grid (SMs x resident
 // CTAs) dealt 16K-element tiles of the flattened parameter space round-robin
@@ -334,6 +335,107 @@ __device__ __forceinline__ void mixed_elem_chunk(const ChunkPtr& t, int64_t len,
     }
 }
 
+// Remainder mode: the fp32 master is the bf16 parameter (high half) plus a
+// signed 16-bit remainder of the bit pattern.
+__device__ __forceinline__ float join_master(uint32_t hi_bits, uint32_t rem16) {
+    return __uint_as_float(hi_bits + uint32_t(int32_t(int16_t(uint16_t(rem16)))));
+}
+// Nearest bf16 high half (ties away from zero) and the remainder restoring it.
+__device__ __forceinline__ void split_master(float x, uint32_t& hi16, uint32_t& rem16) {
+    const uint32_t u = __float_as_uint(x);
+    hi16 = (u + 0x8000u) >> 16;
+    rem16 = (u - (hi16 << 16)) & 0xffffu;
+}
+
+template <int K>
+__device__ __forceinline__ void remainder_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                    const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* r = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], R[kUnroll];
+        F8 M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                R[u] = ld16(r + i * kVec);
+                M[u] = ld32(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                const uint32_t pw[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
+                const uint32_t rw[4] = {R[u].x, R[u].y, R[u].z, R[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t po[4], ro[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int a = 2 * j, b = 2 * j + 1;
+                    const float n0 = mixed_x1<K>(s, coef, bf16_lo(gw[j]),
+                                                 join_master(pw[j] << 16, rw[j]), M[u].x[a], V[u].x[a]);
+                    const float n1 = mixed_x1<K>(s, coef, bf16_hi(gw[j]),
+                                                 join_master(pw[j] & 0xffff0000u, rw[j] >> 16),
+                                                 M[u].x[b], V[u].x[b]);
+                    uint32_t h0, r0, h1, r1;
+                    split_master(n0, h0, r0);
+                    split_master(n1, h1, r1);
+                    po[j] = h0 | (h1 << 16);
+                    ro[j] = r0 | (r1 << 16);
+                }
+                st16(p + i * kVec, make_uint4(po[0], po[1], po[2], po[3]));
+                st16(r + i * kVec, make_uint4(ro[0], ro[1], ro[2], ro[3]));
+                st32(m + i * kVec, M[u]);
+                st32(v + i * kVec, V[u]);
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), join_master(uint32_t(p[i]) << 16, r[i]),
+                                    mi, vi);
+        uint32_t h, rr;
+        split_master(n, h, rr);
+        p[i] = uint16_t(h); r[i] = uint16_t(rr); m[i] = mi; v[i] = vi;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                     const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* r = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), join_master(uint32_t(p[i]) << 16, r[i]),
+                                    mi, vi);
+        uint32_t h, rr;
+        split_master(n, h, rr);
+        p[i] = uint16_t(h); r[i] = uint16_t(rr); m[i] = mi; v[i] = vi;
+    }
+}
+
 // --------------------------------------------------------------- kernels --
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
@@ -388,9 +490,12 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
         if (MODE == ADAMW_MODE_BF16_KAHAN) {
             if (vec) kahan_vec_chunk<K>(cur, len, s, coef, bad);
             else kahan_elem_chunk<K>(cur, len, s, coef, bad);
-        } else {
+        } else if (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
             if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
             else mixed_elem_chunk<K>(cur, len, s, coef, bad);
+        } else {
+            if (vec) remainder_vec_chunk<K>(cur, len, s, coef, bad);
+            else remainder_elem_chunk<K>(cur, len, s, coef, bad);
         }
         cur = nxt;
     }
@@ -677,7 +782,7 @@ copy_probe_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_
 
 struct DeviceInfo {
     int sms = 0;
-    int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};
+    int occ[kModes][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
     int occ_norm = 0;
     int occ_copy = 0;
 };
@@ -703,10 +808,11 @@ int device_info(int dev, DeviceInfo* out) {
         if (!cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
                      "cudaDeviceGetAttribute"))
             return ADAMW_ERR_CUDA;
-        const void* fns[2][3] = {
+        const void* fns[kModes][3] = {
             {update_fn<0, kPlain>(), update_fn<0, kClip>(), update_fn<0, kReport>()},
-            {update_fn<1, kPlain>(), update_fn<1, kClip>(), update_fn<1, kReport>()}};
-        for (int m = 0; m < 2; ++m)
+            {update_fn<1, kPlain>(), update_fn<1, kClip>(), update_fn<1, kReport>()},
+            {update_fn<2, kPlain>(), update_fn<2, kClip>(), update_fn<2, kReport>()}};
+        for (int m = 0; m < kModes; ++m)
             for (int k = 0; k < 3; ++k)
                 if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[m][k], fns[m][k],
                                                                            kBlock, 0),
@@ -785,9 +891,14 @@ cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& 
         if (kind == kClip) return launch_update<0, kClip, DEV>(P, s, report, st);
         return launch_update<0, kReport, DEV>(P, s, report, st);
     }
-    if (kind == kPlain) return launch_update<1, kPlain, DEV>(P, s, report, st);
-    if (kind == kClip) return launch_update<1, kClip, DEV>(P, s, report, st);
-    return launch_update<1, kReport, DEV>(P, s, report, st);
+    if (P->mode == ADAMW_MODE_MIXED_FP32_MASTER) {
+        if (kind == kPlain) return launch_update<1, kPlain, DEV>(P, s, report, st);
+        if (kind == kClip) return launch_update<1, kClip, DEV>(P, s, report, st);
+        return launch_update<1, kReport, DEV>(P, s, report, st);
+    }
+    if (kind == kPlain) return launch_update<2, kPlain, DEV>(P, s, report, st);
+    if (kind == kClip) return launch_update<2, kClip, DEV>(P, s, report, st);
+    return launch_update<2, kReport, DEV>(P, s, report, st);
 }
 
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,

@@ -29,19 +29,34 @@ bool aligned(const void* p, uintptr_t a) {
 // Elements [0, head) take the element path so that every base is 16-byte
 // aligned at `head`; -1 when no head < kVec does that.
 int vector_head(const adamw_tensor_t& t, int32_t mode) {
-    const uintptr_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    int64_t es[5];
+    element_sizes(mode, es);
     const void* ptrs[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
-    const uintptr_t es[5] = {wide, 2, wide, wide, 2};
     for (int h = 0; h < kVec; ++h) {
         bool ok = true;
         for (int s = 0; s < 5 && ok; ++s)
-            ok = ((reinterpret_cast<uintptr_t>(ptrs[s]) + h * es[s]) % 16) == 0;
+            ok = ((reinterpret_cast<uintptr_t>(ptrs[s]) + uintptr_t(h * es[s])) % 16) == 0;
         if (ok) return h;
     }
     return -1;
 }
 
 }  // namespace
+
+void element_sizes(int32_t mode, int64_t es[5]) {
+    const int64_t param = (mode == ADAMW_MODE_MIXED_FP32_MASTER) ? 4 : 2;
+    const int64_t moments = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    es[0] = param;
+    es[1] = 2;
+    es[2] = moments;
+    es[3] = moments;
+    es[4] = 2;
+}
+
+bool valid_mode(int32_t mode) {
+    return mode == ADAMW_MODE_BF16_KAHAN || mode == ADAMW_MODE_MIXED_FP32_MASTER ||
+           mode == ADAMW_MODE_MIXED_BF16_REMAINDER;
+}
 
 void set_cuda_error(const char* where, const char* what) {
     g_cuda_error = std::string(where) + ": " + what;
@@ -52,19 +67,18 @@ const char* last_cuda_error() { return g_cuda_error.c_str(); }
 int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode) {
     if (n < 0) return ADAMW_ERR_INVALID_ARG;
     if (n > 0 && !table) return ADAMW_ERR_INVALID_ARG;
-    if (mode != ADAMW_MODE_BF16_KAHAN && mode != ADAMW_MODE_MIXED_FP32_MASTER)
-        return ADAMW_ERR_INVALID_ARG;
-    const uintptr_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    if (!valid_mode(mode)) return ADAMW_ERR_INVALID_ARG;
+    int64_t es[5];
+    element_sizes(mode, es);
     for (int32_t k = 0; k < n; ++k) {
         const adamw_tensor_t& t = table[k];
         if (t.numel < 0) return ADAMW_ERR_INVALID_ARG;
         if (t.numel == 0) continue;
-        if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq || !t.aux)
-            return ADAMW_ERR_INVALID_ARG;
-        if (!aligned(t.param, wide) || !aligned(t.exp_avg, wide) ||
-            !aligned(t.exp_avg_sq, wide) || !aligned(t.grad, 2) ||
-            !aligned(t.aux, 2))
-            return ADAMW_ERR_MISALIGNED;
+        const void* ptrs[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
+        for (int s = 0; s < 5; ++s) {
+            if (!ptrs[s]) return ADAMW_ERR_INVALID_ARG;
+            if (!aligned(ptrs[s], uintptr_t(es[s]))) return ADAMW_ERR_MISALIGNED;
+        }
     }
     return ADAMW_OK;
 }
@@ -221,7 +235,8 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
 
 void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& P,
                     std::vector<ChunkPtr>* out) {
-    const int64_t wide = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
+    int64_t es[5];
+    element_sizes(mode, es);
     out->resize(P.chunks.size());
     for (size_t i = 0; i < P.chunks.size(); ++i) {
         const ChunkDev& c = P.chunks[i];
@@ -230,11 +245,11 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
             return static_cast<void*>(static_cast<char*>(const_cast<void*>(base)) + c.off * es);
         };
         ChunkPtr& d = (*out)[i];
-        d.p = at(t.param, wide);
-        d.g = at(t.grad, 2);
-        d.m = at(t.exp_avg, wide);
-        d.v = at(t.exp_avg_sq, wide);
-        d.a = at(t.aux, 2);
+        d.p = at(t.param, es[0]);
+        d.g = at(t.grad, es[1]);
+        d.m = at(t.exp_avg, es[2]);
+        d.v = at(t.exp_avg_sq, es[3]);
+        d.a = at(t.aux, es[4]);
         d.len2 = 2 * c.len + c.vec;
     }
 }

@@ -33,6 +33,14 @@ SEED = 42   # the run recipes on the pages pass --seed 42
 
 MODE_BF16_KAHAN = 0
 MODE_MIXED = 1
+MODE_REMAINDER = 2
+
+# torch dtypes of (param, exp_avg/exp_avg_sq, aux) per mode
+MODE_DTYPES = {
+    MODE_BF16_KAHAN: (torch.bfloat16, torch.bfloat16, torch.bfloat16),
+    MODE_MIXED: (torch.float32, torch.float32, torch.bfloat16),
+    MODE_REMAINDER: (torch.bfloat16, torch.float32, torch.int16),
+}
 
 
 @dataclass(frozen=True)
@@ -131,6 +139,17 @@ WORKLOADS: dict[str, Workload] = {
         max_grad_norm=1.0, g_std=1e-2, inf_at=(3, 200, 12345),
         description="OPT-1.3b tensor list, fp32 master + global-norm clip 1.0, "
                     "+inf injected at step 3"),
+    "bert55m_shard_remainder": Workload(
+        "bert55m_shard_remainder", MODE_REMAINDER, (TensorSpec("shard", 13_850_000),), 20,
+        lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, g_std=1e-3,
+        description="one 13,850,000-element shard, fp32 master held as bf16 param + "
+                    "16-bit remainder"),
+    "opt1.3b_remainder_clip": Workload(
+        "opt1.3b_remainder_clip", MODE_REMAINDER, OPT_1_3B, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+        max_grad_norm=1.0, g_std=1e-2, inf_at=(3, 200, 12345),
+        description="OPT-1.3b tensor list, bf16 param + 16-bit remainder master, "
+                    "global-norm clip 1.0, +inf injected at step 3"),
     # profiling-size case of the clipped mixed step (2 GB of state, > L2)
     "opt125m_mixed_clip": Workload(
         "opt125m_mixed_clip", MODE_MIXED, OPT_125M, 5,
@@ -179,7 +198,7 @@ class State:
     param: torch.Tensor        # bf16 (mode 0) or fp32 master (mode 1)
     exp_avg: torch.Tensor
     exp_avg_sq: torch.Tensor
-    aux: torch.Tensor          # bf16 compensation (mode 0) / bf16 param out (mode 1)
+    aux: torch.Tensor          # bf16 compensation / bf16 param out / int16 remainder
     offsets: list[int] = field(default_factory=list)
 
     def views(self, flat: torch.Tensor) -> list[torch.Tensor]:
@@ -203,11 +222,12 @@ def make_state(w: Workload, device="cpu", align_elems: int = 8, skew: int = 0) -
             dst.zero_()
         else:
             dst.copy_(_draw_normal(spec.numel, w.p_std, gen, device))
-    wide = torch.bfloat16 if w.mode == MODE_BF16_KAHAN else torch.float32
-    param = p32.to(wide) if wide != torch.float32 else p32
+    pdt, mdt, adt = MODE_DTYPES[w.mode]
+    # remainder mode starts from bf16-exact masters: the remainder is zero
+    param = p32.to(pdt) if pdt != torch.float32 else p32
     del p32
     z = lambda dt: torch.zeros(length, dtype=dt, device=device)
-    return State(w, param, z(wide), z(wide), z(torch.bfloat16), offs)
+    return State(w, param, z(mdt), z(mdt), z(adt), offs)
 
 
 def make_grad(w: Workload, step: int, device="cpu", offsets: list[int] | None = None,

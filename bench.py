@@ -44,10 +44,10 @@ def bytes_per_param(w: W.Workload) -> int:
     """Algorithmic HBM bytes per parameter per step.
     bf16 Kahan: read p, g, m, v, c (10) + write p, m, v, c (8) = 18.
     mixed: read master, m, v (12) + g (2), write master, m, v (12) + p_out (2)
-    = 28; with clipping the norm pass reads g once more: 30."""
-    if w.mode == W.MODE_BF16_KAHAN:
-        return 18 + (2 if w.max_grad_norm > 0 else 0)
-    return 28 + (2 if w.max_grad_norm > 0 else 0)
+    = 28.  remainder: read p, r (4) + m, v (8) + g (2), write p, r, m, v (12)
+    = 26.  With clipping the norm pass reads g once more: +2."""
+    base = {W.MODE_BF16_KAHAN: 18, W.MODE_MIXED: 28, W.MODE_REMAINDER: 26}[w.mode]
+    return base + (2 if w.max_grad_norm > 0 else 0)
 
 
 def load_peaks() -> dict:
@@ -160,8 +160,7 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arr
     if arrays is None:
         ws = W.truncated(w, n_elems)
         st = W.make_state(ws, "cpu")
-        wide = to16 if ws.mode == W.MODE_BF16_KAHAN else (lambda t: t.numpy())
-        p, m, v, a = wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux)
+        p, m, v, a = (host_array(x) for x in (st.param, st.exp_avg, st.exp_avg_sq, st.aux))
         grads = [to16(W.make_grad(ws, k + 1, "cpu")) for k in range(min(steps, 2))]
         offsets, numels = st.offsets, ws.numels
     else:
@@ -189,13 +188,24 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arr
             sl = slice(s, s + n)
             if ws.mode == W.MODE_BF16_KAHAN:
                 o.bf16_kahan(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
-            else:
+            elif ws.mode == W.MODE_MIXED:
                 o.mixed(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
+            else:
+                o.remainder(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
 
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, pieces))
     dt = time.perf_counter() - t0
     return sum(numels) * steps / dt, dt, threads
+
+
+def host_array(t: torch.Tensor):
+    """Host numpy copy with the oracle's dtype (bf16 as uint16 bits)."""
+    import numpy as np
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
 
 
 def host_threads() -> int:
@@ -381,11 +391,8 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # host copy of the freshly drawn inputs (before any step runs), for
         # the CPU oracle baseline
-        import numpy as np
-        to16 = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
-        wide = to16 if w.mode == W.MODE_BF16_KAHAN else (lambda t: t.cpu().numpy())
-        cpu_arrays = (wide(st.param), wide(st.exp_avg), wide(st.exp_avg_sq), to16(st.aux),
-                      to16(grads[0]), list(st.offsets))
+        cpu_arrays = (host_array(st.param), host_array(st.exp_avg), host_array(st.exp_avg_sq),
+                      host_array(st.aux), host_array(grads[0]), list(st.offsets))
     v = st.views
     plans = [A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode,
                     norm=clip) for g in grads]
@@ -484,8 +491,10 @@ def run_gpu(args):
         "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": w.name, "description": w.description, "n_params": N,
-            "n_tensors": w.n_tensors, "mode": "bf16_kahan" if w.mode == 0 else "mixed_fp32_master",
-            "storage": "bf16" if w.mode == 0 else "fp32 master/m/v, bf16 g and param out",
+            "n_tensors": w.n_tensors,
+            "mode": {0: "bf16_kahan", 1: "mixed_fp32_master", 2: "mixed_bf16_remainder"}[w.mode],
+            "storage": {0: "bf16 p/g/m/v/c", 1: "fp32 master/m/v, bf16 g and param out",
+                        2: "bf16 p + int16 remainder, fp32 m/v, bf16 g"}[w.mode],
             "clip": clip, "bytes_per_param": bpp, "hparams": w.hparams(),
             "l2": (f"256 MiB written before every timed step (L2 flushed; {bpp * N / 1e6:.1f} MB "
                    "moved per step)") if flush else

@@ -17,6 +17,15 @@
  *       #5305, "Usage": distributed_fused_adam; memory breakdown "bf16 mixed"
  *       of the transformers PR = 16 B/param.)
  *
+ *   ADAMW_MODE_MIXED_BF16_REMAINDER  the same update with the fp32 master
+ *       stored as the model's bf16 parameter plus a 16-bit remainder, so the
+ *       sharded optimizer state is fp32 m, fp32 v and the remainder: 10 B/param
+ *       ("2 FP32 optim state + 1 16-bit master param", memory estimate under
+ *       the 4xA40 table of the NeMo PR).  bits(master) = (bits(p16) << 16) +
+ *       r16 (r16 signed, integer addition): exact, so the trajectory equals
+ *       ADAMW_MODE_MIXED_FP32_MASTER's; p16 is the master rounded to nearest,
+ *       ties away from zero.
+ *
  * Arithmetic (identical in both modes up to storage; fp32, one IEEE
  * round-to-nearest per operation, no fused multiply-add):
  *   host, fp64 rounded once to fp32:  step_size = lr / (1 - beta1^t),
@@ -28,6 +37,8 @@
  *       den = sqrt(v')/sbc2 + eps ;  upd = step_size*(m'/den) + lrwd*p
  *   bf16 mode:  y = c - upd ; p' = bf16(p + y) ; c' = bf16(y - (p' - p))
  *   mixed mode: master' = master - upd ; p_out = bf16(master')
+ *   remainder mode: master = join(p16, r16) ; master' = master - upd ;
+ *       (p16', r16') = split(master')
  *   clipping:   norm = sqrt(sum g^2) over every tensor of the plan;
  *       coef = min(1, max_grad_norm / (norm + 1e-6)); a non-finite gradient
  *       anywhere sets the non-finite flag and the step writes no state.
@@ -52,6 +63,7 @@ typedef struct CUstream_st* adamw_stream_t;
 /* Storage modes. */
 #define ADAMW_MODE_BF16_KAHAN 0
 #define ADAMW_MODE_MIXED_FP32_MASTER 1
+#define ADAMW_MODE_MIXED_BF16_REMAINDER 2
 
 /* adamw_plan_create flags. */
 #define ADAMW_PLAN_NORM 1 /* allocate the global-norm workspace (clipping) */
@@ -74,12 +86,13 @@ typedef struct CUstream_st* adamw_stream_t;
  * pinned host memory needs no separate host-to-device copy.  The five buffers
  * of one tensor hold `numel` elements each and must not overlap one another
  * (different tensors may not overlap either).
- *   param       bf16 p (read/write)        | fp32 master (read/write)
- *   grad        bf16 g (read only)         | bf16 g (read only)
- *   exp_avg     bf16 m (read/write)        | fp32 m (read/write)
- *   exp_avg_sq  bf16 v (read/write)        | fp32 v (read/write)
- *   aux         bf16 Kahan c (read/write)  | bf16 param out (write only)
- * Element alignment is required (2 B for bf16, 4 B for fp32).  Tensors whose
+ *              bf16 Kahan            | mixed fp32 master   | mixed remainder
+ *   param      bf16 p (read/write)   | fp32 master (r/w)   | bf16 p (r/w)
+ *   grad       bf16 g (read)         | bf16 g (read)       | bf16 g (read)
+ *   exp_avg    bf16 m (r/w)          | fp32 m (r/w)        | fp32 m (r/w)
+ *   exp_avg_sq bf16 v (r/w)          | fp32 v (r/w)        | fp32 v (r/w)
+ *   aux        bf16 Kahan c (r/w)    | bf16 p out (write)  | int16 r (r/w)
+ * Element alignment is required (2 B for 16-bit, 4 B for fp32 buffers).  Tensors whose
  * five bases are all 16-byte aligned take the vectorised path; others are
  * still updated correctly, more slowly.  numel may be 0. */
 typedef struct {

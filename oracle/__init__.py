@@ -88,6 +88,9 @@ class Oracle:
         L.oracle_adamw_bf16_kahan.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_bf16_plain.argtypes = [vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_mixed.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_adamw_remainder.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_split_master.argtypes = [vp, vp, vp, i64]
+        L.oracle_join_master.argtypes = [vp, vp, vp, i64]
         L.oracle_grad_sumsq.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int32)]  # acc[2]
         L.oracle_clip_coef.argtypes = [ctypes.c_double, f32,
@@ -139,6 +142,28 @@ class Oracle:
         self.lib.oracle_adamw_mixed(_ptr(master), _ptr(g), _ptr(m), _ptr(v),
                                     _ptr(p_out), n, ctypes.byref(hp), t, coef)
 
+    def remainder(self, p16, g, m, v, r16, hp: Hparams, t: int, coef: float = 1.0):
+        n = p16.size
+        for a, dt in ((p16, np.uint16), (g, np.uint16), (m, np.float32), (v, np.float32),
+                      (r16, np.int16)):
+            _check(a, dt, n)
+        self.lib.oracle_adamw_remainder(_ptr(p16), _ptr(g), _ptr(m), _ptr(v), _ptr(r16), n,
+                                        ctypes.byref(hp), t, coef)
+
+    def split_master(self, x: np.ndarray):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        p16 = np.empty(x.shape, np.uint16)
+        r16 = np.empty(x.shape, np.int16)
+        self.lib.oracle_split_master(_ptr(x), _ptr(p16), _ptr(r16), x.size)
+        return p16, r16
+
+    def join_master(self, p16: np.ndarray, r16: np.ndarray) -> np.ndarray:
+        p16 = np.ascontiguousarray(p16, dtype=np.uint16)
+        r16 = np.ascontiguousarray(r16, dtype=np.int16)
+        out = np.empty(p16.shape, np.float32)
+        self.lib.oracle_join_master(_ptr(p16), _ptr(r16), _ptr(out), p16.size)
+        return out
+
     # -- norm ------------------------------------------------------------------
     def grad_sumsq(self, grads) -> tuple[float, bool]:
         """Sum of squares over the tensors in order (compensated fp64) and
@@ -160,11 +185,13 @@ class Oracle:
         """``tensors``: list of (param, grad, exp_avg, exp_avg_sq, aux) numpy
         arrays.  Returns (skipped: bool, norm: float)."""
         arr = (TensorEntry * max(1, len(tensors)))()
-        wide = np.uint16 if mode == 0 else np.float32
+        pt = np.float32 if mode == 1 else np.uint16
+        mv = np.uint16 if mode == 0 else np.float32
+        at = np.int16 if mode == 2 else np.uint16
         for k, (p, g, m, v, a) in enumerate(tensors):
             n = g.size
-            _check(p, wide, n); _check(g, np.uint16, n); _check(m, wide, n)
-            _check(v, wide, n); _check(a, np.uint16, n)
+            _check(p, pt, n); _check(g, np.uint16, n); _check(m, mv, n)
+            _check(v, mv, n); _check(a, at, n)
             arr[k] = TensorEntry(p.ctypes.data, g.ctypes.data, m.ctypes.data,
                                  v.ctypes.data, a.ctypes.data, n)
         norm = ctypes.c_double(0.0)

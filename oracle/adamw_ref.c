@@ -48,6 +48,14 @@
  *   mixed mode (fp32 master/m/v, bf16 grad in, bf16 param out):
  *     master' = master - upd ;  p_out = bf16(master')
  *
+ *   remainder mode (the same update; the fp32 master is stored as the bf16
+ *   parameter plus a 16-bit remainder, 10 B/param of optimizer state: "2 FP32
+ *   optim state + 1 16-bit master param" in the memory estimate of
+ *   "Distributed optimizer support for BERT", NeMo PR #5305):
+ *     bits(master) = (bits(p16) << 16) + r16     (r16 signed, integer add)
+ *     p16 = high half of master rounded to nearest, ties away from zero
+ *     (ties cannot round down: the remainder would be +32768)
+ *
  *   global-norm clipping (optional): norm = sqrt(sum of g^2) over all
  *   tensors in list order, the sum in compensated fp64; any non-finite g
  *   sets the flag and the step writes nothing; otherwise
@@ -250,6 +258,65 @@ void oracle_adamw_mixed(float* master, const uint16_t* g, float* m, float* v,
     }
 }
 
+/* ------------------------------------------------------ remainder mode -- */
+
+/* The fp32 master held as a bf16 high half and a signed 16-bit remainder of
+ * the bit pattern: bits(master) = (bits(p16) << 16) + r16. */
+static float master_from_halves(uint16_t p16, int16_t r16)
+{
+    uint32_t u = ((uint32_t)p16 << 16) + (uint32_t)(int32_t)r16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Splits an fp32 value into its nearest bf16 (ties away from zero in
+ * magnitude) and the remainder that restores it exactly. */
+static void halves_from_master(float f, uint16_t* p16, int16_t* r16)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t hi = (uint16_t)((u + 0x8000u) >> 16);
+    *p16 = hi;
+    *r16 = (int16_t)(int32_t)(u - ((uint32_t)hi << 16));
+}
+
+void oracle_split_master(const float* in, uint16_t* p16, int16_t* r16, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) halves_from_master(in[i], &p16[i], &r16[i]);
+}
+
+void oracle_join_master(const uint16_t* p16, const int16_t* r16, float* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = master_from_halves(p16[i], r16[i]);
+}
+
+/* One step over one shard in remainder mode: p16 (the model's bf16
+ * parameter) and r16 in place, fp32 m, v in place, bf16 grad read.  The
+ * update is the mixed mode's, on the master the two halves hold. */
+void oracle_adamw_remainder(uint16_t* p16, const uint16_t* g, float* m, float* v,
+                            int16_t* r16, int64_t n,
+                            const oracle_hparams_t* hp, int64_t t, float coef)
+{
+    step_scalars_t s = make_scalars(hp, t);
+    const float b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps;
+    const int clip = hp->max_grad_norm > 0.0f;
+
+    for (int64_t i = 0; i < n; ++i) {
+        float gi = bf16_bits_to_f32(g[i]);
+        if (clip) gi = gi * coef;
+        float p0 = master_from_halves(p16[i], r16[i]);
+        float m1 = (b1 * m[i]) + (s.omb1 * gi);
+        float v1 = (b2 * v[i]) + ((s.omb2 * gi) * gi);
+        float den = (sqrtf(v1) / s.sbc2) + eps;
+        float upd = (s.step_size * (m1 / den)) + (s.lrwd * p0);
+        float pn = p0 - upd;
+        m[i] = m1;
+        v[i] = v1;
+        halves_from_master(pn, &p16[i], &r16[i]);
+    }
+}
+
 /* ------------------------------------------------- global norm and clip -- */
 
 /* Adds sum of g^2 of one bf16 tensor, in element order, to the running sum
@@ -298,16 +365,16 @@ float oracle_clip_coef(double sumsq, float max_norm, double* norm_out)
 /* ------------------------------------------------ one step over a list -- */
 
 typedef struct {
-    void* param;      /* bf16 mode: bf16 p      mixed mode: fp32 master */
+    void* param;      /* bf16: bf16 p    mixed: fp32 master  remainder: bf16 p */
     const void* grad; /* bf16 */
-    void* exp_avg;    /* bf16 mode: bf16        mixed mode: fp32 */
-    void* exp_avg_sq; /* bf16 mode: bf16        mixed mode: fp32 */
-    void* aux;        /* bf16 mode: bf16 c      mixed mode: bf16 param out */
+    void* exp_avg;    /* bf16: bf16      mixed, remainder: fp32 */
+    void* exp_avg_sq; /* bf16: bf16      mixed, remainder: fp32 */
+    void* aux;        /* bf16: bf16 c    mixed: bf16 p out   remainder: int16 r */
     int64_t numel;
 } oracle_tensor_t;
 
 /* The whole optimizer step over a tensor list (host buffers), mode 0 = bf16
- * Kahan, mode 1 = mixed.  With clipping, the norm is taken first over every
+ * Kahan, mode 1 = mixed, mode 2 = remainder.  With clipping, the norm is taken first over every
  * tensor; a non-finite gradient anywhere makes the call write nothing and
  * return 1 (the caller must not advance t).  Returns 0 after an applied step.
  * norm_out (nullable) receives the fp64 norm when clipping. */
@@ -333,6 +400,10 @@ int32_t oracle_adamw_list_step(const oracle_tensor_t* list, int32_t n_tensors,
                                     (uint16_t*)e->exp_avg,
                                     (uint16_t*)e->exp_avg_sq,
                                     (uint16_t*)e->aux, e->numel, hp, t, coef);
+        else if (mode == 2)
+            oracle_adamw_remainder((uint16_t*)e->param, (const uint16_t*)e->grad,
+                                   (float*)e->exp_avg, (float*)e->exp_avg_sq,
+                                   (int16_t*)e->aux, e->numel, hp, t, coef);
         else
             oracle_adamw_mixed((float*)e->param, (const uint16_t*)e->grad,
                                (float*)e->exp_avg, (float*)e->exp_avg_sq,

@@ -417,7 +417,58 @@ def pin_bias_correction_powers(o: O.Oracle):
             assert np.all(np.abs(got - want) <= tol), (b1, b2, t, got, want)
 
 
+# ------------------------------------------------------- remainder mode --
+
+def pin_remainder_split_roundtrip(o: O.Oracle, n_random: int = 1 << 22):
+    """bf16 high half + int16 remainder hold an fp32 value exactly, and the
+    high half is the nearest bf16 (torch's RNE) except at exact ties, which
+    go away from zero."""
+    pats = np.concatenate([_special_patterns(),
+                           _rng(12).integers(0, 1 << 32, n_random, dtype=np.uint64).astype(np.uint32)])
+    x = pats.view(F32)
+    p16, r16 = o.split_master(x)
+    back = o.join_master(p16, r16)
+    assert np.array_equal(back.view(np.uint32), pats), "split/join is not exact"
+    nan = np.isnan(x)
+    tie = (pats & 0xFFFF) == 0x8000
+    ref = torch_bf16_bits(x)
+    ok = ~nan & ~tie
+    assert np.array_equal(p16[ok], ref[ok]), "high half is not the nearest bf16"
+    assert np.array_equal(p16[tie & ~nan], ((pats[tie & ~nan] >> 16) + 1).astype(np.uint16))
+    assert np.all(np.abs(r16.astype(np.int32)) <= 0x8000)
+
+
+def pin_remainder_equals_mixed_master(o: O.Oracle, steps: int = 12):
+    """Remainder mode stores the same fp32 master as the mixed mode, so its
+    trajectory is the mixed mode's bit for bit (itself pinned to
+    torch.optim.AdamW), and the bf16 parameter is that master's high half."""
+    r = _rng(13)
+    n = 5000
+    p0 = torch_bf16_bits((r.standard_normal(n) * 0.02).astype(F32))   # bf16-exact start
+    hp = O.hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_grad_norm=0.5)
+    master = bf16_to_f64(p0).astype(F32)
+    m, v, pout = np.zeros(n, F32), np.zeros(n, F32), np.zeros(n, np.uint16)
+    p16, r16 = p0.copy(), np.zeros(n, np.int16)
+    m2, v2 = np.zeros(n, F32), np.zeros(n, F32)
+    for t in range(1, steps + 1):
+        gh = torch_bf16_bits((r.standard_normal(n) * 1e-2).astype(F32))
+        coef, _ = o.clip_coef(o.grad_sumsq([gh])[0], 0.5)
+        o.mixed(master, gh, m, v, pout, hp, t, coef)
+        o.remainder(p16, gh, m2, v2, r16, hp, t, coef)
+    joined = o.join_master(p16, r16)
+    assert np.array_equal(joined.view(np.uint32), master.view(np.uint32)), "master differs"
+    assert np.array_equal(m2.view(np.uint32), m.view(np.uint32))
+    assert np.array_equal(v2.view(np.uint32), v.view(np.uint32))
+    hi, _ = o.split_master(master)
+    assert np.array_equal(hi, p16)
+    assert np.any(r16 != 0), "updates must leave a remainder"
+    # the bf16 parameter is within half a bf16 ulp of the master
+    assert np.all(np.abs(bf16_to_f64(p16) - joined) <= 0.5 * ulp_bf16(joined))
+
+
 ALL_PINS = [
+    pin_remainder_split_roundtrip,
+    pin_remainder_equals_mixed_master,
     pin_bias_correction_powers,
     pin_bf16_rne_vs_torch,
     pin_bf16_rne_definition,

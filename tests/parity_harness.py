@@ -34,6 +34,15 @@ def to_f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().numpy().astype(np.float32, copy=False)
 
 
+def to_np(t: torch.Tensor) -> np.ndarray:
+    """Host copy with the oracle's dtype: bf16 -> uint16 bits, int16, fp32."""
+    if t.dtype == torch.bfloat16:
+        return to_u16(t)
+    if t.dtype == torch.int16:
+        return t.detach().contiguous().cpu().numpy()
+    return to_f32(t)
+
+
 def hp_pair(w: W.Workload):
     h = w.hparams()
     return A.hparams(**h), O.hparams(**h)
@@ -69,6 +78,12 @@ class Report:
 
 
 def compare(rep: Report, name: str, gpu: np.ndarray, ref: np.ndarray):
+    if gpu.dtype == np.int16:   # remainder of the master: must be exact
+        rep.n += gpu.size
+        rep.exact += int(np.sum(gpu == ref))
+        if not np.array_equal(gpu, ref):
+            rep.failures.append(f"{name}: {int(np.sum(gpu != ref))} remainders differ")
+        return
     if gpu.dtype == np.uint16:
         mu, nan_ok, ex = bf16_ulp_diff(gpu, ref)
         rep.max_ulp = max(rep.max_ulp, mu)
@@ -99,7 +114,7 @@ class GpuSide:
     def __init__(self, w: W.Workload, device="cuda", state: W.State | None = None):
         self.w = w
         self.st = state or W.make_state(w, device)
-        self.g = torch.zeros_like(self.st.aux)
+        self.g = torch.zeros(self.st.aux.numel(), dtype=torch.bfloat16, device=self.st.aux.device)
         v = self.st.views
         self.plan = A.Plan(v(self.st.param), v(self.g), v(self.st.exp_avg), v(self.st.exp_avg_sq),
                            v(self.st.aux), w.mode, norm=True)
@@ -135,10 +150,17 @@ class OracleRun:
     @classmethod
     def from_state(cls, st: W.State):
         w = st.workload
-        wide = to_u16 if w.mode == W.MODE_BF16_KAHAN else to_f32
-        arrays = dict(param=wide(st.param), exp_avg=wide(st.exp_avg),
-                      exp_avg_sq=wide(st.exp_avg_sq), aux=to_u16(st.aux))
+        arrays = dict(param=to_np(st.param), exp_avg=to_np(st.exp_avg),
+                      exp_avg_sq=to_np(st.exp_avg_sq), aux=to_np(st.aux))
         return cls(w, arrays, w.numels, st.offsets)
+
+    def step_arrays(self, p, g, m, v, a, t, coef, hp):
+        if self.w.mode == W.MODE_BF16_KAHAN:
+            self.o.bf16_kahan(p, g, m, v, a, hp, t, coef)
+        elif self.w.mode == W.MODE_MIXED:
+            self.o.mixed(p, g, m, v, a, hp, t, coef)
+        else:
+            self.o.remainder(p, g, m, v, a, hp, t, coef)
 
     def views(self, name, k):
         o, n = self.offsets[k], self.numels[k]
@@ -161,10 +183,7 @@ class OracleRun:
             if self.numels[k] == 0:
                 return
             p, m, v, a = (self.views(x, k) for x in ("param", "exp_avg", "exp_avg_sq", "aux"))
-            if self.w.mode == W.MODE_BF16_KAHAN:
-                o.bf16_kahan(p, gs[k], m, v, a, hp, t, coef)
-            else:
-                o.mixed(p, gs[k], m, v, a, hp, t, coef)
+            self.step_arrays(p, gs[k], m, v, a, t, coef, hp)
 
         order = sorted(range(len(self.numels)), key=lambda k: -self.numels[k])
         with ThreadPoolExecutor(THREADS) as ex:
@@ -176,9 +195,8 @@ class OracleRun:
 def compare_state(gpu: GpuSide, ref: OracleRun, rep: Report | None = None) -> Report:
     rep = rep or Report()
     st = gpu.st
-    wide = to_u16 if gpu.w.mode == W.MODE_BF16_KAHAN else to_f32
-    got = dict(param=wide(st.param), exp_avg=wide(st.exp_avg), exp_avg_sq=wide(st.exp_avg_sq),
-               aux=to_u16(st.aux))
+    got = dict(param=to_np(st.param), exp_avg=to_np(st.exp_avg), exp_avg_sq=to_np(st.exp_avg_sq),
+               aux=to_np(st.aux))
     for k, (o, n) in enumerate(zip(ref.offsets, ref.numels)):
         if n == 0:
             continue
@@ -246,10 +264,9 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
     gpu = GpuSide(w, device)
     idx = sample_indices(gpu, per_tensor)
     it = torch.from_numpy(idx).to(device)
-    wide = to_u16 if w.mode == W.MODE_BF16_KAHAN else to_f32
     st = gpu.st
-    arrays = dict(param=wide(st.param[it]), exp_avg=wide(st.exp_avg[it]),
-                  exp_avg_sq=wide(st.exp_avg_sq[it]), aux=to_u16(st.aux[it]))
+    arrays = dict(param=to_np(st.param[it]), exp_avg=to_np(st.exp_avg[it]),
+                  exp_avg_sq=to_np(st.exp_avg_sq[it]), aux=to_np(st.aux[it]))
     ref = OracleRun(w, arrays, [idx.size], [0])
     o = ref.o
     hp_g, hp_o = hp_pair(w)
@@ -269,18 +286,15 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
         if not oskipped:
             ref.t += 1
             p, m, v, a = (ref.a[x] for x in ("param", "exp_avg", "exp_avg_sq", "aux"))
-            if w.mode == W.MODE_BF16_KAHAN:
-                o.bf16_kahan(p, g_s, m, v, a, hp_o, ref.t, coef if clip else 1.0)
-            else:
-                o.mixed(p, g_s, m, v, a, hp_o, ref.t, coef if clip else 1.0)
+            ref.step_arrays(p, g_s, m, v, a, ref.t, coef if clip else 1.0, hp_o)
         gnorm = float(gpu.norm.item()) if clip else float("nan")
         log.append((k, skipped, oskipped, flag, bad, gnorm, norm))
         if skipped != oskipped or flag != bad:
             rep.failures.append(f"step {k}: skip/flag gpu=({skipped},{flag}) oracle=({oskipped},{bad})")
         if clip and abs(gnorm - norm) > 1e-12 * norm:
             rep.failures.append(f"step {k}: norm gpu {gnorm!r} oracle {norm!r}")
-    got = dict(param=wide(st.param[it]), exp_avg=wide(st.exp_avg[it]),
-               exp_avg_sq=wide(st.exp_avg_sq[it]), aux=to_u16(st.aux[it]))
+    got = dict(param=to_np(st.param[it]), exp_avg=to_np(st.exp_avg[it]),
+               exp_avg_sq=to_np(st.exp_avg_sq[it]), aux=to_np(st.aux[it]))
     for name in ("param", "exp_avg", "exp_avg_sq", "aux"):
         compare(rep, f"sampled {name}", got[name], ref.a[name])
     gpu.plan.close()

@@ -33,16 +33,17 @@ def test_library_exports_every_declared_symbol():
     assert not missing, f"declared but not exported: {missing}"
 
 
+ELEM_SIZES = {0: (2, 2, 2, 2, 2), 1: (4, 2, 4, 4, 2), 2: (2, 2, 4, 4, 2)}
+
+
 def _fake(base, n, mode=0, skew=(0, 0, 0, 0, 0)):
-    wide = 2 if mode == 0 else 4
-    es = (wide, 2, wide, wide, 2)
+    es = ELEM_SIZES[mode]
     return tuple(base + (k + 1) * (1 << 36) + s * e for k, (s, e) in enumerate(zip(skew, es))) + (n,)
 
 
 def _check_partition(entries, mode, grid):
     chunks = A.adamw_plan_chunks(entries, mode, grid)
-    wide = 2 if mode == 0 else 4
-    es = (wide, 2, wide, wide, 2)
+    es = ELEM_SIZES[mode]
     covered = {k: np.zeros(e[5], np.int32) for k, e in enumerate(entries)}
     per_cta = np.zeros(grid, np.int64)
     last_cta = 0
@@ -68,7 +69,7 @@ def _check_partition(entries, mode, grid):
 
 def test_partition_covers_each_element_once_and_balances():
     sizes = [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257]
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         entries = [_fake(i << 30, n, mode) for i, n in enumerate(sizes)]
         for grid in (1, 2, 5, 152, 608, 5000):
             _check_partition(entries, mode, grid)
@@ -88,6 +89,15 @@ def test_partition_misaligned_bases_take_head_or_element_path():
     e_mix = [_fake(0, 999, 1, skew=(1, 5, 1, 1, 5))]
     ch = _check_partition(e_mix, 1, 3)
     assert ch[0].vec == 0 and ch[0].len == 3 and all(c.vec for c in ch[1:])
+    # remainder mode: bf16 param/remainder 5 elements and fp32 moments 1
+    # element past a boundary: the same 3-element head aligns all five
+    e_rem = [_fake(0, 999, 2, skew=(5, 5, 1, 1, 5))]
+    ch = _check_partition(e_rem, 2, 3)
+    assert ch[0].vec == 0 and ch[0].len == 3 and all(c.vec for c in ch[1:])
+    # fp32 moments must be 4-byte aligned in remainder mode
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_plan_chunks([(16, 16, 34, 48, 64, 10)], 2, 2)
+    assert e.value.status == A.ADAMW_ERR_MISALIGNED
 
 
 def test_opt_1_3b_partition():

@@ -49,6 +49,44 @@ def test_opt125m_bf16_kahan_full_list():
     assert rep.exact == rep.n
 
 
+def test_bert_shard_remainder():
+    rep, log = H.run_parity(W.WORKLOADS["bert55m_shard_remainder"])
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
+def test_opt1_3b_remainder_clip_inf_skip_sampled_full_size():
+    w = W.WORKLOADS["opt1.3b_remainder_clip"]
+    rep, log = H.run_sampled(w, per_tensor=512)
+    _assert(rep, log)
+    assert [k for (k, s, *_r) in log if s] == [w.inf_at[0]], log
+    assert rep.exact == rep.n
+
+
+def test_remainder_mode_holds_the_mixed_mode_master():
+    """On the GPU too, the remainder mode's (bf16 param, remainder) pair is
+    the mixed mode's fp32 master bit for bit, step after step."""
+    import oracle as O
+    o = O.load()
+    sizes = [70001, 4099, 1 << 20]
+    wr = _small("rem", mode=W.MODE_REMAINDER, sizes=sizes, max_grad_norm=0.5, steps=5)
+    wm = _small("mix", mode=W.MODE_MIXED, sizes=sizes, max_grad_norm=0.5, steps=5)
+    r = H.GpuSide(wr)
+    m = H.GpuSide(wm)
+    m.st.param.copy_(r.st.param.float())           # same bf16-exact start
+    hp, _ = H.hp_pair(wr)
+    for k in range(1, 6):
+        r.set_grad(k)
+        m.g.copy_(r.g)
+        r.step(hp)
+        m.step(hp)
+    joined = o.join_master(H.to_u16(r.st.param), H.to_np(r.st.aux))
+    assert np.array_equal(joined.view(np.uint32), H.to_f32(m.st.param).view(np.uint32))
+    assert torch.equal(r.st.exp_avg, m.st.exp_avg) and torch.equal(r.st.exp_avg_sq, m.st.exp_avg_sq)
+    r.plan.close()
+    m.plan.close()
+
+
 def test_opt1_3b_bf16_kahan_sampled_full_size():
     rep, log = H.run_sampled(W.WORKLOADS["opt1.3b_bf16_kahan"], per_tensor=1024)
     _assert(rep, log)
@@ -71,7 +109,7 @@ def test_opt1_3b_mixed_clip_inf_skip_sampled_full_size():
 
 # ------------------------------------------------------------- edge cases --
 
-@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED])
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
 @pytest.mark.parametrize("clip", [0.0, 0.5])
 @pytest.mark.parametrize("layout", [(8, 0), (1, 3), (1, 1)])
 def test_ragged_lists(mode, clip, layout):
@@ -83,7 +121,7 @@ def test_ragged_lists(mode, clip, layout):
     assert rep.exact == rep.n
 
 
-@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED])
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
 def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     w = _small("skip", mode=mode, max_grad_norm=1.0, inf_at=(2, 8, 777), steps=4)
     rep, log = H.run_parity(w)
@@ -179,7 +217,7 @@ def test_empty_plan_and_zero_length_tensors():
 def test_api_errors_on_gpu():
     w = _small("err", sizes=[1000])
     st = W.make_state(w, "cuda")
-    g = torch.zeros_like(st.aux)
+    g = torch.zeros(st.aux.numel(), dtype=torch.bfloat16, device="cuda")
     v = st.views
     plan = A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode, norm=False)
     with pytest.raises(A.AdamWError) as e:
@@ -332,7 +370,8 @@ def _same_state(x, y):
 
 
 @pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_BF16_KAHAN, 0.5),
-                                       (W.MODE_MIXED, 0.0), (W.MODE_MIXED, 1.0)])
+                                       (W.MODE_MIXED, 0.0), (W.MODE_MIXED, 1.0),
+                                       (W.MODE_REMAINDER, 1.0)])
 def test_device_step_matches_host_step(mode, clip):
     """Hyperparameters and the step counter in device memory give the same
     bytes as the host path, including a skipped step (inf at step 3)."""

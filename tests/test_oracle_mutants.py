@@ -55,6 +55,14 @@ MUTANTS = [
     ("norm_uncompensated", "    acc[1] = comp;\n", "    acc[1] = 0.0 * comp;\n"),
     ("nonfinite_missed", "if (!isfinite(x)) bad = 1;", "(void)0;"),
     ("skip_still_writes", "        if (bad) return 1;\n", "        (void)bad;\n"),
+    ("split_truncates", "    uint16_t hi = (uint16_t)((u + 0x8000u) >> 16);\n",
+     "    uint16_t hi = (uint16_t)(u >> 16);\n"),
+    ("join_ignores_remainder", "    uint32_t u = ((uint32_t)p16 << 16) + (uint32_t)(int32_t)r16;\n",
+     "    uint32_t u = ((uint32_t)p16 << 16); (void)r16;\n"),
+    ("remainder_sign", "    *r16 = (int16_t)(int32_t)(u - ((uint32_t)hi << 16));\n",
+     "    *r16 = (int16_t)(int32_t)(((uint32_t)hi << 16) - u);\n"),
+    ("remainder_mode_no_decay", "        float upd = (s.step_size * (m1 / den)) + (s.lrwd * p0);\n        float pn = p0 - upd;\n        m[i] = m1;",
+     "        float upd = (s.step_size * (m1 / den));\n        float pn = p0 - upd;\n        m[i] = m1;"),
     ("clip_scale_ignored_mixed", "float p0 = master[i];\n",
      "float p0 = master[i]; gi = bf16_bits_to_f32(g[i]);\n"),
 ]
