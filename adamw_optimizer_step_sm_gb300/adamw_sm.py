@@ -22,6 +22,8 @@ from . import build as _build
 MODE_BF16_KAHAN = 0
 MODE_MIXED_FP32_MASTER = 1
 MODE_MIXED_BF16_REMAINDER = 2
+MODE_BF16_PLAIN = 3
+MODE_BF16_KAHAN_FP32_VAR = 4
 PLAN_NORM = 1
 STEP_CLIP = 1
 STEP_NORM = 2
@@ -86,6 +88,10 @@ def load() -> ctypes.CDLL:
             L.adamw_grad_norm.argtypes = [vp, vp, vp, vp]
             L.adamw_step_device.argtypes = [vp, vp, vp, i32, vp, vp, vp]
             L.adamw_plan_destroy.argtypes = [vp]
+            L.adamw_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+            L.adamw_lr_linear_warmup.argtypes = [ctypes.c_float, i64, i64, i64]
+            L.adamw_lr_linear_warmup.restype = ctypes.c_float
+            L.adamw_lr_linear_warmup_device.argtypes = [vp, vp, ctypes.c_float, i64, i64, vp]
             L.adamw_plan_get_info.argtypes = [vp, ctypes.POINTER(adamw_plan_info_t)]
             L.adamw_plan_chunks.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32, i32,
                                             ctypes.POINTER(adamw_chunk_t), i64,
@@ -102,7 +108,8 @@ def load() -> ctypes.CDLL:
             for name in ("adamw_plan_create", "adamw_step", "adamw_grad_norm", "adamw_step_device",
                          "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
                          "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc",
-                         "adamw_step_table", "adamw_step_table_cache_clear"):
+                         "adamw_step_table", "adamw_step_table_cache_clear",
+                         "adamw_plan_device_status", "adamw_lr_linear_warmup_device"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -186,6 +193,24 @@ def adamw_plan_destroy(plan: int) -> None:
     _check(load().adamw_plan_destroy(plan), "adamw_plan_destroy")
 
 
+def adamw_lr_linear_warmup(base_lr: float, step: int, warmup: int, total: int) -> float:
+    return float(load().adamw_lr_linear_warmup(base_lr, step, warmup, total))
+
+
+def adamw_lr_linear_warmup_device(d_hp: int, d_step: int, base_lr: float, warmup: int,
+                                  total: int, stream: int = 0) -> None:
+    _check(load().adamw_lr_linear_warmup_device(d_hp, d_step, base_lr, warmup, total,
+                                                stream or None), "adamw_lr_linear_warmup_device")
+
+
+def adamw_plan_device_status(plan: int) -> int:
+    """Reads and clears the plan's device status word (1: a bounded wait in
+    one of its kernels ran out)."""
+    out = ctypes.c_int32(0)
+    _check(load().adamw_plan_device_status(plan, ctypes.byref(out)), "adamw_plan_device_status")
+    return out.value
+
+
 def adamw_plan_get_info(plan: int) -> adamw_plan_info_t:
     info = adamw_plan_info_t()
     _check(load().adamw_plan_get_info(plan, ctypes.byref(info)), "adamw_plan_get_info")
@@ -234,6 +259,8 @@ class Plan:
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, auxs, mode: int,
                  norm: bool = False):
         import torch
+        if auxs is None:
+            auxs = [None] * len(list(params))
         lists = [list(x) for x in (params, grads, exp_avgs, exp_avg_sqs, auxs)]
         n = len(lists[0])
         if any(len(x) != n for x in lists):
@@ -242,19 +269,25 @@ class Plan:
                 MODE_MIXED_FP32_MASTER: (torch.float32, torch.bfloat16, torch.float32,
                                          torch.float32, torch.bfloat16),
                 MODE_MIXED_BF16_REMAINDER: (torch.bfloat16, torch.bfloat16, torch.float32,
-                                            torch.float32, torch.int16)}[mode]
+                                            torch.float32, torch.int16),
+                MODE_BF16_PLAIN: (torch.bfloat16,) * 4 + (None,),
+                MODE_BF16_KAHAN_FP32_VAR: (torch.bfloat16, torch.bfloat16, torch.bfloat16,
+                                           torch.float32, torch.bfloat16)}[mode]
         entries = []
         for k in range(n):
             ts = [x[k] for x in lists]
             numel = ts[0].numel()
             for j, (t, dt) in enumerate(zip(ts, want)):
+                if dt is None:       # a buffer the mode does not use
+                    continue
                 # gradients may live in pinned host memory (read over the
                 # CPU-GPU link); everything else on the device
                 where_ok = t.is_cuda or (j == 1 and t.is_pinned())
                 if not where_ok or t.dtype != dt or not t.is_contiguous() or t.numel() != numel:
                     raise TypeError(f"tensor {k}: want contiguous CUDA {dt} of {numel} elements"
                                     + (" (or pinned host memory)" if j == 1 else ""))
-            entries.append(adamw_tensor_t(*(t.data_ptr() for t in ts), numel))
+            entries.append(adamw_tensor_t(*(t.data_ptr() if t is not None else None for t in ts),
+                                          numel))
         self._keep = lists
         self.mode = mode
         dev = lists[0][0].device if n else torch.device("cuda", torch.cuda.current_device())

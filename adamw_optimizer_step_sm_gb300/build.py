@@ -60,36 +60,49 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
-    """Compile the library when a source is newer than it; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, defines=(), out_dir: str | None = None) -> str:
+    """Compile the library when a source is newer than it; returns its path.
+
+    ``defines`` (NAME=VALUE strings) set the kernels' build-time tuning
+    constants; such builds go to ``out_dir`` (load one with the environment
+    variable ADAMW_SM_LIBRARY)."""
+    build_dir = out_dir or BUILD_DIR
+    lib_path = os.path.join(build_dir, LIB_NAME)
+    if not force and not defines and out_dir is None and up_to_date():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     cu, cpp = _sources()
+    dflags = [f"-D{d}" for d in defines]
     jobs = []
     objs = []
     for src in cu:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        jobs.append([nvcc, *NVCC_FLAGS, *extra_nvcc, "-Xptxas", "-v", "-c", src, "-o", obj])
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+        jobs.append([nvcc, *NVCC_FLAGS, *dflags, "-Xptxas", "-v", "-c", src, "-o", obj])
         objs.append(obj)
     for src in cpp:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        jobs.append(["g++", *CXX_FLAGS, "-c", src, "-o", obj])
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+        jobs.append(["g++", *CXX_FLAGS, *dflags, "-c", src, "-o", obj])
         objs.append(obj)
     with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         logs = list(ex.map(_run, jobs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if verbose:
         for log in logs:
             sys.stdout.write(log)
-    with open(os.path.join(BUILD_DIR, "ptxas.log"), "w") as f:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         f.write("\n".join(logs))
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB_PATH)
+    import argparse
+    ap = argparse.ArgumentParser(description="build libadamw_sm.so for sm_103a")
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--define", action="append", default=[], metavar="NAME=VALUE",
+                    help="a build-time tuning constant, e.g. ADAMW_BULK=1")
+    ap.add_argument("--out", default=None, help="output directory for a tuning build")
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=True, defines=a.define, out_dir=a.out))

@@ -90,7 +90,7 @@ struct StepRecord {
 
 // ---- host planner (plan_build.cpp) ----
 
-constexpr int kModes = 3;
+constexpr int kModes = 5;
 bool valid_mode(int32_t mode);
 // Bytes per element of param, grad, exp_avg, exp_avg_sq, aux in a mode.
 void element_sizes(int32_t mode, int64_t es[5]);
@@ -122,8 +122,8 @@ int32_t choose_grid(int64_t total, int32_t max_grid);
 // on `grid` CTAs (0: contiguous ranges).
 int64_t update_tile_elems(int64_t total, int32_t grid);
 
-// Every buffer of the list can be dereferenced by `device` (device_access.cpp).
-int check_device_access(const adamw_tensor_t* table, int32_t n, int device);
+// Every buffer the mode uses can be dereferenced by `device` (device_access.cpp).
+int check_device_access(const adamw_tensor_t* table, int32_t n, int32_t mode, int device);
 
 // Remembers a CUDA error text for adamw_status_string (per host thread).
 void set_cuda_error(const char* where, const char* what);

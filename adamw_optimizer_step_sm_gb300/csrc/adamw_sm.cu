@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -335,6 +336,200 @@ __device__ __forceinline__ void mixed_elem_chunk(const ChunkPtr& t, int64_t len,
     }
 }
 
+// bf16 without compensation, two elements per 32-bit word: p' = bf16(p - upd).
+template <int K>
+__device__ __forceinline__ void plain_x2(const StepScalars& s, float coef, uint32_t gw,
+                                         uint32_t& pw, uint32_t& mw, uint32_t& vw) {
+    float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+    if (K == kClip) {
+        g0 = __fmul_rn(g0, coef);
+        g1 = __fmul_rn(g1, coef);
+    }
+    const float p0 = bf16_lo(pw), p1 = bf16_hi(pw);
+    float ma, mb, va, vb;
+    moments(s, g0, bf16_lo(mw), bf16_lo(vw), ma, va);
+    moments(s, g1, bf16_hi(mw), bf16_hi(vw), mb, vb);
+    mw = pack_bf16x2(ma, mb);
+    vw = pack_bf16x2(va, vb);
+    pw = pack_bf16x2(__fsub_rn(p0, update_of(s, bf16_lo(mw), bf16_lo(vw), p0)),
+                     __fsub_rn(p1, update_of(s, bf16_hi(mw), bf16_hi(vw), p1)));
+}
+
+template <int K>
+__device__ __forceinline__ void plain_x1(const StepScalars& s, float coef, uint16_t gh,
+                                         uint16_t& ph, uint16_t& mh, uint16_t& vh) {
+    float g = from_bf16(gh);
+    if (K == kClip) g = __fmul_rn(g, coef);
+    const float p0 = from_bf16(ph);
+    float m1, v1;
+    moments(s, g, from_bf16(mh), from_bf16(vh), m1, v1);
+    mh = to_bf16(m1);
+    vh = to_bf16(v1);
+    ph = to_bf16(__fsub_rn(p0, update_of(s, from_bf16(mh), from_bf16(vh), p0)));
+}
+
+// bf16 Kahan with fp32 variance, one element: v stays fp32.
+template <int K>
+__device__ __forceinline__ void kahan_v32_x1(const StepScalars& s, float coef, float g,
+                                             float p0, float m0, float& v, float c0,
+                                             uint16_t& ph, uint16_t& mh, uint16_t& ch) {
+    if (K == kClip) g = __fmul_rn(g, coef);
+    float m1, v1;
+    moments(s, g, m0, v, m1, v1);
+    mh = to_bf16(m1);
+    v = v1;
+    const float y = __fsub_rn(c0, update_of(s, from_bf16(mh), v1, p0));
+    ph = to_bf16(__fadd_rn(p0, y));
+    ch = to_bf16(__fsub_rn(y, __fsub_rn(from_bf16(ph), p0)));
+}
+
+template <int K>
+__device__ __forceinline__ void plain_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld16(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(G[u].x) | bf16x2_nonfinite(G[u].y) |
+                           bf16x2_nonfinite(G[u].z) | bf16x2_nonfinite(G[u].w);
+                plain_x2<K>(s, coef, G[u].x, P[u].x, M[u].x, V[u].x);
+                plain_x2<K>(s, coef, G[u].y, P[u].y, M[u].y, V[u].y);
+                plain_x2<K>(s, coef, G[u].z, P[u].z, M[u].z, V[u].z);
+                plain_x2<K>(s, coef, G[u].w, P[u].w, M[u].w, V[u].w);
+                st16(p + i * kVec, P[u]);
+                st16(m + i * kVec, M[u]);
+                st16(v + i * kVec, V[u]);
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        plain_x1<K>(s, coef, gh, ph, mh, vh);
+        p[i] = ph; m[i] = mh; v[i] = vh;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void plain_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        plain_x1<K>(s, coef, gh, ph, mh, vh);
+        p[i] = ph; m[i] = mh; v[i] = vh;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_v32_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                    const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], C[kUnroll];
+        F8 V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+                C[u] = ld16(c + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                const uint32_t pw[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
+                const uint32_t mw[4] = {M[u].x, M[u].y, M[u].z, M[u].w};
+                const uint32_t cw[4] = {C[u].x, C[u].y, C[u].z, C[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t po[4], mo[4], co[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint16_t ph0, mh0, ch0, ph1, mh1, ch1;
+                    kahan_v32_x1<K>(s, coef, bf16_lo(gw[j]), bf16_lo(pw[j]), bf16_lo(mw[j]),
+                                    V[u].x[2 * j], bf16_lo(cw[j]), ph0, mh0, ch0);
+                    kahan_v32_x1<K>(s, coef, bf16_hi(gw[j]), bf16_hi(pw[j]), bf16_hi(mw[j]),
+                                    V[u].x[2 * j + 1], bf16_hi(cw[j]), ph1, mh1, ch1);
+                    po[j] = uint32_t(ph0) | (uint32_t(ph1) << 16);
+                    mo[j] = uint32_t(mh0) | (uint32_t(mh1) << 16);
+                    co[j] = uint32_t(ch0) | (uint32_t(ch1) << 16);
+                }
+                st16(p + i * kVec, make_uint4(po[0], po[1], po[2], po[3]));
+                st16(m + i * kVec, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+                st32(v + i * kVec, V[u]);
+                st16(c + i * kVec, make_uint4(co[0], co[1], co[2], co[3]));
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float vi = v[i];
+        uint16_t ph, mh, ch;
+        kahan_v32_x1<K>(s, coef, from_bf16(gh), from_bf16(p[i]), from_bf16(m[i]), vi,
+                        from_bf16(c[i]), ph, mh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vi; c[i] = ch;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_v32_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                     const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float vi = v[i];
+        uint16_t ph, mh, ch;
+        kahan_v32_x1<K>(s, coef, from_bf16(gh), from_bf16(p[i]), from_bf16(m[i]), vi,
+                        from_bf16(c[i]), ph, mh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vi; c[i] = ch;
+    }
+}
+
 // Remainder mode: the fp32 master is the bf16 parameter (high half) plus a
 // signed 16-bit remainder of the bit pattern.
 __device__ __forceinline__ float join_master(uint32_t hi_bits, uint32_t rem16) {
@@ -493,9 +688,15 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
         } else if (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
             if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
             else mixed_elem_chunk<K>(cur, len, s, coef, bad);
-        } else {
+        } else if (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
             if (vec) remainder_vec_chunk<K>(cur, len, s, coef, bad);
             else remainder_elem_chunk<K>(cur, len, s, coef, bad);
+        } else if (MODE == ADAMW_MODE_BF16_PLAIN) {
+            if (vec) plain_vec_chunk<K>(cur, len, s, coef, bad);
+            else plain_elem_chunk<K>(cur, len, s, coef, bad);
+        } else {
+            if (vec) kahan_v32_vec_chunk<K>(cur, len, s, coef, bad);
+            else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
         }
         cur = nxt;
     }
@@ -503,6 +704,211 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
         if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
     }
 }
+
+// ------------------------------------------- bulk-copy staged update (A) --
+//
+// Mode A with the five input streams of each stage brought into shared
+// memory by cp.async.bulk (one 1-D bulk copy per stream, completion counted
+// on an mbarrier) instead of by per-thread 16-byte loads.  Thread 0 issues
+// stage j + NS while the CTA computes stage j from shared memory; results
+// go straight to global memory with 16-byte stores.  Every mbarrier wait is
+// bounded: a wait that does not complete sets *err and the CTA returns.
+#ifndef ADAMW_BULK
+#define ADAMW_BULK 0
+#endif
+#if ADAMW_BULK
+#ifndef ADAMW_BULK_STAGES
+#define ADAMW_BULK_STAGES 2
+#endif
+#ifndef ADAMW_BULK_ELEMS
+#define ADAMW_BULK_ELEMS 4096
+#endif
+constexpr int kBulkStages = ADAMW_BULK_STAGES;
+constexpr int kBulkElems = ADAMW_BULK_ELEMS;  // per stage, multiple of kBlock * kVec
+constexpr uint32_t kBulkStreamBytes = kBulkElems * 2;
+constexpr size_t kBulkSmem = size_t(kBulkStages) * 5 * kBulkStreamBytes;
+static_assert(kBulkElems % (kBlock * kVec) == 0, "a stage is whole vectors of the block");
+constexpr uint32_t kWaitLimit = 1u << 20;  // try_wait rounds (about a second) before giving up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false after kWaitLimit rounds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+struct BulkJob {
+    uint16_t* p;
+    const uint16_t* g;
+    uint16_t* m;
+    uint16_t* v;
+    uint16_t* c;
+    int32_t n;  // elements, a multiple of kVec
+};
+
+template <int K>
+__global__ void __launch_bounds__(kBlock)
+adamw_update_bulk_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
+                         StepScalars s, const NormOut* __restrict__ norm,
+                         int32_t* __restrict__ report, int32_t* __restrict__ err) {
+    extern __shared__ __align__(128) unsigned char stage_buf[];
+    __shared__ __align__(8) uint64_t bar[kBulkStages];
+    __shared__ BulkJob job[kBulkStages];
+    __shared__ int32_t njobs_sh;
+
+    float coef = 1.0f;
+    if (K == kClip) {
+        if (norm->nonfinite) return;
+        coef = norm->coef;
+    }
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    auto buf = [&](int slot, int stream) {
+        return reinterpret_cast<uint16_t*>(stage_buf + (size_t(slot) * 5 + stream) * kBulkStreamBytes);
+    };
+
+    // producer state (thread 0 only): next chunk and element offset to issue
+    int32_t pci = c0;
+    int64_t poff = 0;
+    auto issue = [&](int slot) {
+        while (pci < c1) {
+            const ChunkPtr ch = load_chunk(chunks + pci);
+            const int64_t len8 = (ch.len2 & 1) ? ((ch.len2 >> 1) / kVec * kVec) : 0;
+            if (poff < len8) {
+                const int32_t n = int32_t(len8 - poff < kBulkElems ? len8 - poff : kBulkElems);
+                BulkJob& jb = job[slot];
+                jb.p = static_cast<uint16_t*>(ch.p) + poff;
+                jb.g = static_cast<const uint16_t*>(ch.g) + poff;
+                jb.m = static_cast<uint16_t*>(ch.m) + poff;
+                jb.v = static_cast<uint16_t*>(ch.v) + poff;
+                jb.c = static_cast<uint16_t*>(ch.a) + poff;
+                jb.n = n;
+                const uint32_t bytes = uint32_t(n) * 2;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(&bar[slot], 5 * bytes);
+                bulk_load(buf(slot, 0), jb.p, bytes, &bar[slot]);
+                bulk_load(buf(slot, 1), jb.g, bytes, &bar[slot]);
+                bulk_load(buf(slot, 2), jb.m, bytes, &bar[slot]);
+                bulk_load(buf(slot, 3), jb.v, bytes, &bar[slot]);
+                bulk_load(buf(slot, 4), jb.c, bytes, &bar[slot]);
+                poff += n;
+                return;
+            }
+            ++pci;
+            poff = 0;
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        int32_t nj = 0;
+        for (int32_t ci = c0; ci < c1; ++ci) {
+            const ChunkPtr ch = load_chunk(chunks + ci);
+            const int64_t len8 = (ch.len2 & 1) ? ((ch.len2 >> 1) / kVec * kVec) : 0;
+            nj += int32_t((len8 + kBulkElems - 1) / kBulkElems);
+        }
+        njobs_sh = nj;
+        for (int i = 0; i < kBulkStages; ++i) mbar_init(&bar[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int i = 0; i < kBulkStages && i < nj; ++i) issue(i);
+    }
+    __syncthreads();
+    const int32_t njobs = njobs_sh;
+    bool bad = false;
+    int32_t j = 0;
+    for (; j < njobs; ++j) {
+        const int slot = j % kBulkStages;
+        const bool ok = mbar_wait_bounded(&bar[slot], uint32_t(j / kBulkStages) & 1u);
+        if (__syncthreads_or(!ok)) break;
+        const BulkJob jb = job[slot];
+        const int32_t nvec = jb.n / kVec;
+#pragma unroll
+        for (int u = 0; u < kBulkElems / (kBlock * kVec); ++u) {
+            const int32_t i = u * kBlock + threadIdx.x;
+            if (i < nvec) {
+                uint4 P = *reinterpret_cast<const uint4*>(buf(slot, 0) + i * kVec);
+                const uint4 G = *reinterpret_cast<const uint4*>(buf(slot, 1) + i * kVec);
+                uint4 M = *reinterpret_cast<const uint4*>(buf(slot, 2) + i * kVec);
+                uint4 V = *reinterpret_cast<const uint4*>(buf(slot, 3) + i * kVec);
+                uint4 C = *reinterpret_cast<const uint4*>(buf(slot, 4) + i * kVec);
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(G.x) | bf16x2_nonfinite(G.y) | bf16x2_nonfinite(G.z) |
+                           bf16x2_nonfinite(G.w);
+                kahan_x2<K>(s, coef, G.x, P.x, M.x, V.x, C.x);
+                kahan_x2<K>(s, coef, G.y, P.y, M.y, V.y, C.y);
+                kahan_x2<K>(s, coef, G.z, P.z, M.z, V.z, C.z);
+                kahan_x2<K>(s, coef, G.w, P.w, M.w, V.w, C.w);
+                st16(jb.p + i * kVec, P);
+                st16(jb.m + i * kVec, M);
+                st16(jb.v + i * kVec, V);
+                st16(jb.c + i * kVec, C);
+            }
+        }
+        __syncthreads();  // every thread is done with the slot
+        if (threadIdx.x == 0 && j + kBulkStages < njobs) issue(slot);
+    }
+    if (j < njobs) {
+        // a wait ran out: report it, let the copies already issued land
+        // (bounded), and leave without touching anything else
+        if (threadIdx.x == 0) {
+            atomicExch(err, 1);
+            for (int32_t k = j; k < njobs && k < j + kBulkStages; ++k)
+                mbar_wait_bounded(&bar[k % kBulkStages], uint32_t(k / kBulkStages) & 1u);
+        }
+        return;
+    }
+    // element path: tensors that are not 16-byte aligned, and vector tails
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        const ChunkPtr ch = load_chunk(chunks + ci);
+        const int64_t len = ch.len2 >> 1;
+        if (ch.len2 & 1) {
+            const int64_t len8 = len / kVec * kVec;
+            if (len8 < len) {
+                ChunkPtr t = ch;
+                t.p = static_cast<uint16_t*>(ch.p) + len8;
+                t.g = static_cast<const uint16_t*>(ch.g) + len8;
+                t.m = static_cast<uint16_t*>(ch.m) + len8;
+                t.v = static_cast<uint16_t*>(ch.v) + len8;
+                t.a = static_cast<uint16_t*>(ch.a) + len8;
+                kahan_elem_chunk<K>(t, len - len8, s, coef, bad);
+            }
+        } else {
+            kahan_elem_chunk<K>(ch, len, s, coef, bad);
+        }
+    }
+    if (K == kReport) {
+        if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
+    }
+}
+#endif  // ADAMW_BULK
 
 // Error-free fp32 accumulation of non-negative terms: s + e is the exact sum
 // of everything added since the last flush, up to the rounding of e itself.
@@ -762,6 +1168,23 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
     }
 }
 
+// The linear warm-up / linear decay schedule on the device: d_hp->lr for the
+// update t = *d_step + 1, with the host function's fp64 operations.
+__global__ void lr_linear_warmup_kernel(adamw_hparams_t* __restrict__ d_hp,
+                                        const int64_t* __restrict__ d_step, float base_lr,
+                                        int64_t warmup, int64_t total) {
+    const int64_t k = *d_step;  // applied updates before this one
+    double f;
+    if (k < warmup) {
+        f = __ddiv_rn(double(k), double(warmup > 1 ? warmup : 1));
+    } else {
+        const double span = double((total - warmup) > 1 ? (total - warmup) : 1);
+        f = __ddiv_rn(double(total - k), span);
+        if (f < 0.0) f = 0.0;
+    }
+    d_hp->lr = __double2float_rn(__dmul_rn(double(base_lr), f));
+}
+
 // Plain 16-byte streaming copy (HBM ceiling probe).
 __global__ void __launch_bounds__(kBlock)
 copy_probe_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n) {
@@ -782,9 +1205,10 @@ copy_probe_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_
 
 struct DeviceInfo {
     int sms = 0;
-    int occ[kModes][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
+    int occ[kModes][3] = {};
     int occ_norm = 0;
     int occ_copy = 0;
+    int occ_bulk[3] = {0, 0, 0};
 };
 
 std::mutex g_dev_mu;
@@ -811,13 +1235,31 @@ int device_info(int dev, DeviceInfo* out) {
         const void* fns[kModes][3] = {
             {update_fn<0, kPlain>(), update_fn<0, kClip>(), update_fn<0, kReport>()},
             {update_fn<1, kPlain>(), update_fn<1, kClip>(), update_fn<1, kReport>()},
-            {update_fn<2, kPlain>(), update_fn<2, kClip>(), update_fn<2, kReport>()}};
+            {update_fn<2, kPlain>(), update_fn<2, kClip>(), update_fn<2, kReport>()},
+            {update_fn<3, kPlain>(), update_fn<3, kClip>(), update_fn<3, kReport>()},
+            {update_fn<4, kPlain>(), update_fn<4, kClip>(), update_fn<4, kReport>()}};
         for (int m = 0; m < kModes; ++m)
             for (int k = 0; k < 3; ++k)
                 if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ[m][k], fns[m][k],
                                                                            kBlock, 0),
                              "occupancy"))
                     return ADAMW_ERR_CUDA;
+#if ADAMW_BULK
+        {
+            const void* bulk_fns[3] = {reinterpret_cast<const void*>(&adamw_update_bulk_kernel<kPlain>),
+                                       reinterpret_cast<const void*>(&adamw_update_bulk_kernel<kClip>),
+                                       reinterpret_cast<const void*>(&adamw_update_bulk_kernel<kReport>)};
+            for (int k = 0; k < 3; ++k) {
+                if (!cuda_ok(cudaFuncSetAttribute(bulk_fns[k],
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  int(kBulkSmem)), "cudaFuncSetAttribute") ||
+                    !cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_bulk[k], bulk_fns[k],
+                                                                           kBlock, kBulkSmem),
+                             "occupancy"))
+                    return ADAMW_ERR_CUDA;
+            }
+        }
+#endif
         if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                          &d.occ_norm, norm_partial_kernel, kBlock, 0), "occupancy") ||
             !cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -869,6 +1311,7 @@ struct adamw_plan {
     int32_t* flag = nullptr;
     NormOut* norm = nullptr;
     StepRecord* rec = nullptr;     // device-resident step path
+    int32_t* status = nullptr;     // set by a kernel whose bounded wait ran out
 };
 
 namespace {
@@ -883,9 +1326,26 @@ cudaError_t launch_update(const adamw_plan* P, const StepScalars& s, int32_t* re
     return cudaGetLastError();
 }
 
+#if ADAMW_BULK
+template <int K>
+cudaError_t launch_bulk(const adamw_plan* P, const StepScalars& s, int32_t* report,
+                        cudaStream_t st) {
+    adamw_update_bulk_kernel<K><<<P->upd.grid, kBlock, kBulkSmem, st>>>(
+        P->upd.chunks, P->upd.cta_begin, s, P->norm, report, P->status);
+    return cudaGetLastError();
+}
+#endif
+
 template <bool DEV>
 cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& s,
                               int32_t* report, cudaStream_t st) {
+#if ADAMW_BULK
+    if (!DEV && P->mode == ADAMW_MODE_BF16_KAHAN) {
+        if (kind == kPlain) return launch_bulk<kPlain>(P, s, report, st);
+        if (kind == kClip) return launch_bulk<kClip>(P, s, report, st);
+        return launch_bulk<kReport>(P, s, report, st);
+    }
+#endif
     if (P->mode == ADAMW_MODE_BF16_KAHAN) {
         if (kind == kPlain) return launch_update<0, kPlain, DEV>(P, s, report, st);
         if (kind == kClip) return launch_update<0, kClip, DEV>(P, s, report, st);
@@ -896,9 +1356,19 @@ cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& 
         if (kind == kClip) return launch_update<1, kClip, DEV>(P, s, report, st);
         return launch_update<1, kReport, DEV>(P, s, report, st);
     }
-    if (kind == kPlain) return launch_update<2, kPlain, DEV>(P, s, report, st);
-    if (kind == kClip) return launch_update<2, kClip, DEV>(P, s, report, st);
-    return launch_update<2, kReport, DEV>(P, s, report, st);
+    if (P->mode == ADAMW_MODE_MIXED_BF16_REMAINDER) {
+        if (kind == kPlain) return launch_update<2, kPlain, DEV>(P, s, report, st);
+        if (kind == kClip) return launch_update<2, kClip, DEV>(P, s, report, st);
+        return launch_update<2, kReport, DEV>(P, s, report, st);
+    }
+    if (P->mode == ADAMW_MODE_BF16_PLAIN) {
+        if (kind == kPlain) return launch_update<3, kPlain, DEV>(P, s, report, st);
+        if (kind == kClip) return launch_update<3, kClip, DEV>(P, s, report, st);
+        return launch_update<3, kReport, DEV>(P, s, report, st);
+    }
+    if (kind == kPlain) return launch_update<4, kPlain, DEV>(P, s, report, st);
+    if (kind == kClip) return launch_update<4, kClip, DEV>(P, s, report, st);
+    return launch_update<4, kReport, DEV>(P, s, report, st);
 }
 
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
@@ -924,7 +1394,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int dev = 0;
     if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice")) return ADAMW_ERR_CUDA;
-    rc = check_device_access(host_table, n_tensors, dev);
+    rc = check_device_access(host_table, n_tensors, mode, dev);
     if (rc != ADAMW_OK) return rc;
     DeviceInfo di;
     rc = device_info(dev, &di);
@@ -932,6 +1402,10 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int occ = di.occ[mode][kPlain];
     for (int k = 0; k < 3; ++k) occ = occ < di.occ[mode][k] ? occ : di.occ[mode][k];
+#if ADAMW_BULK
+    if (mode == ADAMW_MODE_BF16_KAHAN)
+        for (int k = 0; k < 3; ++k) occ = occ < di.occ_bulk[k] ? occ : di.occ_bulk[k];
+#endif
     if (occ < 1) occ = 1;
     const int occ_norm = di.occ_norm > 0 ? di.occ_norm : 1;
 
@@ -977,6 +1451,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_f = off; off = align_up(off + sizeof(int32_t) * size_t(grid_norm), 256);
     const size_t o_n = off; off = align_up(off + sizeof(NormOut), 256);
     const size_t o_r = off; off = align_up(off + sizeof(StepRecord), 256);
+    const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;
@@ -992,6 +1467,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->flag = reinterpret_cast<int32_t*>(b + o_f);
     P->norm = reinterpret_cast<NormOut*>(b + o_n);
     P->rec = reinterpret_cast<StepRecord*>(b + o_r);
+    P->status = reinterpret_cast<int32_t*>(b + o_s);
 
     auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
         return bytes == 0 || cuda_ok(cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice), what);
@@ -1110,6 +1586,29 @@ extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
     const int kind = clip ? kClip : (!want_norm && d_nonfinite) ? kReport : kPlain;
     int32_t* report = (kind == kReport) ? d_nonfinite : nullptr;
     if (!cuda_ok(launch_update_any<true>(plan, kind, StepScalars{}, report, st), "update launch"))
+        return ADAMW_ERR_CUDA;
+    return ADAMW_OK;
+}
+
+extern "C" int adamw_lr_linear_warmup_device(adamw_hparams_t* d_hp, const int64_t* d_step,
+                                             float base_lr, int64_t warmup, int64_t total,
+                                             adamw_stream_t stream) {
+    if (!d_hp || !d_step || warmup < 0 || total < 0 || !std::isfinite(base_lr))
+        return ADAMW_ERR_INVALID_ARG;
+    lr_linear_warmup_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        d_hp, d_step, base_lr, warmup, total);
+    return cuda_ok(cudaGetLastError(), "schedule launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
+}
+
+extern "C" int adamw_plan_device_status(adamw_plan_t plan, int32_t* out) {
+    if (!plan || !out) return ADAMW_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return ADAMW_ERR_CUDA;
+    const int32_t zero = 0;
+    if (!cuda_ok(cudaMemcpy(out, plan->status, sizeof(int32_t), cudaMemcpyDeviceToHost),
+                 "cudaMemcpy(status)") ||
+        !cuda_ok(cudaMemcpy(plan->status, &zero, sizeof(int32_t), cudaMemcpyHostToDevice),
+                 "cudaMemcpy(status)"))
         return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }

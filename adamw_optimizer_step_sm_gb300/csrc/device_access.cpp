@@ -12,7 +12,9 @@
 
 namespace adamw {
 
-int check_device_access(const adamw_tensor_t* table, int32_t n, int device) {
+int check_device_access(const adamw_tensor_t* table, int32_t n, int32_t mode, int device) {
+    int64_t es[5];
+    element_sizes(mode, es);
     int pageable = 0;
     if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, device) != cudaSuccess) {
         set_cuda_error("cudaDeviceGetAttribute", cudaGetErrorString(cudaGetLastError()));
@@ -22,7 +24,9 @@ int check_device_access(const adamw_tensor_t* table, int32_t n, int device) {
         const adamw_tensor_t& t = table[k];
         if (t.numel == 0) continue;
         const void* ptrs[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
-        for (const void* p : ptrs) {
+        for (int s = 0; s < 5; ++s) {
+            if (es[s] == 0) continue;  // a buffer the mode does not use
+            const void* p = ptrs[s];
             cudaPointerAttributes a{};
             if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
                 set_cuda_error("cudaPointerGetAttributes", cudaGetErrorString(cudaGetLastError()));

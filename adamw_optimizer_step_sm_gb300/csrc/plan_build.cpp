@@ -44,19 +44,18 @@ int vector_head(const adamw_tensor_t& t, int32_t mode) {
 }  // namespace
 
 void element_sizes(int32_t mode, int64_t es[5]) {
-    const int64_t param = (mode == ADAMW_MODE_MIXED_FP32_MASTER) ? 4 : 2;
-    const int64_t moments = (mode == ADAMW_MODE_BF16_KAHAN) ? 2 : 4;
-    es[0] = param;
-    es[1] = 2;
-    es[2] = moments;
-    es[3] = moments;
-    es[4] = 2;
+    // param, grad, exp_avg, exp_avg_sq, aux (0: aux unused)
+    static const int64_t table[kModes][5] = {
+        {2, 2, 2, 2, 2},  // bf16 Kahan
+        {4, 2, 4, 4, 2},  // mixed fp32 master
+        {2, 2, 4, 4, 2},  // mixed bf16 + remainder
+        {2, 2, 2, 2, 0},  // bf16 without compensation
+        {2, 2, 2, 4, 2},  // bf16 Kahan, fp32 variance
+    };
+    for (int s = 0; s < 5; ++s) es[s] = table[mode][s];
 }
 
-bool valid_mode(int32_t mode) {
-    return mode == ADAMW_MODE_BF16_KAHAN || mode == ADAMW_MODE_MIXED_FP32_MASTER ||
-           mode == ADAMW_MODE_MIXED_BF16_REMAINDER;
-}
+bool valid_mode(int32_t mode) { return mode >= 0 && mode < kModes; }
 
 void set_cuda_error(const char* where, const char* what) {
     g_cuda_error = std::string(where) + ": " + what;
@@ -76,6 +75,7 @@ int validate_table(const adamw_tensor_t* table, int32_t n, int32_t mode) {
         if (t.numel == 0) continue;
         const void* ptrs[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
         for (int s = 0; s < 5; ++s) {
+            if (es[s] == 0) continue;  // a buffer the mode does not use
             if (!ptrs[s]) return ADAMW_ERR_INVALID_ARG;
             if (!aligned(ptrs[s], uintptr_t(es[s]))) return ADAMW_ERR_MISALIGNED;
         }
@@ -249,7 +249,7 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
         d.g = at(t.grad, es[1]);
         d.m = at(t.exp_avg, es[2]);
         d.v = at(t.exp_avg_sq, es[3]);
-        d.a = at(t.aux, es[4]);
+        d.a = es[4] ? at(t.aux, es[4]) : nullptr;
         d.len2 = 2 * c.len + c.vec;
     }
 }
@@ -297,6 +297,24 @@ extern "C" int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step,
     out5[3] = s.omb2;
     out5[4] = s.lrwd;
     return ADAMW_OK;
+}
+
+// The recipe's linear schedule ("--lr_scheduler_type linear --warmup_steps
+// W"): the update with k = step - 1 applied updates before it uses
+// lr * k / max(1, W) while k < W, then lr * max(0, (T - k) / max(1, T - W)).
+extern "C" float adamw_lr_linear_warmup(float base_lr, int64_t step, int64_t warmup,
+                                        int64_t total) {
+    if (step < 1 || warmup < 0 || total < 0) return 0.0f;
+    const int64_t k = step - 1;
+    double f;
+    if (k < warmup) {
+        f = double(k) / double(warmup > 1 ? warmup : 1);
+    } else {
+        const double span = double((total - warmup) > 1 ? (total - warmup) : 1);
+        f = double(total - k) / span;
+        if (f < 0.0) f = 0.0;
+    }
+    return float(double(base_lr) * f);
 }
 
 extern "C" const char* adamw_status_string(int status) {

@@ -34,12 +34,16 @@ SEED = 42   # the run recipes on the pages pass --seed 42
 MODE_BF16_KAHAN = 0
 MODE_MIXED = 1
 MODE_REMAINDER = 2
+MODE_BF16_PLAIN = 3
+MODE_BF16_KAHAN_V32 = 4
 
-# torch dtypes of (param, exp_avg/exp_avg_sq, aux) per mode
+# torch dtypes of (param, exp_avg, exp_avg_sq, aux) per mode (None: unused)
 MODE_DTYPES = {
-    MODE_BF16_KAHAN: (torch.bfloat16, torch.bfloat16, torch.bfloat16),
-    MODE_MIXED: (torch.float32, torch.float32, torch.bfloat16),
-    MODE_REMAINDER: (torch.bfloat16, torch.float32, torch.int16),
+    MODE_BF16_KAHAN: (torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16),
+    MODE_MIXED: (torch.float32, torch.float32, torch.float32, torch.bfloat16),
+    MODE_REMAINDER: (torch.bfloat16, torch.float32, torch.float32, torch.int16),
+    MODE_BF16_PLAIN: (torch.bfloat16, torch.bfloat16, torch.bfloat16, None),
+    MODE_BF16_KAHAN_V32: (torch.bfloat16, torch.bfloat16, torch.float32, torch.bfloat16),
 }
 
 
@@ -150,6 +154,15 @@ WORKLOADS: dict[str, Workload] = {
         max_grad_norm=1.0, g_std=1e-2, inf_at=(3, 200, 12345),
         description="OPT-1.3b tensor list, bf16 param + 16-bit remainder master, "
                     "global-norm clip 1.0, +inf injected at step 3"),
+    "opt1.3b_bf16_plain": Workload(
+        "opt1.3b_bf16_plain", MODE_BF16_PLAIN, OPT_1_3B, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, g_std=1e-2,
+        heavy_tail=True, description="OPT-1.3b tensor list, pure bf16 without Kahan "
+                                     "compensation"),
+    "opt1.3b_bf16_kahan_v32": Workload(
+        "opt1.3b_bf16_kahan_v32", MODE_BF16_KAHAN_V32, OPT_1_3B, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, g_std=1e-2,
+        heavy_tail=True, description="OPT-1.3b tensor list, bf16 Kahan with fp32 variance"),
     # profiling-size case of the clipped mixed step (2 GB of state, > L2)
     "opt125m_mixed_clip": Workload(
         "opt125m_mixed_clip", MODE_MIXED, OPT_125M, 5,
@@ -198,10 +211,12 @@ class State:
     param: torch.Tensor        # bf16 (mode 0) or fp32 master (mode 1)
     exp_avg: torch.Tensor
     exp_avg_sq: torch.Tensor
-    aux: torch.Tensor          # bf16 compensation / bf16 param out / int16 remainder
+    aux: torch.Tensor | None   # bf16 compensation / bf16 param out / int16 remainder
     offsets: list[int] = field(default_factory=list)
 
-    def views(self, flat: torch.Tensor) -> list[torch.Tensor]:
+    def views(self, flat: torch.Tensor | None) -> list:
+        if flat is None:
+            return [None] * len(self.offsets)
         return [flat[o:o + n] for o, n in zip(self.offsets, self.workload.numels)]
 
 
@@ -222,12 +237,12 @@ def make_state(w: Workload, device="cpu", align_elems: int = 8, skew: int = 0) -
             dst.zero_()
         else:
             dst.copy_(_draw_normal(spec.numel, w.p_std, gen, device))
-    pdt, mdt, adt = MODE_DTYPES[w.mode]
+    pdt, mdt, vdt, adt = MODE_DTYPES[w.mode]
     # remainder mode starts from bf16-exact masters: the remainder is zero
     param = p32.to(pdt) if pdt != torch.float32 else p32
     del p32
-    z = lambda dt: torch.zeros(length, dtype=dt, device=device)
-    return State(w, param, z(mdt), z(mdt), z(adt), offs)
+    z = lambda dt: torch.zeros(length, dtype=dt, device=device) if dt is not None else None
+    return State(w, param, z(mdt), z(vdt), z(adt), offs)
 
 
 def make_grad(w: Workload, step: int, device="cpu", offsets: list[int] | None = None,

@@ -45,8 +45,11 @@ def bytes_per_param(w: W.Workload) -> int:
     bf16 Kahan: read p, g, m, v, c (10) + write p, m, v, c (8) = 18.
     mixed: read master, m, v (12) + g (2), write master, m, v (12) + p_out (2)
     = 28.  remainder: read p, r (4) + m, v (8) + g (2), write p, r, m, v (12)
-    = 26.  With clipping the norm pass reads g once more: +2."""
-    base = {W.MODE_BF16_KAHAN: 18, W.MODE_MIXED: 28, W.MODE_REMAINDER: 26}[w.mode]
+    = 26.  bf16 plain: read p, g, m, v (8), write p, m, v (6) = 14.  bf16
+    Kahan with fp32 v: read 12, write 10 = 22.  With clipping the norm pass
+    reads g once more: +2."""
+    base = {W.MODE_BF16_KAHAN: 18, W.MODE_MIXED: 28, W.MODE_REMAINDER: 26,
+            W.MODE_BF16_PLAIN: 14, W.MODE_BF16_KAHAN_V32: 22}[w.mode]
     return base + (2 if w.max_grad_norm > 0 else 0)
 
 
@@ -190,8 +193,12 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arr
                 o.bf16_kahan(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
             elif ws.mode == W.MODE_MIXED:
                 o.mixed(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
-            else:
+            elif ws.mode == W.MODE_REMAINDER:
                 o.remainder(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
+            elif ws.mode == W.MODE_BF16_PLAIN:
+                o.bf16_plain(p[sl], g[sl], m[sl], v[sl], hp, t, coef)
+            else:
+                o.bf16_kahan_v32(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
 
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, pieces))
@@ -199,9 +206,11 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arr
     return sum(numels) * steps / dt, dt, threads
 
 
-def host_array(t: torch.Tensor):
+def host_array(t: torch.Tensor | None):
     """Host numpy copy with the oracle's dtype (bf16 as uint16 bits)."""
     import numpy as np
+    if t is None:
+        return None
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
@@ -492,9 +501,12 @@ def run_gpu(args):
         "config": {
             "workload": w.name, "description": w.description, "n_params": N,
             "n_tensors": w.n_tensors,
-            "mode": {0: "bf16_kahan", 1: "mixed_fp32_master", 2: "mixed_bf16_remainder"}[w.mode],
+            "mode": {0: "bf16_kahan", 1: "mixed_fp32_master", 2: "mixed_bf16_remainder",
+                     3: "bf16_plain", 4: "bf16_kahan_fp32_variance"}[w.mode],
             "storage": {0: "bf16 p/g/m/v/c", 1: "fp32 master/m/v, bf16 g and param out",
-                        2: "bf16 p + int16 remainder, fp32 m/v, bf16 g"}[w.mode],
+                        2: "bf16 p + int16 remainder, fp32 m/v, bf16 g",
+                        3: "bf16 p/g/m/v, no compensation",
+                        4: "bf16 p/g/m/c, fp32 v"}[w.mode],
             "clip": clip, "bytes_per_param": bpp, "hparams": w.hparams(),
             "l2": (f"256 MiB written before every timed step (L2 flushed; {bpp * N / 1e6:.1f} MB "
                    "moved per step)") if flush else

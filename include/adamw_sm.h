@@ -26,6 +26,12 @@
  *       ADAMW_MODE_MIXED_FP32_MASTER's; p16 is the master rounded to nearest,
  *       ties away from zero.
  *
+ *   ADAMW_MODE_BF16_PLAIN  AnyPrecisionAdamW with use_kahan_summation=false:
+ *       bf16 p, g, m, v, no compensation buffer (aux unused, may be NULL).
+ *
+ *   ADAMW_MODE_BF16_KAHAN_FP32_VAR  AnyPrecisionAdamW with bf16 momentum and
+ *       compensation and variance_dtype=float32: bf16 p, g, m, c, fp32 v.
+ *
  * Arithmetic (identical in both modes up to storage; fp32, one IEEE
  * round-to-nearest per operation, no fused multiply-add):
  *   host, fp64 rounded once to fp32:  step_size = lr / (1 - beta1^t),
@@ -39,6 +45,8 @@
  *   mixed mode: master' = master - upd ; p_out = bf16(master')
  *   remainder mode: master = join(p16, r16) ; master' = master - upd ;
  *       (p16', r16') = split(master')
+ *   bf16 plain: p' = bf16(p - upd)
+ *   bf16 Kahan fp32 variance: as bf16 mode with v' kept in fp32
  *   clipping:   norm = sqrt(sum g^2) over every tensor of the plan;
  *       coef = min(1, max_grad_norm / (norm + 1e-6)); a non-finite gradient
  *       anywhere sets the non-finite flag and the step writes no state.
@@ -64,6 +72,8 @@ typedef struct CUstream_st* adamw_stream_t;
 #define ADAMW_MODE_BF16_KAHAN 0
 #define ADAMW_MODE_MIXED_FP32_MASTER 1
 #define ADAMW_MODE_MIXED_BF16_REMAINDER 2
+#define ADAMW_MODE_BF16_PLAIN 3
+#define ADAMW_MODE_BF16_KAHAN_FP32_VAR 4
 
 /* adamw_plan_create flags. */
 #define ADAMW_PLAN_NORM 1 /* allocate the global-norm workspace (clipping) */
@@ -86,12 +96,17 @@ typedef struct CUstream_st* adamw_stream_t;
  * pinned host memory needs no separate host-to-device copy.  The five buffers
  * of one tensor hold `numel` elements each and must not overlap one another
  * (different tensors may not overlap either).
- *              bf16 Kahan            | mixed fp32 master   | mixed remainder
- *   param      bf16 p (read/write)   | fp32 master (r/w)   | bf16 p (r/w)
- *   grad       bf16 g (read)         | bf16 g (read)       | bf16 g (read)
- *   exp_avg    bf16 m (r/w)          | fp32 m (r/w)        | fp32 m (r/w)
- *   exp_avg_sq bf16 v (r/w)          | fp32 v (r/w)        | fp32 v (r/w)
- *   aux        bf16 Kahan c (r/w)    | bf16 p out (write)  | int16 r (r/w)
+ *              bf16 Kahan          | mixed fp32 master  | mixed remainder
+ *   param      bf16 p (read/write) | fp32 master (r/w)  | bf16 p (r/w)
+ *   grad       bf16 g (read)       | bf16 g (read)      | bf16 g (read)
+ *   exp_avg    bf16 m (r/w)        | fp32 m (r/w)       | fp32 m (r/w)
+ *   exp_avg_sq bf16 v (r/w)        | fp32 v (r/w)       | fp32 v (r/w)
+ *   aux        bf16 Kahan c (r/w)  | bf16 p out (write) | int16 r (r/w)
+ *              bf16 plain          | bf16 Kahan fp32 variance
+ *   param      bf16 p (r/w)        | bf16 p (r/w)
+ *   exp_avg    bf16 m (r/w)        | bf16 m (r/w)
+ *   exp_avg_sq bf16 v (r/w)        | fp32 v (r/w)
+ *   aux        unused (NULL ok)    | bf16 Kahan c (r/w)
  * Element alignment is required (2 B for 16-bit, 4 B for fp32 buffers).  Tensors whose
  * five bases are all 16-byte aligned take the vectorised path; others are
  * still updated correctly, more slowly.  numel may be 0. */
@@ -197,12 +212,34 @@ int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp, int64_t* d
                       int32_t flags, double* d_grad_norm, int32_t* d_nonfinite,
                       adamw_stream_t stream);
 
+/* The run recipe's learning-rate schedule ("--lr_scheduler_type linear
+ * --warmup_steps W", transformers PR #21312, "Train from scratch") for the
+ * update `step` (>= 1) of a run of `total` updates: with k = step - 1,
+ * base_lr * k / max(1, W) while k < W, then base_lr * max(0, (total - k) /
+ * max(1, total - W)); fp64, rounded once to fp32.  The first update of a
+ * warm-up therefore has lr 0.  Host-only; returns 0 for step < 1 or negative
+ * W or total. */
+float adamw_lr_linear_warmup(float base_lr, int64_t step, int64_t warmup, int64_t total);
+
+/* The same schedule on the device, for the device-resident step: writes
+ * d_hp->lr for the update *d_step + 1 (d_step as in adamw_step_device),
+ * bit-identical to adamw_lr_linear_warmup.  One single-thread launch on
+ * stream; capturable in a CUDA graph before adamw_step_device.
+ * Errors: INVALID_ARG, CUDA. */
+int adamw_lr_linear_warmup_device(adamw_hparams_t* d_hp, const int64_t* d_step, float base_lr,
+                                  int64_t warmup, int64_t total, adamw_stream_t stream);
+
 /* The global gradient L2 norm and non-finite flag of the plan's gradients,
  * without an update (the two-stage reduction the clipped step runs first).
  * d_grad_norm and d_nonfinite as in adamw_step (either may be NULL).
  * Errors: INVALID_ARG, NO_NORM, CUDA. */
 int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm,
                     int32_t* d_nonfinite, adamw_stream_t stream);
+
+/* Reads and clears the plan's device status word (synchronous): 0, or 1 when
+ * a kernel of this plan gave up on a bounded wait (the launch then left its
+ * work undone; nothing waits forever).  Errors: INVALID_ARG, CUDA. */
+int adamw_plan_device_status(adamw_plan_t plan, int32_t* out);
 
 /* Releases the plan's device memory (synchronises the plan's device first).
  * NULL is accepted. */

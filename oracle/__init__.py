@@ -89,6 +89,9 @@ class Oracle:
         L.oracle_adamw_bf16_plain.argtypes = [vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_mixed.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_remainder.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_adamw_bf16_kahan_v32.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_lr_linear_warmup.argtypes = [f32, i64, i64, i64]
+        L.oracle_lr_linear_warmup.restype = f32
         L.oracle_split_master.argtypes = [vp, vp, vp, i64]
         L.oracle_join_master.argtypes = [vp, vp, vp, i64]
         L.oracle_grad_sumsq.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_double),
@@ -150,6 +153,17 @@ class Oracle:
         self.lib.oracle_adamw_remainder(_ptr(p16), _ptr(g), _ptr(m), _ptr(v), _ptr(r16), n,
                                         ctypes.byref(hp), t, coef)
 
+    def bf16_kahan_v32(self, p, g, m, v, c, hp: Hparams, t: int, coef: float = 1.0):
+        n = p.size
+        for a, dt in ((p, np.uint16), (g, np.uint16), (m, np.uint16), (v, np.float32),
+                      (c, np.uint16)):
+            _check(a, dt, n)
+        self.lib.oracle_adamw_bf16_kahan_v32(_ptr(p), _ptr(g), _ptr(m), _ptr(v), _ptr(c), n,
+                                             ctypes.byref(hp), t, coef)
+
+    def lr_linear_warmup(self, base_lr: float, t: int, warmup: int, total: int) -> float:
+        return float(np.float32(self.lib.oracle_lr_linear_warmup(base_lr, t, warmup, total)))
+
     def split_master(self, x: np.ndarray):
         x = np.ascontiguousarray(x, dtype=np.float32)
         p16 = np.empty(x.shape, np.uint16)
@@ -185,15 +199,17 @@ class Oracle:
         """``tensors``: list of (param, grad, exp_avg, exp_avg_sq, aux) numpy
         arrays.  Returns (skipped: bool, norm: float)."""
         arr = (TensorEntry * max(1, len(tensors)))()
-        pt = np.float32 if mode == 1 else np.uint16
-        mv = np.uint16 if mode == 0 else np.float32
-        at = np.int16 if mode == 2 else np.uint16
+        u16, f32, i16 = np.uint16, np.float32, np.int16
+        want = {0: (u16, u16, u16, u16), 1: (f32, f32, f32, u16), 2: (u16, f32, f32, i16),
+                3: (u16, u16, u16, None), 4: (u16, u16, f32, u16)}[mode]
         for k, (p, g, m, v, a) in enumerate(tensors):
             n = g.size
-            _check(p, pt, n); _check(g, np.uint16, n); _check(m, mv, n)
-            _check(v, mv, n); _check(a, at, n)
+            _check(p, want[0], n); _check(g, np.uint16, n); _check(m, want[1], n)
+            _check(v, want[2], n)
+            if want[3] is not None:
+                _check(a, want[3], n)
             arr[k] = TensorEntry(p.ctypes.data, g.ctypes.data, m.ctypes.data,
-                                 v.ctypes.data, a.ctypes.data, n)
+                                 v.ctypes.data, a.ctypes.data if a is not None else None, n)
         norm = ctypes.c_double(0.0)
         rc = self.lib.oracle_adamw_list_step(arr, len(tensors), mode,
                                              ctypes.byref(hp), t,

@@ -48,6 +48,9 @@
  *   mixed mode (fp32 master/m/v, bf16 grad in, bf16 param out):
  *     master' = master - upd ;  p_out = bf16(master')
  *
+ *   bf16 without compensation (use_kahan_summation=false): p' = bf16(p - upd)
+ *   bf16 Kahan with fp32 variance (variance_dtype=float32): v' kept in fp32
+ *
  *   remainder mode (the same update; the fp32 master is stored as the bf16
  *   parameter plus a 16-bit remainder, 10 B/param of optimizer state: "2 FP32
  *   optim state + 1 16-bit master param" in the memory estimate of
@@ -230,6 +233,58 @@ void oracle_adamw_bf16_plain(uint16_t* p, const uint16_t* g, uint16_t* m,
     }
 }
 
+/* bf16 parameters, bf16 momentum and compensation, fp32 variance (the
+ * run recipe's optim_args with variance_dtype=float32): the same Kahan step
+ * as oracle_adamw_bf16_kahan with v kept (and used) in fp32. */
+void oracle_adamw_bf16_kahan_v32(uint16_t* p, const uint16_t* g, uint16_t* m,
+                                 float* v, uint16_t* c, int64_t n,
+                                 const oracle_hparams_t* hp, int64_t t, float coef)
+{
+    step_scalars_t s = make_scalars(hp, t);
+    const float b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps;
+    const int clip = hp->max_grad_norm > 0.0f;
+
+    for (int64_t i = 0; i < n; ++i) {
+        float gi = bf16_bits_to_f32(g[i]);
+        if (clip) gi = gi * coef;
+        float p0 = bf16_bits_to_f32(p[i]);
+        float c0 = bf16_bits_to_f32(c[i]);
+        float m1 = (b1 * bf16_bits_to_f32(m[i])) + (s.omb1 * gi);
+        float v1 = (b2 * v[i]) + ((s.omb2 * gi) * gi);
+        uint16_t m1h = f32_to_bf16_rne(m1);
+        float den = (sqrtf(v1) / s.sbc2) + eps;
+        float upd = (s.step_size * (bf16_bits_to_f32(m1h) / den)) + (s.lrwd * p0);
+        float y = c0 - upd;
+        uint16_t pnh = f32_to_bf16_rne(p0 + y);
+        float pn = bf16_bits_to_f32(pnh);
+        p[i] = pnh;
+        m[i] = m1h;
+        v[i] = v1;
+        c[i] = f32_to_bf16_rne(y - (pn - p0));
+    }
+}
+
+/* ----------------------------------------------------- learning rate -- */
+
+/* The recipe's --lr_scheduler_type linear --warmup_steps W for T training
+ * steps: the update with t applied steps before it (k = t - 1) uses
+ * lr * k / max(1, W) while k < W, then lr * max(0, (T - k) / max(1, T - W));
+ * fp64, rounded once to fp32.  (The first update of a warm-up therefore uses
+ * lr 0, as a scheduler that advances after each optimizer step does.) */
+float oracle_lr_linear_warmup(float base_lr, int64_t t, int64_t warmup, int64_t total)
+{
+    int64_t k = t - 1;
+    double f;
+    if (k < warmup)
+        f = (double)k / (double)(warmup > 1 ? warmup : 1);
+    else {
+        double span = (double)((total - warmup) > 1 ? (total - warmup) : 1);
+        f = (double)(total - k) / span;
+        if (f < 0.0) f = 0.0;
+    }
+    return (float)((double)base_lr * f);
+}
+
 /* ----------------------------------------------------------- mixed mode -- */
 
 /* One step over one shard: fp32 master, m, v in place; bf16 grad read;
@@ -374,7 +429,8 @@ typedef struct {
 } oracle_tensor_t;
 
 /* The whole optimizer step over a tensor list (host buffers), mode 0 = bf16
- * Kahan, mode 1 = mixed, mode 2 = remainder.  With clipping, the norm is taken first over every
+ * Kahan, 1 = mixed, 2 = remainder, 3 = bf16 without compensation (aux
+ * unused), 4 = bf16 Kahan with fp32 variance.  With clipping, the norm is taken first over every
  * tensor; a non-finite gradient anywhere makes the call write nothing and
  * return 1 (the caller must not advance t).  Returns 0 after an applied step.
  * norm_out (nullable) receives the fp64 norm when clipping. */
@@ -404,6 +460,14 @@ int32_t oracle_adamw_list_step(const oracle_tensor_t* list, int32_t n_tensors,
             oracle_adamw_remainder((uint16_t*)e->param, (const uint16_t*)e->grad,
                                    (float*)e->exp_avg, (float*)e->exp_avg_sq,
                                    (int16_t*)e->aux, e->numel, hp, t, coef);
+        else if (mode == 3)
+            oracle_adamw_bf16_plain((uint16_t*)e->param, (const uint16_t*)e->grad,
+                                    (uint16_t*)e->exp_avg, (uint16_t*)e->exp_avg_sq,
+                                    e->numel, hp, t, coef);
+        else if (mode == 4)
+            oracle_adamw_bf16_kahan_v32((uint16_t*)e->param, (const uint16_t*)e->grad,
+                                        (uint16_t*)e->exp_avg, (float*)e->exp_avg_sq,
+                                        (uint16_t*)e->aux, e->numel, hp, t, coef);
         else
             oracle_adamw_mixed((float*)e->param, (const uint16_t*)e->grad,
                                (float*)e->exp_avg, (float*)e->exp_avg_sq,

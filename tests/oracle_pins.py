@@ -417,6 +417,76 @@ def pin_bias_correction_powers(o: O.Oracle):
             assert np.all(np.abs(got - want) <= tol), (b1, b2, t, got, want)
 
 
+# ------------------------------------------- other AnyPrecision options --
+
+def pin_first_step_bf16_plain_and_v32(o: O.Oracle):
+    """t = 1 closed form for the two other storage options: without
+    compensation p' is the nearest bf16 to p - upd; with fp32 variance only
+    the bf16 momentum rounds (half the error budget of the all-bf16 mode)."""
+    p32, g32 = _first_step_inputs(seed=14)
+    ph, gh = torch_bf16_bits(p32), torch_bf16_bits(g32)
+    hp = O.hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    g, p0 = bf16_to_f64(gh), bf16_to_f64(ph)
+    lr, eps, wd = f32(1e-3), f32(1e-8), f32(0.1)
+    adam = lr * g / (np.abs(g) + eps)
+    want = p0 - adam - lr * wd * p0
+    # no compensation
+    p, m, v = ph.copy(), np.zeros_like(ph), np.zeros_like(ph)
+    o.bf16_plain(p, gh, m, v, hp, 1)
+    err = np.abs(bf16_to_f64(p) - want)
+    assert np.all(err <= 0.5 * ulp_bf16(want) + 6e-3 * np.abs(adam) + 8 * ulp_f32(p0))
+    # fp32 variance: v exact to fp32, p + c within the bf16-momentum error
+    p, m, c = ph.copy(), np.zeros_like(ph), np.zeros_like(ph)
+    v32 = np.zeros(ph.size, F32)
+    o.bf16_kahan_v32(p, gh, m, v32, c, hp, 1)
+    assert np.all(np.abs(v32 - (1 - f32(0.95)) * g * g) <= 4 * EPS32 * np.abs(v32) + 1e-45)
+    got = bf16_to_f64(p) + bf16_to_f64(c)
+    cn = bf16_to_f64(c)
+    tol = 4.1e-3 * np.abs(adam) + 0.5 * ulp_bf16(cn) * (cn != 0) + 8 * ulp_f32(p0)
+    assert np.all(np.abs(got - want) <= tol), f"v32 first step off by {np.max(np.abs(got - want) / tol):.3g}"
+
+
+def pin_torch_adamw_fp64_vs_v32(o: O.Oracle, steps: int = 10):
+    """fp32 variance mode against fp64 torch.optim.AdamW: the variance agrees
+    to fp32 rounding (1e-5 relative after 10 steps), unlike the bf16 variance
+    of the all-bf16 mode; momentum within its bf16 storage error."""
+    r = _rng(15)
+    n = 64
+    ph = torch_bf16_bits((r.standard_normal(n) * 0.02).astype(F32))
+    grads_h = [torch_bf16_bits((r.standard_normal(n) * 1e-2).astype(F32)) for _ in range(steps)]
+    hp = O.hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    p, m, c = ph.copy(), np.zeros_like(ph), np.zeros_like(ph)
+    v = np.zeros(n, F32)
+    for t, gh in enumerate(grads_h, 1):
+        o.bf16_kahan_v32(p, gh, m, v, c, hp, t)
+    tg = [torch.from_numpy(bf16_to_f64(gh)) for gh in grads_h]
+    tp, tm, tv = _torch_adamw(torch.from_numpy(bf16_to_f64(ph)), tg, f32(2e-4),
+                              (f32(0.9), f32(0.95)), f32(1e-8), f32(0.1))
+    tp, tm, tv = tp.numpy(), tm.numpy(), tv.numpy()
+    # v is fed by the exact bf16 gradients; only m's bf16 rounding differs
+    assert np.all(np.abs(v - tv) <= 1e-5 * np.abs(tv) + 1e-30), "fp32 variance vs fp64"
+    assert np.max(np.abs(bf16_to_f64(m) - tm)) <= 0.02 * np.max(np.abs(tm))
+    got = bf16_to_f64(p) + bf16_to_f64(c)
+    assert np.all(np.abs(got - tp) <= 0.02 * steps * f32(2e-4) + ulp_bf16(bf16_to_f64(c)))
+
+
+def pin_lr_linear_warmup(o: O.Oracle):
+    """The recipe's linear schedule with 500 warm-up steps (here over 1000
+    training steps): lr 0 on the first update, half at 250 applied steps,
+    the peak at 500, half again at 750, 0 from 1000 on; linear in between."""
+    base, W_, T_ = f32(2e-4), 500, 1000
+    lr = lambda t: o.lr_linear_warmup(base, t, W_, T_)
+    assert lr(1) == 0.0
+    assert lr(251) == f32(base * 0.5) and lr(501) == base and lr(751) == f32(base * 0.5)
+    assert lr(1001) == 0.0 and lr(5000) == 0.0
+    up = [lr(t) for t in range(1, 502)]
+    down = [lr(t) for t in range(501, 1002)]
+    assert all(a <= b for a, b in zip(up, up[1:])) and all(a >= b for a, b in zip(down, down[1:]))
+    assert abs(lr(101) - base * 100 / 500) <= 2 * EPS32 * base
+    # no warm-up: the peak from the first update
+    assert o.lr_linear_warmup(base, 1, 0, 1000) == base
+
+
 # ------------------------------------------------------- remainder mode --
 
 def pin_remainder_split_roundtrip(o: O.Oracle, n_random: int = 1 << 22):
@@ -467,6 +537,9 @@ def pin_remainder_equals_mixed_master(o: O.Oracle, steps: int = 12):
 
 
 ALL_PINS = [
+    pin_first_step_bf16_plain_and_v32,
+    pin_torch_adamw_fp64_vs_v32,
+    pin_lr_linear_warmup,
     pin_remainder_split_roundtrip,
     pin_remainder_equals_mixed_master,
     pin_bias_correction_powers,

@@ -34,8 +34,10 @@ def to_f32(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().numpy().astype(np.float32, copy=False)
 
 
-def to_np(t: torch.Tensor) -> np.ndarray:
+def to_np(t: torch.Tensor | None) -> np.ndarray | None:
     """Host copy with the oracle's dtype: bf16 -> uint16 bits, int16, fp32."""
+    if t is None:
+        return None
     if t.dtype == torch.bfloat16:
         return to_u16(t)
     if t.dtype == torch.int16:
@@ -114,7 +116,7 @@ class GpuSide:
     def __init__(self, w: W.Workload, device="cuda", state: W.State | None = None):
         self.w = w
         self.st = state or W.make_state(w, device)
-        self.g = torch.zeros(self.st.aux.numel(), dtype=torch.bfloat16, device=self.st.aux.device)
+        self.g = torch.zeros(self.st.param.numel(), dtype=torch.bfloat16, device=self.st.param.device)
         v = self.st.views
         self.plan = A.Plan(v(self.st.param), v(self.g), v(self.st.exp_avg), v(self.st.exp_avg_sq),
                            v(self.st.aux), w.mode, norm=True)
@@ -159,12 +161,16 @@ class OracleRun:
             self.o.bf16_kahan(p, g, m, v, a, hp, t, coef)
         elif self.w.mode == W.MODE_MIXED:
             self.o.mixed(p, g, m, v, a, hp, t, coef)
-        else:
+        elif self.w.mode == W.MODE_REMAINDER:
             self.o.remainder(p, g, m, v, a, hp, t, coef)
+        elif self.w.mode == W.MODE_BF16_PLAIN:
+            self.o.bf16_plain(p, g, m, v, hp, t, coef)
+        else:
+            self.o.bf16_kahan_v32(p, g, m, v, a, hp, t, coef)
 
     def views(self, name, k):
         o, n = self.offsets[k], self.numels[k]
-        return self.a[name][o:o + n]
+        return None if self.a[name] is None else self.a[name][o:o + n]
 
     def step(self, g_flat: np.ndarray, hp: O.Hparams):
         """Returns (skipped, norm, nonfinite)."""
@@ -201,7 +207,8 @@ def compare_state(gpu: GpuSide, ref: OracleRun, rep: Report | None = None) -> Re
         if n == 0:
             continue
         for name in ("param", "exp_avg", "exp_avg_sq", "aux"):
-            compare(rep, f"tensor {k} {name}", got[name][o:o + n], ref.a[name][o:o + n])
+            if got[name] is not None:
+                compare(rep, f"tensor {k} {name}", got[name][o:o + n], ref.a[name][o:o + n])
     return rep
 
 
@@ -245,7 +252,8 @@ def sample_indices(gpu: GpuSide, per_tensor: int, seed: int = 0) -> np.ndarray:
     entries = []
     v = st.views
     for tensors in zip(v(st.param), v(gpu.g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux)):
-        entries.append(tuple(t.data_ptr() for t in tensors) + (tensors[0].numel(),))
+        entries.append(tuple(t.data_ptr() if t is not None else 0 for t in tensors)
+                       + (tensors[0].numel(),))
     for c in A.adamw_plan_chunks(entries, w.mode, gpu.plan.info.grid):
         o = st.offsets[c.tensor] + c.offset
         for d in (0, 1, 7, 8, c.len - 9, c.len - 8, c.len - 1):
@@ -265,8 +273,9 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
     idx = sample_indices(gpu, per_tensor)
     it = torch.from_numpy(idx).to(device)
     st = gpu.st
-    arrays = dict(param=to_np(st.param[it]), exp_avg=to_np(st.exp_avg[it]),
-                  exp_avg_sq=to_np(st.exp_avg_sq[it]), aux=to_np(st.aux[it]))
+    take = lambda x: None if x is None else to_np(x[it])
+    arrays = dict(param=take(st.param), exp_avg=take(st.exp_avg),
+                  exp_avg_sq=take(st.exp_avg_sq), aux=take(st.aux))
     ref = OracleRun(w, arrays, [idx.size], [0])
     o = ref.o
     hp_g, hp_o = hp_pair(w)
@@ -293,9 +302,10 @@ def run_sampled(w: W.Workload, per_tensor: int = 2048, steps: int | None = None,
             rep.failures.append(f"step {k}: skip/flag gpu=({skipped},{flag}) oracle=({oskipped},{bad})")
         if clip and abs(gnorm - norm) > 1e-12 * norm:
             rep.failures.append(f"step {k}: norm gpu {gnorm!r} oracle {norm!r}")
-    got = dict(param=to_np(st.param[it]), exp_avg=to_np(st.exp_avg[it]),
-               exp_avg_sq=to_np(st.exp_avg_sq[it]), aux=to_np(st.aux[it]))
+    got = dict(param=take(st.param), exp_avg=take(st.exp_avg),
+               exp_avg_sq=take(st.exp_avg_sq), aux=take(st.aux))
     for name in ("param", "exp_avg", "exp_avg_sq", "aux"):
-        compare(rep, f"sampled {name}", got[name], ref.a[name])
+        if got[name] is not None:
+            compare(rep, f"sampled {name}", got[name], ref.a[name])
     gpu.plan.close()
     return rep, log

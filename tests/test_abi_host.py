@@ -165,3 +165,17 @@ def test_gpu_entry_points_fail_loudly_without_a_gpu():
     with pytest.raises(A.AdamWError) as e:
         A.adamw_plan_create([_fake(0, 64)], 0)
     assert e.value.status == A.ADAMW_ERR_CUDA
+
+
+@pytest.mark.parametrize("warmup,total", [(500, 1000), (0, 100), (1, 1), (7, 3), (500, 500), (3, 10**7)])
+def test_lr_schedule_agrees_with_the_oracle(warmup, total):
+    """The library's and the oracle's linear warm-up schedules, computed
+    independently from the recipe's definition, agree bit for bit."""
+    o = oracle.load()
+    for t in list(range(1, 30)) + [warmup, warmup + 1, warmup + 2, total - 1, total, total + 1,
+                                   total + 5, 10**6]:
+        if t < 1:
+            continue
+        a = np.float32(A.adamw_lr_linear_warmup(np.float32(2e-4), t, warmup, total))
+        b = np.float32(o.lr_linear_warmup(np.float32(2e-4), t, warmup, total))
+        assert a.view(np.uint32) == b.view(np.uint32), (t, a, b)

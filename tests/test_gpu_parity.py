@@ -87,6 +87,13 @@ def test_remainder_mode_holds_the_mixed_mode_master():
     m.plan.close()
 
 
+@pytest.mark.parametrize("name", ["opt1.3b_bf16_plain", "opt1.3b_bf16_kahan_v32"])
+def test_other_anyprecision_options_sampled_full_size(name):
+    rep, log = H.run_sampled(W.WORKLOADS[name], per_tensor=512)
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
 def test_opt1_3b_bf16_kahan_sampled_full_size():
     rep, log = H.run_sampled(W.WORKLOADS["opt1.3b_bf16_kahan"], per_tensor=1024)
     _assert(rep, log)
@@ -109,7 +116,8 @@ def test_opt1_3b_mixed_clip_inf_skip_sampled_full_size():
 
 # ------------------------------------------------------------- edge cases --
 
-@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER,
+                                  W.MODE_BF16_PLAIN, W.MODE_BF16_KAHAN_V32])
 @pytest.mark.parametrize("clip", [0.0, 0.5])
 @pytest.mark.parametrize("layout", [(8, 0), (1, 3), (1, 1)])
 def test_ragged_lists(mode, clip, layout):
@@ -366,7 +374,8 @@ def _twin(w):
 
 def _same_state(x, y):
     for p, q in zip((x.param, x.exp_avg, x.exp_avg_sq, x.aux), (y.param, y.exp_avg, y.exp_avg_sq, y.aux)):
-        assert torch.equal(p.view(torch.uint8), q.view(torch.uint8))
+        if p is not None:
+            assert torch.equal(p.view(torch.uint8), q.view(torch.uint8))
 
 
 @pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_BF16_KAHAN, 0.5),
@@ -444,6 +453,42 @@ def test_device_step_replayed_from_a_cuda_graph(mode, clip):
         graph.replay()
     torch.cuda.synchronize()
     assert int(d_step.item()) == 6
+    _same_state(a.st, b_state)
+    for p in (a.plan, b_plan, wa.plan, wb_plan):
+        p.close()
+
+
+def test_schedule_and_step_replayed_from_a_cuda_graph():
+    """The recipe's linear warm-up schedule and the step, both on the device,
+    captured once and replayed: every update uses the schedule's lr for its
+    own t, bit-identical to the host path fed the oracle's schedule."""
+    import oracle as O
+    o = O.load()
+    w = _small("sched", steps=8)
+    a, b_state, b_plan = _twin(w)
+    base, warm, total = 2e-4, 3, 6
+    d_hp = A.device_hparams(A.hparams(**w.hparams()))
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    warm_state = _small("warm2", sizes=[64], steps=1)
+    wa, wb_state, wb_plan = _twin(warm_state)
+    scratch_hp = A.device_hparams(A.hparams())
+    scratch_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    A.adamw_lr_linear_warmup_device(scratch_hp.data_ptr(), scratch_step.data_ptr(), base, warm, total,
+                                    torch.cuda.current_stream().cuda_stream)
+    wb_plan.step_device(scratch_hp, scratch_step, 0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        A.adamw_lr_linear_warmup_device(d_hp.data_ptr(), d_step.data_ptr(), base, warm, total,
+                                        torch.cuda.current_stream().cuda_stream)
+        b_plan.step_device(d_hp, d_step, 0)
+    for k in range(1, 9):
+        a.set_grad(k)
+        lr = o.lr_linear_warmup(np.float32(base), k, warm, total)
+        a.step(A.hparams(**{**w.hparams(), "lr": lr}), want_flag=False)
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(d_step.item()) == 8
     _same_state(a.st, b_state)
     for p in (a.plan, b_plan, wa.plan, wb_plan):
         p.close()

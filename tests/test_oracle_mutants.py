@@ -63,6 +63,15 @@ MUTANTS = [
      "    *r16 = (int16_t)(int32_t)(((uint32_t)hi << 16) - u);\n"),
     ("remainder_mode_no_decay", "        float upd = (s.step_size * (m1 / den)) + (s.lrwd * p0);\n        float pn = p0 - upd;\n        m[i] = m1;",
      "        float upd = (s.step_size * (m1 / den));\n        float pn = p0 - upd;\n        m[i] = m1;"),
+    ("v32_variance_rounded", "        v[i] = v1;\n        c[i] = f32_to_bf16_rne(y - (pn - p0));\n",
+     "        v[i] = bf16_bits_to_f32(f32_to_bf16_rne(v1));\n        c[i] = f32_to_bf16_rne(y - (pn - p0));\n"),
+    ("v32_comp_sign", "        c[i] = f32_to_bf16_rne(y - (pn - p0));\n",
+     "        c[i] = f32_to_bf16_rne(y + (pn - p0));\n"),
+    ("plain_update_sign", "        p[i] = f32_to_bf16_rne(p0 - upd);\n",
+     "        p[i] = f32_to_bf16_rne(p0 + upd);\n"),
+    ("lr_no_warmup", "    if (k < warmup)\n", "    if (k < 0)\n"),
+    ("lr_decay_off_by_one", "        f = (double)(total - k) / span;\n",
+     "        f = (double)(total - k - 1) / span;\n"),
     ("clip_scale_ignored_mixed", "float p0 = master[i];\n",
      "float p0 = master[i]; gi = bf16_bits_to_f32(g[i]);\n"),
 ]
