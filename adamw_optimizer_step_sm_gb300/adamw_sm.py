@@ -25,6 +25,7 @@ MODE_MIXED_BF16_REMAINDER = 2
 MODE_BF16_PLAIN = 3
 MODE_BF16_KAHAN_FP32_VAR = 4
 PLAN_NORM = 1
+PLAN_NO_FUSE = 2
 STEP_CLIP = 1
 STEP_NORM = 2
 
@@ -61,7 +62,7 @@ class adamw_plan_info_t(ctypes.Structure):
                 ("block", ctypes.c_int32), ("n_chunks", ctypes.c_int64),
                 ("scalar_elems", ctypes.c_int64), ("device", ctypes.c_int32),
                 ("has_norm", ctypes.c_int32), ("norm_grid", ctypes.c_int32),
-                ("pad_", ctypes.c_int32)]
+                ("fused", ctypes.c_int32)]
 
 
 class adamw_chunk_t(ctypes.Structure):
@@ -257,7 +258,7 @@ class Plan:
     """
 
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, auxs, mode: int,
-                 norm: bool = False):
+                 norm: bool = False, fuse: bool = True):
         import torch
         if auxs is None:
             auxs = [None] * len(list(params))
@@ -292,7 +293,8 @@ class Plan:
         self.mode = mode
         dev = lists[0][0].device if n else torch.device("cuda", torch.cuda.current_device())
         with torch.cuda.device(dev):
-            self.handle = adamw_plan_create(entries, mode, PLAN_NORM if norm else 0)
+            self.handle = adamw_plan_create(entries, mode, (PLAN_NORM if norm else 0)
+                                            | (0 if fuse else PLAN_NO_FUSE))
         self.device = dev
         self.info = adamw_plan_get_info(self.handle)
 

@@ -17,6 +17,9 @@ namespace adamw {
 constexpr int kBlock = ADAMW_BLOCK;
 // Elements per vector: 8 bf16 = one 16-byte load; 8 fp32 = two.
 constexpr int kVec = 8;
+// Largest gradient list (bytes) whose clipped steps run as one fused
+// launch: half of GB300's 129 MB L2, so the norm pass leaves g in L2.
+constexpr int64_t kFusedMaxGradBytes = int64_t(64) << 20;
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.
 constexpr int64_t kMinElemsPerCta = int64_t(kBlock) * kVec;

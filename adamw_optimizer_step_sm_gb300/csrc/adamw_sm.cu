@@ -656,6 +656,11 @@ __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]), fetching the
 // next chunk's descriptor before working on the current one.
+template <int MODE, int K>
+__device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                           int32_t c1, const StepScalars& s, float coef,
+                                           bool& bad);
+
 // DEV: the scalars, clip coefficient and skip decision come from the
 // StepRecord the device-resident step path's prologue wrote.
 template <int MODE, int K, bool DEV>
@@ -674,7 +679,18 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
         coef = norm->coef;
     }
     bool bad = false;
-    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    update_cta<MODE, K>(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], s, coef, bad);
+    if (K == kReport) {
+        if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
+    }
+}
+
+// ---- the CTA's share of the update: chunks [c0, c1), each chunk's
+// descriptor fetched one ahead.
+template <int MODE, int K>
+__device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                           int32_t c1, const StepScalars& s, float coef,
+                                           bool& bad) {
     ChunkPtr cur;
     if (c0 < c1) cur = load_chunk(chunks + c0);
     for (int32_t ci = c0; ci < c1; ++ci) {
@@ -699,9 +715,6 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
             else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
         }
         cur = nxt;
-    }
-    if (K == kReport) {
-        if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
     }
 }
 
@@ -992,11 +1005,22 @@ __device__ __forceinline__ double block_sum(double x) {
 // 64 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
 // inf or NaN gradients) recomputes its elements in fp64, which also decides
 // the non-finite flag.
+__device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                                 int32_t c1, double* __restrict__ partial,
+                                                 int32_t* __restrict__ flag);
+
 __global__ void __launch_bounds__(kBlock)
 norm_partial_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin,
                     double* __restrict__ partial, int32_t* __restrict__ flag) {
-    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    norm_partial_cta(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], partial, flag);
+}
+
+// The CTA's partial sum of squares and non-finite flag, written to
+// partial[blockIdx.x] and flag[blockIdx.x].
+__device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                                 int32_t c1, double* __restrict__ partial,
+                                                 int32_t* __restrict__ flag) {
     Sum2F32 grp;
     double acc = 0.0;
     float err = 0.0f;
@@ -1168,6 +1192,82 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
     }
 }
 
+// ---- fused clipped step (one cooperative launch) ----
+//
+// For lists whose gradients fit in L2: stage 1 of the norm, a grid barrier,
+// then every CTA sums all partials itself in the fixed order (no second
+// barrier), decides clip or skip, and updates its share -- the second read
+// of g comes from L2.  Needs every CTA resident at once (cooperative launch).
+// The barrier is a monotonic 64-bit arrival counter: the CTA whose ticket is
+// t waits until the counter reaches the next multiple of the grid.  The wait
+// is bounded: a CTA that gives up sets *status and returns without updating.
+constexpr uint32_t kBarrierSpins = 1u << 21;   // about a second with the sleeps
+
+__device__ __forceinline__ unsigned long long load_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int MODE>
+__global__ void ADAMW_UPDATE_BOUNDS
+adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
+                        const int32_t* __restrict__ upd_begin,
+                        const ChunkPtr* __restrict__ nrm_chunks,
+                        const int32_t* __restrict__ nrm_begin, StepScalars s,
+                        double* __restrict__ partial, int32_t* __restrict__ flag,
+                        NormOut* __restrict__ nout, double* __restrict__ user_norm,
+                        int32_t* __restrict__ user_flag, unsigned long long* __restrict__ arrivals,
+                        int32_t* __restrict__ status) {
+    __shared__ int passed;
+    norm_partial_cta(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1], partial, flag);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long ticket = atomicAdd(arrivals, 1ull);
+        const unsigned long long target = (ticket / gridDim.x + 1) * gridDim.x;
+        int ok = 0;
+        for (uint32_t i = 0; i < kBarrierSpins; ++i) {
+            if (load_acquire_u64(arrivals) >= target) {
+                ok = 1;
+                break;
+            }
+            __nanosleep(256);
+        }
+        if (!ok) atomicExch(status, 1);
+        passed = ok;
+    }
+    __syncthreads();
+    if (!passed) return;
+    // every CTA: the same fixed-order sum as norm_finalize_kernel
+    double x = 0.0;
+    bool bad = false;
+    for (int32_t i = threadIdx.x; i < int32_t(gridDim.x); i += kBlock) {
+        x += __ldcg(partial + i);
+        bad |= __ldcg(flag + i) != 0;
+    }
+    const double tot = block_sum(x);
+    const int any = __syncthreads_or(bad);
+    __shared__ float coef_sh;
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(tot);
+        double coef = double(s.max_grad_norm) / (norm + 1e-6);
+        if (coef > 1.0) coef = 1.0;
+        coef_sh = float(coef);
+        if (blockIdx.x == 0) {
+            nout->norm = norm;
+            nout->coef = float(coef);
+            nout->nonfinite = any;
+            if (user_norm) *user_norm = norm;
+            if (user_flag) *user_flag = any;
+        }
+    }
+    __syncthreads();
+    if (any) return;  // skipped step: no writes
+    bool unused = false;
+    update_cta<MODE, kClip>(upd_chunks, upd_begin[blockIdx.x], upd_begin[blockIdx.x + 1], s,
+                            coef_sh, unused);
+}
+
 // The linear warm-up / linear decay schedule on the device: d_hp->lr for the
 // update t = *d_step + 1, with the host function's fp64 operations.
 __global__ void lr_linear_warmup_kernel(adamw_hparams_t* __restrict__ d_hp,
@@ -1209,6 +1309,8 @@ struct DeviceInfo {
     int occ_norm = 0;
     int occ_copy = 0;
     int occ_bulk[3] = {0, 0, 0};
+    int occ_fused[kModes] = {};
+    int cooperative = 0;
 };
 
 std::mutex g_dev_mu;
@@ -1260,6 +1362,22 @@ int device_info(int dev, DeviceInfo* out) {
             }
         }
 #endif
+        {
+            const void* fused_fns[kModes] = {
+                reinterpret_cast<const void*>(&adamw_fused_clip_kernel<0>),
+                reinterpret_cast<const void*>(&adamw_fused_clip_kernel<1>),
+                reinterpret_cast<const void*>(&adamw_fused_clip_kernel<2>),
+                reinterpret_cast<const void*>(&adamw_fused_clip_kernel<3>),
+                reinterpret_cast<const void*>(&adamw_fused_clip_kernel<4>)};
+            for (int m = 0; m < kModes; ++m)
+                if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.occ_fused[m],
+                                                                           fused_fns[m], kBlock, 0),
+                             "occupancy"))
+                    return ADAMW_ERR_CUDA;
+            if (!cuda_ok(cudaDeviceGetAttribute(&d.cooperative, cudaDevAttrCooperativeLaunch, dev),
+                         "cudaDeviceGetAttribute"))
+                return ADAMW_ERR_CUDA;
+        }
         if (!cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                          &d.occ_norm, norm_partial_kernel, kBlock, 0), "occupancy") ||
             !cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -1312,6 +1430,8 @@ struct adamw_plan {
     NormOut* norm = nullptr;
     StepRecord* rec = nullptr;     // device-resident step path
     int32_t* status = nullptr;     // set by a kernel whose bounded wait ran out
+    bool fused = false;            // clipped steps run as one cooperative launch
+    unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
 };
 
 namespace {
@@ -1371,6 +1491,36 @@ cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& 
     return launch_update<4, kReport, DEV>(P, s, report, st);
 }
 
+template <int MODE>
+cudaError_t launch_fused_mode(const adamw_plan* P, const StepScalars& s, double* user_norm,
+                              int32_t* user_flag, cudaStream_t st) {
+    const ChunkPtr* uc = P->upd.chunks;
+    const int32_t* ub = P->upd.cta_begin;
+    const ChunkPtr* nc = P->nrm.chunks;
+    const int32_t* nb = P->nrm.cta_begin;
+    StepScalars sc = s;
+    double* partial = P->partial;
+    int32_t* flag = P->flag;
+    NormOut* nout = P->norm;
+    unsigned long long* arrivals = P->arrivals;
+    int32_t* status = P->status;
+    void* args[] = {&uc, &ub, &nc, &nb, &sc, &partial, &flag, &nout, &user_norm, &user_flag,
+                    &arrivals, &status};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&adamw_fused_clip_kernel<MODE>),
+                                       dim3(P->upd.grid), dim3(kBlock), args, 0, st);
+}
+
+cudaError_t launch_fused(const adamw_plan* P, const StepScalars& s, double* user_norm,
+                         int32_t* user_flag, cudaStream_t st) {
+    switch (P->mode) {
+        case 0: return launch_fused_mode<0>(P, s, user_norm, user_flag, st);
+        case 1: return launch_fused_mode<1>(P, s, user_norm, user_flag, st);
+        case 2: return launch_fused_mode<2>(P, s, user_norm, user_flag, st);
+        case 3: return launch_fused_mode<3>(P, s, user_norm, user_flag, st);
+        default: return launch_fused_mode<4>(P, s, user_norm, user_flag, st);
+    }
+}
+
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
                         int32_t* user_flag, cudaStream_t st) {
     norm_partial_kernel<<<P->nrm.grid, kBlock, 0, st>>>(P->nrm.chunks, P->nrm.cta_begin,
@@ -1388,7 +1538,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
                                  int32_t mode, int32_t flags, adamw_plan_t* out) {
     if (!out) return ADAMW_ERR_INVALID_ARG;
     *out = nullptr;
-    if (flags & ~ADAMW_PLAN_NORM) return ADAMW_ERR_INVALID_ARG;
+    if (flags & ~(ADAMW_PLAN_NORM | ADAMW_PLAN_NO_FUSE)) return ADAMW_ERR_INVALID_ARG;
     int rc = validate_table(host_table, n_tensors, mode);
     if (rc != ADAMW_OK) return rc;
 
@@ -1411,8 +1561,17 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int64_t total = 0;
     for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;
+    // Lists whose gradients fit in half of L2 run clipped steps as one fused
+    // cooperative launch (the norm pass leaves g in L2 for the update).
+    const bool fused = (flags & ADAMW_PLAN_NORM) && !(flags & ADAMW_PLAN_NO_FUSE) &&
+                       di.cooperative && di.occ_fused[mode] > 0 &&
+                       total * 2 <= kFusedMaxGradBytes;
+    if (fused) occ = occ < di.occ_fused[mode] ? occ : di.occ_fused[mode];
     const int32_t grid = choose_grid(total, di.sms * occ);
-    const int32_t grid_norm = (flags & ADAMW_PLAN_NORM) ? choose_grid(total, di.sms * occ_norm) : 0;
+    // the fused kernel's norm pass uses the update grid; plans without it
+    // give the norm pass its own, larger grid
+    const int32_t grid_norm = !(flags & ADAMW_PLAN_NORM) ? 0
+                              : fused ? grid : choose_grid(total, di.sms * occ_norm);
 
     Partition part, part_norm;
     std::vector<ChunkPtr> cp, cp_norm;
@@ -1452,6 +1611,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_n = off; off = align_up(off + sizeof(NormOut), 256);
     const size_t o_r = off; off = align_up(off + sizeof(StepRecord), 256);
     const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
+    const size_t o_a = off; off = align_up(off + sizeof(unsigned long long), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;
@@ -1468,6 +1628,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->norm = reinterpret_cast<NormOut*>(b + o_n);
     P->rec = reinterpret_cast<StepRecord*>(b + o_r);
     P->status = reinterpret_cast<int32_t*>(b + o_s);
+    P->arrivals = reinterpret_cast<unsigned long long*>(b + o_a);
+    P->fused = fused;
 
     auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
         return bytes == 0 || cuda_ok(cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice), what);
@@ -1515,6 +1677,11 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
         return ADAMW_OK;
     }
 
+    if (clip && plan->fused) {
+        if (!cuda_ok(launch_fused(plan, s, d_grad_norm, d_nonfinite, st), "fused launch"))
+            return ADAMW_ERR_CUDA;
+        return ADAMW_OK;
+    }
     int kind = kPlain;
     int32_t* report = nullptr;
     if (need_norm) {
@@ -1636,6 +1803,7 @@ extern "C" int adamw_plan_get_info(adamw_plan_t plan, adamw_plan_info_t* out) {
     out->block = kBlock;
     out->n_chunks = plan->upd.n_chunks;
     out->norm_grid = plan->nrm.grid;
+    out->fused = plan->fused ? 1 : 0;
     out->scalar_elems = plan->scalar_elems;
     out->device = plan->device;
     out->has_norm = (plan->flags & ADAMW_PLAN_NORM) ? 1 : 0;

@@ -143,6 +143,12 @@ WORKLOADS: dict[str, Workload] = {
         max_grad_norm=1.0, g_std=1e-2, inf_at=(3, 200, 12345),
         description="OPT-1.3b tensor list, fp32 master + global-norm clip 1.0, "
                     "+inf injected at step 3"),
+    "bert55m_shard_mixed_clip": Workload(
+        "bert55m_shard_mixed_clip", MODE_MIXED, (TensorSpec("shard", 13_850_000),), 20,
+        lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, g_std=1e-3,
+        max_grad_norm=1.0, inf_at=(7, 0, 4242),
+        description="one 13,850,000-element shard, fp32 master, global-norm clip 1.0 "
+                    "(one fused launch per step), +inf injected at step 7"),
     "bert55m_shard_remainder": Workload(
         "bert55m_shard_remainder", MODE_REMAINDER, (TensorSpec("shard", 13_850_000),), 20,
         lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, g_std=1e-3,

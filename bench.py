@@ -404,12 +404,12 @@ def run_gpu(args):
                       host_array(st.aux), host_array(grads[0]), list(st.offsets))
     v = st.views
     plans = [A.Plan(v(st.param), v(g), v(st.exp_avg), v(st.exp_avg_sq), v(st.aux), w.mode,
-                    norm=clip) for g in grads]
+                    norm=clip, fuse=not args.no_fuse) for g in grads]
     hp = A.hparams(**w.hparams())
     stream = torch.cuda.current_stream(device)
     norm = torch.zeros(1, dtype=torch.float64, device=device)
     flag = torch.zeros(1, dtype=torch.int32, device=device)
-    launches_per_step = 3 if clip else 1
+    launches_per_step = (1 if plans[0].info.fused else 3) if clip else 1
 
     t = 0
     for i in range(args.warmup):
@@ -513,6 +513,7 @@ def run_gpu(args):
                   f"inputs larger than L2 ({bpp * N / 1e9:.2f} GB moved per step)",
             "grads": f"{n_grad} resident grad buffers drawn before timing, cycled",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "fused_clipped_step": bool(plans[0].info.fused),
         },
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -582,6 +583,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
+    ap.add_argument("--no-fuse", action="store_true",
+                    help="run clipped steps as three launches even where one fused launch fits")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed steps
     if args.impl == "reference":

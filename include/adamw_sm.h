@@ -76,7 +76,8 @@ typedef struct CUstream_st* adamw_stream_t;
 #define ADAMW_MODE_BF16_KAHAN_FP32_VAR 4
 
 /* adamw_plan_create flags. */
-#define ADAMW_PLAN_NORM 1 /* allocate the global-norm workspace (clipping) */
+#define ADAMW_PLAN_NORM 1     /* allocate the global-norm workspace (clipping)  */
+#define ADAMW_PLAN_NO_FUSE 2  /* never run a clipped step as one fused launch   */
 
 /* Status codes (0 = success, negative = error). */
 #define ADAMW_OK 0
@@ -144,7 +145,7 @@ typedef struct {
     int32_t device;        /* CUDA device the plan lives on                 */
     int32_t has_norm;      /* ADAMW_PLAN_NORM was given                     */
     int32_t norm_grid;     /* CTAs of the norm-partial kernel (0: no norm)  */
-    int32_t pad_;
+    int32_t fused;         /* clipped steps run as one fused launch         */
 } adamw_plan_info_t;
 
 /* One piece of a tensor assigned to one CTA (host-side view of the plan). */
@@ -161,7 +162,11 @@ typedef struct {
  * flattened element space over a persistent grid (grid = SM count x resident
  * CTAs per SM, fewer for small lists), uploads the tensor table and the chunk
  * table, and (with ADAMW_PLAN_NORM) builds the norm kernel's own partition
- * and allocates the norm workspace.
+ * and allocates the norm workspace.  With ADAMW_PLAN_NORM, a list whose
+ * gradients take at most 64 MiB (half of L2) runs its clipped steps as one
+ * cooperative launch: norm partials, a bounded grid barrier, and the update
+ * reading g again from L2 (unless ADAMW_PLAN_NO_FUSE; adamw_plan_info_t.fused
+ * says which).  The norm is the same either way.
  * Synchronous (it allocates and copies).  host_table is read during the call
  * only.  On error *out is left NULL and nothing stays allocated.
  * Errors: INVALID_ARG (NULL out or table with n_tensors > 0, n_tensors < 0,

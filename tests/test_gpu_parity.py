@@ -94,6 +94,51 @@ def test_other_anyprecision_options_sampled_full_size(name):
     assert rep.exact == rep.n
 
 
+def test_fused_clipped_shard_matches_oracle():
+    """A 13.85M-element shard with clipping: each clipped step is one fused
+    cooperative launch (norm, grid barrier, update); bit-identical to the
+    oracle over 20 steps including the skipped step 7."""
+    w = W.WORKLOADS["bert55m_shard_mixed_clip"]
+    gpu = H.GpuSide(w)
+    assert gpu.plan.info.fused == 1
+    gpu.plan.close()
+    rep, log = H.run_parity(w)
+    _assert(rep, log)
+    assert [k for (k, s, *_r) in log if s] == [7]
+    assert rep.exact == rep.n
+
+
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
+def test_fused_and_unfused_clipped_steps_agree(mode):
+    """The fused launch and the three-launch path give the same bytes and the
+    same norm (the norm pass uses the same partition either way)."""
+    w = _small("fuse", mode=mode, max_grad_norm=0.5, steps=4, inf_at=(3, 8, 99))
+    a = H.GpuSide(w)
+    b_state = W.make_state(w, "cuda")
+    v = b_state.views
+    b_plan = A.Plan(v(b_state.param), v(a.g), v(b_state.exp_avg), v(b_state.exp_avg_sq),
+                    v(b_state.aux), mode, norm=True, fuse=False)
+    assert a.plan.info.fused == 1 and b_plan.info.fused == 0
+    assert a.plan.info.norm_grid == a.plan.info.grid
+    hp, _ = H.hp_pair(w)
+    nb = torch.zeros(1, dtype=torch.float64, device="cuda")
+    fb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tb = 0
+    for k in range(1, 5):
+        a.set_grad(k)
+        skipped = a.step(hp)
+        b_plan.step(hp, tb + 1, grad_norm=nb, nonfinite=fb)
+        torch.cuda.synchronize()
+        if not fb.item():
+            tb += 1
+        assert skipped == bool(fb.item()) == (k == 3)
+        assert a.norm.item() == nb.item() or (k == 3)
+    _same_state(a.st, b_state)
+    assert A.adamw_plan_device_status(a.plan.handle) == 0
+    a.plan.close()
+    b_plan.close()
+
+
 def test_opt1_3b_bf16_kahan_sampled_full_size():
     rep, log = H.run_sampled(W.WORKLOADS["opt1.3b_bf16_kahan"], per_tensor=1024)
     _assert(rep, log)
