@@ -90,6 +90,7 @@ def load() -> ctypes.CDLL:
             L.adamw_step_device.argtypes = [vp, vp, vp, i32, vp, vp, vp]
             L.adamw_plan_destroy.argtypes = [vp]
             L.adamw_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+            L.adamw_plan_test_skew_barrier.argtypes = [vp, i64]
             L.adamw_lr_linear_warmup.argtypes = [ctypes.c_float, i64, i64, i64]
             L.adamw_lr_linear_warmup.restype = ctypes.c_float
             L.adamw_lr_linear_warmup_device.argtypes = [vp, vp, ctypes.c_float, i64, i64, vp]
@@ -110,7 +111,8 @@ def load() -> ctypes.CDLL:
                          "adamw_plan_destroy", "adamw_plan_get_info", "adamw_plan_chunks",
                          "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc",
                          "adamw_step_table", "adamw_step_table_cache_clear",
-                         "adamw_plan_device_status", "adamw_lr_linear_warmup_device"):
+                         "adamw_plan_device_status", "adamw_lr_linear_warmup_device",
+                         "adamw_plan_test_skew_barrier"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -210,6 +212,11 @@ def adamw_plan_device_status(plan: int) -> int:
     out = ctypes.c_int32(0)
     _check(load().adamw_plan_device_status(plan, ctypes.byref(out)), "adamw_plan_device_status")
     return out.value
+
+
+def adamw_plan_test_skew_barrier(plan: int, delta: int) -> None:
+    """Failure-path tests only: misalign the fused step's barrier counter."""
+    _check(load().adamw_plan_test_skew_barrier(plan, delta), "adamw_plan_test_skew_barrier")
 
 
 def adamw_plan_get_info(plan: int) -> adamw_plan_info_t:

@@ -1771,13 +1771,36 @@ extern "C" int adamw_plan_device_status(adamw_plan_t plan, int32_t* out) {
     if (!plan || !out) return ADAMW_ERR_INVALID_ARG;
     DeviceGuard guard(plan->device);
     if (!guard.ok) return ADAMW_ERR_CUDA;
-    const int32_t zero = 0;
-    if (!cuda_ok(cudaMemcpy(out, plan->status, sizeof(int32_t), cudaMemcpyDeviceToHost),
-                 "cudaMemcpy(status)") ||
-        !cuda_ok(cudaMemcpy(plan->status, &zero, sizeof(int32_t), cudaMemcpyHostToDevice),
+    if (!cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize") ||
+        !cuda_ok(cudaMemcpy(out, plan->status, sizeof(int32_t), cudaMemcpyDeviceToHost),
                  "cudaMemcpy(status)"))
         return ADAMW_ERR_CUDA;
+    if (*out != 0) {
+        // a wait ran out: clear the word and realign the fused-step barrier
+        // counter (no kernel of the plan is running after the synchronise)
+        const int32_t zero = 0;
+        const unsigned long long start = 0;
+        if (!cuda_ok(cudaMemcpy(plan->status, &zero, sizeof(int32_t), cudaMemcpyHostToDevice),
+                     "cudaMemcpy(status)") ||
+            !cuda_ok(cudaMemcpy(plan->arrivals, &start, sizeof(start), cudaMemcpyHostToDevice),
+                     "cudaMemcpy(arrivals)"))
+            return ADAMW_ERR_CUDA;
+    }
     return ADAMW_OK;
+}
+
+extern "C" int adamw_plan_test_skew_barrier(adamw_plan_t plan, int64_t delta) {
+    if (!plan) return ADAMW_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return ADAMW_ERR_CUDA;
+    unsigned long long v = 0;
+    if (!cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize") ||
+        !cuda_ok(cudaMemcpy(&v, plan->arrivals, sizeof(v), cudaMemcpyDeviceToHost),
+                 "cudaMemcpy(arrivals)"))
+        return ADAMW_ERR_CUDA;
+    v += static_cast<unsigned long long>(delta);
+    return cuda_ok(cudaMemcpy(plan->arrivals, &v, sizeof(v), cudaMemcpyHostToDevice),
+                   "cudaMemcpy(arrivals)") ? ADAMW_OK : ADAMW_ERR_CUDA;
 }
 
 extern "C" int adamw_plan_destroy(adamw_plan_t plan) {

@@ -226,13 +226,15 @@ class State:
         return [flat[o:o + n] for o, n in zip(self.offsets, self.workload.numels)]
 
 
-def make_state(w: Workload, device="cpu", align_elems: int = 8, skew: int = 0) -> State:
+def make_state(w: Workload, device="cpu", align_elems: int = 8, skew: int = 0,
+               tail_pad: int = 0) -> State:
     """Initial optimizer state: params drawn, moments and aux zero.  Tensors sit
     in one flat buffer per kind at offsets rounded to ``align_elems`` elements,
-    the first one ``skew`` elements in (ragged layouts use 1 and a skew)."""
+    the first one ``skew`` elements in (ragged layouts use 1 and a skew), with
+    ``tail_pad`` spare elements after the last one."""
     offs, length = tensor_offsets(w.numels, align_elems)
     offs = [o + skew for o in offs]
-    length += skew
+    length += skew + tail_pad
     p32 = torch.zeros(length, dtype=torch.float32, device=device)
     gen = _gen(device, w.seed, 1)
     for spec, o in zip(w.tensors, offs):

@@ -241,10 +241,19 @@ int adamw_lr_linear_warmup_device(adamw_hparams_t* d_hp, const int64_t* d_step, 
 int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm,
                     int32_t* d_nonfinite, adamw_stream_t stream);
 
-/* Reads and clears the plan's device status word (synchronous): 0, or 1 when
- * a kernel of this plan gave up on a bounded wait (the launch then left its
- * work undone; nothing waits forever).  Errors: INVALID_ARG, CUDA. */
+/* Reads and clears the plan's device status word (synchronises the plan's
+ * device first): 0, or 1 when a kernel of this plan gave up on a bounded wait
+ * (every device-side wait in this library is bounded, about a second; the
+ * launch then left its CTA's work undone, so the step is partly applied).
+ * Clearing also realigns the fused step's barrier counter, so the plan is
+ * usable again.  Errors: INVALID_ARG, CUDA. */
 int adamw_plan_device_status(adamw_plan_t plan, int32_t* out);
+
+/* For failure-path tests only: shifts the fused clipped step's grid-barrier
+ * counter by `delta` (synchronous), so that in the next fused launch one
+ * CTA's bounded barrier wait runs out and sets the device status.  Never
+ * needed in normal use.  Errors: INVALID_ARG, CUDA. */
+int adamw_plan_test_skew_barrier(adamw_plan_t plan, int64_t delta);
 
 /* Releases the plan's device memory (synchronises the plan's device first).
  * NULL is accepted. */

@@ -139,6 +139,38 @@ def test_fused_and_unfused_clipped_steps_agree(mode):
     b_plan.close()
 
 
+def test_fused_barrier_wait_runs_out_and_reports():
+    """Failure detection without a GPU fault: with the barrier counter shifted
+    by one, the last CTA to arrive waits for an arrival that never comes; its
+    bounded wait (about half a second) runs out, it sets the device status and
+    returns.  The host reads the status, which also realigns the counter, and
+    the next steps run normally on the same context."""
+    import time
+    w = _small("stall", mode=W.MODE_MIXED, max_grad_norm=1.0, steps=3)
+    gpu = H.GpuSide(w)
+    assert gpu.plan.info.fused == 1
+    hp, _ = H.hp_pair(w)
+    gpu.set_grad(1)
+    gpu.step(hp)
+    assert A.adamw_plan_device_status(gpu.plan.handle) == 0
+    A.adamw_plan_test_skew_barrier(gpu.plan.handle, 1)
+    gpu.set_grad(2)
+    t0 = time.perf_counter()
+    gpu.plan.step(hp, 2, grad_norm=gpu.norm, nonfinite=gpu.flag)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert A.adamw_plan_device_status(gpu.plan.handle) == 1
+    assert 0.05 < waited < 30
+    # the context and the plan work again
+    for k in (3, 4):
+        gpu.set_grad(k)
+        gpu.plan.step(hp, k, grad_norm=gpu.norm, nonfinite=gpu.flag)
+    torch.cuda.synchronize()
+    assert A.adamw_plan_device_status(gpu.plan.handle) == 0
+    assert np.isfinite(gpu.norm.item())
+    gpu.plan.close()
+
+
 def test_opt1_3b_bf16_kahan_sampled_full_size():
     rep, log = H.run_sampled(W.WORKLOADS["opt1.3b_bf16_kahan"], per_tensor=1024)
     _assert(rep, log)
@@ -537,3 +569,36 @@ def test_schedule_and_step_replayed_from_a_cuda_graph():
     _same_state(a.st, b_state)
     for p in (a.plan, b_plan, wa.plan, wb_plan):
         p.close()
+
+
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER,
+                                  W.MODE_BF16_PLAIN, W.MODE_BF16_KAHAN_V32])
+def test_canaries_around_tensors_stay_untouched(mode):
+    """Bounds check without a sanitizer: every element of the flat buffers
+    that belongs to no tensor (the skew, the gaps between tensors, a
+    4096-element tail) holds a canary pattern, and the gradient buffer is
+    read-only; after clipped and unclipped steps not one of those bytes may
+    have changed."""
+    w = _small("canary", mode=mode, max_grad_norm=0.0, steps=3)
+    st = W.make_state(w, "cuda", align_elems=8, skew=5, tail_pad=4096)
+    gpu = H.GpuSide(w, "cuda", st)
+    covered = torch.zeros(st.param.numel(), dtype=torch.bool, device="cuda")
+    for o, n in zip(st.offsets, w.numels):
+        covered[o:o + n] = True
+    gaps = ~covered
+    bufs = [b for b in (st.param, st.exp_avg, st.exp_avg_sq, st.aux) if b is not None]
+    for b in bufs:
+        raw = b.view(torch.uint8).view(-1, b.element_size())
+        raw[gaps] = 0xA5
+    hp_plain, _ = H.hp_pair(w)
+    hp_clip = A.hparams(**{**w.hparams(), "max_grad_norm": 0.5})
+    for k in range(1, 4):
+        gpu.set_grad(k)
+        g_before = gpu.g.clone()
+        gpu.plan.step(hp_clip if k == 2 else hp_plain, k, grad_norm=gpu.norm if k == 2 else None)
+        torch.cuda.synchronize()
+        assert torch.equal(gpu.g.view(torch.int16), g_before.view(torch.int16)), "grad written"
+    for b in bufs:
+        raw = b.view(torch.uint8).view(-1, b.element_size())
+        assert bool((raw[gaps] == 0xA5).all()), f"a {b.dtype} canary changed"
+    gpu.plan.close()
