@@ -57,12 +57,12 @@ struct alignas(16) ChunkPtr {
 static_assert(sizeof(ChunkPtr) == 48, "chunk layout");
 
 // Elements per round-robin tile of the interleaved partition of the update
-// kernel (measured on GB300: 16384 beats contiguous per-CTA ranges by ~6 %
-// on the 1.3B-parameter list, because the whole grid then streams one narrow
-// window of each buffer).  Lists with fewer than two tiles per CTA, and the
+// kernel (measured on GB300: round-robin tiles beat contiguous per-CTA ranges
+// by ~6 % on the 1.3B-parameter list, because the whole grid then streams one
+// narrow window of each buffer; 8192 is 1 % faster than 16384 and 32768).  Lists with fewer than two tiles per CTA, and the
 // read-only norm pass, use contiguous ranges.
 #ifndef ADAMW_TILE_ELEMS
-#define ADAMW_TILE_ELEMS 16384
+#define ADAMW_TILE_ELEMS 8192
 #endif
 constexpr int64_t kTileElems = ADAMW_TILE_ELEMS;
 

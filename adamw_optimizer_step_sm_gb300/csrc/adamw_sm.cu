@@ -6,7 +6,7 @@
 // with about twenty fp32 operations in between.
 // That is far below the GPU's ridge point, so HBM bandwidth bounds it and the
 // kernels are built to keep DRAM streaming: a persistent grid (SMs x resident
-// CTAs) dealt 16K-element tiles of the flattened parameter space round-robin
+// CTAs) dealt 8K-element tiles of the flattened parameter space round-robin
 // (so the grid sweeps every buffer together), chunk descriptors prefetched one
 // ahead, 16-byte vector loads issued U vectors ahead of the arithmetic, fp32
 // math, 16-byte stores.  No tensor cores: nothing here is a contraction.
@@ -1192,6 +1192,49 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
     }
 }
 
+// ---- device-resident step without a norm pass: one launch ----
+//
+// Every CTA reads the hyperparameters and the step counter itself and
+// computes the scalars (the host planner's fp64 operations); the last CTA to
+// finish -- found with an arrival counter -- advances the counter and writes
+// the non-finite flag, so no CTA can read a counter that was already
+// advanced.  Invalid hyperparameters: nothing is updated, the flag is -1.
+template <int MODE, int K>
+__global__ void ADAMW_UPDATE_BOUNDS
+adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
+                         const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
+                         unsigned int* __restrict__ done, int32_t* __restrict__ flagword,
+                         int32_t* __restrict__ user_flag) {
+    __shared__ StepScalars s_sh;
+    __shared__ int valid_sh;
+    __shared__ int64_t t_sh;
+    if (threadIdx.x == 0) {
+        const adamw_hparams_t hp = *d_hp;
+        const int valid = hparams_valid_dev(hp);
+        const int64_t t = __ldcg(d_step) + 1;
+        if (valid) make_scalars_dev(hp, t, &s_sh);
+        valid_sh = valid;
+        t_sh = t;
+    }
+    __syncthreads();
+    bool bad = false;
+    if (valid_sh)
+        update_cta<MODE, K>(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], s_sh, 1.0f,
+                            bad);
+    const int any = (K == kReport) ? __syncthreads_or(bad) : 0;
+    if (threadIdx.x == 0) {
+        if (any) atomicOr(flagword, 1);
+        __threadfence();
+        if (atomicAdd(done, 1u) == gridDim.x - 1) {  // the last CTA
+            __threadfence();
+            const int32_t f = atomicExch(flagword, 0);
+            if (valid_sh) *d_step = t_sh;
+            if (user_flag) *user_flag = valid_sh ? f : -1;
+            *done = 0;
+        }
+    }
+}
+
 // ---- fused clipped step (one cooperative launch) ----
 //
 // For lists whose gradients fit in L2: stage 1 of the norm, a grid barrier,
@@ -1432,6 +1475,8 @@ struct adamw_plan {
     int32_t* status = nullptr;     // set by a kernel whose bounded wait ran out
     bool fused = false;            // clipped steps run as one cooperative launch
     unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
+    unsigned int* done = nullptr;  // finished CTAs of a one-launch device step
+    int32_t* flagword = nullptr;   // its non-finite flag, collected across CTAs
 };
 
 namespace {
@@ -1489,6 +1534,26 @@ cudaError_t launch_update_any(const adamw_plan* P, int kind, const StepScalars& 
     if (kind == kPlain) return launch_update<4, kPlain, DEV>(P, s, report, st);
     if (kind == kClip) return launch_update<4, kClip, DEV>(P, s, report, st);
     return launch_update<4, kReport, DEV>(P, s, report, st);
+}
+
+template <int MODE, int K>
+cudaError_t launch_self_mode(const adamw_plan* P, const adamw_hparams_t* d_hp, int64_t* d_step,
+                             int32_t* user_flag, cudaStream_t st) {
+    adamw_update_self_kernel<MODE, K><<<P->upd.grid, kBlock, 0, st>>>(
+        P->upd.chunks, P->upd.cta_begin, d_hp, d_step, P->done, P->flagword, user_flag);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t launch_self(const adamw_plan* P, const adamw_hparams_t* d_hp, int64_t* d_step,
+                        int32_t* user_flag, cudaStream_t st) {
+    switch (P->mode) {
+        case 0: return launch_self_mode<0, K>(P, d_hp, d_step, user_flag, st);
+        case 1: return launch_self_mode<1, K>(P, d_hp, d_step, user_flag, st);
+        case 2: return launch_self_mode<2, K>(P, d_hp, d_step, user_flag, st);
+        case 3: return launch_self_mode<3, K>(P, d_hp, d_step, user_flag, st);
+        default: return launch_self_mode<4, K>(P, d_hp, d_step, user_flag, st);
+    }
 }
 
 template <int MODE>
@@ -1612,6 +1677,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_r = off; off = align_up(off + sizeof(StepRecord), 256);
     const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
     const size_t o_a = off; off = align_up(off + sizeof(unsigned long long), 256);
+    const size_t o_d = off; off = align_up(off + 2 * sizeof(uint32_t), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;
@@ -1629,6 +1695,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->rec = reinterpret_cast<StepRecord*>(b + o_r);
     P->status = reinterpret_cast<int32_t*>(b + o_s);
     P->arrivals = reinterpret_cast<unsigned long long*>(b + o_a);
+    P->done = reinterpret_cast<unsigned int*>(b + o_d);
+    P->flagword = reinterpret_cast<int32_t*>(b + o_d + sizeof(uint32_t));
     P->fused = fused;
 
     auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
@@ -1735,6 +1803,13 @@ extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
     if (!guard.ok) {
         set_cuda_error("cudaSetDevice", cudaGetErrorString(cudaGetLastError()));
         return ADAMW_ERR_CUDA;
+    }
+    if (!want_norm && plan->upd.grid > 0) {
+        // one launch: every CTA computes the scalars, the last one advances
+        // the counter
+        const cudaError_t e = d_nonfinite ? launch_self<kReport>(plan, d_hp, d_step, d_nonfinite, st)
+                                          : launch_self<kPlain>(plan, d_hp, d_step, nullptr, st);
+        return cuda_ok(e, "update launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
     }
     const bool norm_pass = want_norm && plan->nrm.grid > 0;
     if (norm_pass) {

@@ -378,11 +378,11 @@ def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
 
 def run_gpu(args):
     world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
     A.load()
     w = W.WORKLOADS[args.workload]
     from dataclasses import replace

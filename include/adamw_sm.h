@@ -207,8 +207,10 @@ int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t step,
  * the hyperparameters in d_hp are out of range (then *d_nonfinite = -1).
  * d_grad_norm, d_nonfinite: as in adamw_step.  The scalars are computed on
  * the device with the same fp64 operations as the host path, so results are
- * bit-identical to adamw_step with the same t.  Launches: a one-CTA prologue
- * and the update, plus the norm pass when clipping or the norm is asked.
+ * bit-identical to adamw_step with the same t.  Launches: one (every CTA
+ * computes the scalars, the last one to finish advances the counter) when
+ * neither clipping nor the norm is asked; otherwise the norm pass, a one-CTA
+ * prologue and the update.
  * No host synchronisation and no allocation; all pointers are device-
  * accessible memory the caller owns (not checked here).
  * Errors: INVALID_ARG (NULL plan, d_hp or d_step, unknown flag), NO_NORM,
