@@ -91,6 +91,10 @@ struct StepRecord {
     int32_t pad_[2];
 };
 
+// Kernel flavours: plain step, clipped step (reads the norm finalize's
+// output, skips on non-finite), plain step that also reports non-finite g.
+enum Kind { kPlain = 0, kClip = 1, kReport = 2 };
+
 // ---- host planner (plan_build.cpp) ----
 
 constexpr int kModes = 5;

@@ -1,0 +1,868 @@
+// device_common.cuh -- device-side building blocks of every kernel: bf16
+// helpers, streaming 16-byte loads and stores, the per-element AdamW
+// arithmetic of each storage mode, the chunk walkers, the CTA bodies of the
+// update and of the norm pass, and the device-side per-step scalars.
+//
+// Arithmetic order follows the definition in include/adamw_sm.h exactly, with
+// the IEEE round-to-nearest intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn,
+// __fsqrt_rn) so that no multiply-add is fused and every result is the one a
+// strict host implementation of the same formula gives.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "adamw_internal.h"
+
+// Everything here has internal linkage: each translation unit that includes
+// this header compiles its own copy of what it uses.
+namespace {
+
+using namespace adamw;
+
+// ------------------------------------------------------------ helpers ----
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two fp32 -> bf16, round to nearest even, lo in the low half-word.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    uint32_t u;
+    memcpy(&u, &r, sizeof u);
+    return u;
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float from_bf16(uint16_t h) {
+    return __uint_as_float(uint32_t(h) << 16);
+}
+
+// Streaming 16-byte accesses.  Every byte is touched once per step.  The
+// cache policy of loads and stores is a build-time constant: 0 = default,
+// 1 = evict-first (.cs), 2 = L1 no-allocate, 3 = last-use (.lu) for loads.
+// Measured on GB300, the default policy is as fast as any hint for lists
+// larger than L2 and keeps L2-resident lists resident between steps.
+#ifndef ADAMW_LD_POLICY
+#define ADAMW_LD_POLICY 0
+#endif
+#ifndef ADAMW_ST_POLICY
+#define ADAMW_ST_POLICY 0
+#endif
+__device__ __forceinline__ uint4 ld16(const void* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#if ADAMW_LD_POLICY == 1
+    return __ldcs(q);
+#elif ADAMW_LD_POLICY == 2
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(q));
+    return r;
+#elif ADAMW_LD_POLICY == 3
+    return __ldlu(q);
+#else
+    return *q;
+#endif
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#if ADAMW_ST_POLICY == 1
+    __stcs(q, v);
+#else
+    *q = v;
+#endif
+}
+
+__device__ __forceinline__ bool bf16x2_nonfinite(uint32_t w) {
+    return ((w & 0x7f80u) == 0x7f80u) || ((w & 0x7f800000u) == 0x7f800000u);
+}
+
+// ------------------------------------------------ per-element arithmetic --
+
+// m' and v' of one element (fp32).
+__device__ __forceinline__ void moments(const StepScalars& s, float g, float m0,
+                                        float v0, float& m1, float& v1) {
+    m1 = __fadd_rn(__fmul_rn(s.beta1, m0), __fmul_rn(s.omb1, g));
+    v1 = __fadd_rn(__fmul_rn(s.beta2, v0), __fmul_rn(__fmul_rn(s.omb2, g), g));
+}
+
+// upd = step_size * (m / (sqrt(v)/sbc2 + eps)) + lrwd * p
+__device__ __forceinline__ float update_of(const StepScalars& s, float m, float v,
+                                          float p0) {
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sbc2), s.eps);
+    return __fadd_rn(__fmul_rn(s.step_size, __fdiv_rn(m, den)), __fmul_rn(s.lrwd, p0));
+}
+
+// bf16 Kahan mode on two elements packed in 32-bit words (lo, hi halves).
+template <int K>
+__device__ __forceinline__ void kahan_x2(const StepScalars& s, float coef, uint32_t gw,
+                                         uint32_t& pw, uint32_t& mw, uint32_t& vw,
+                                         uint32_t& cw) {
+    float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+    if (K == kClip) {
+        g0 = __fmul_rn(g0, coef);
+        g1 = __fmul_rn(g1, coef);
+    }
+    const float p0 = bf16_lo(pw), p1 = bf16_hi(pw);
+    float ma, mb, va, vb;
+    moments(s, g0, bf16_lo(mw), bf16_lo(vw), ma, va);
+    moments(s, g1, bf16_hi(mw), bf16_hi(vw), mb, vb);
+    mw = pack_bf16x2(ma, mb);
+    vw = pack_bf16x2(va, vb);
+    // the stored (bf16) moments feed the update
+    const float y0 = __fsub_rn(bf16_lo(cw), update_of(s, bf16_lo(mw), bf16_lo(vw), p0));
+    const float y1 = __fsub_rn(bf16_hi(cw), update_of(s, bf16_hi(mw), bf16_hi(vw), p1));
+    const uint32_t pn = pack_bf16x2(__fadd_rn(p0, y0), __fadd_rn(p1, y1));
+    cw = pack_bf16x2(__fsub_rn(y0, __fsub_rn(bf16_lo(pn), p0)),
+                     __fsub_rn(y1, __fsub_rn(bf16_hi(pn), p1)));
+    pw = pn;
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_x1(const StepScalars& s, float coef, uint16_t gh,
+                                         uint16_t& ph, uint16_t& mh, uint16_t& vh,
+                                         uint16_t& ch) {
+    float g = from_bf16(gh);
+    if (K == kClip) g = __fmul_rn(g, coef);
+    const float p0 = from_bf16(ph);
+    float m1, v1;
+    moments(s, g, from_bf16(mh), from_bf16(vh), m1, v1);
+    mh = to_bf16(m1);
+    vh = to_bf16(v1);
+    const float y = __fsub_rn(from_bf16(ch), update_of(s, from_bf16(mh), from_bf16(vh), p0));
+    const uint16_t pn = to_bf16(__fadd_rn(p0, y));
+    ch = to_bf16(__fsub_rn(y, __fsub_rn(from_bf16(pn), p0)));
+    ph = pn;
+}
+
+// mixed mode on one element; returns the new master.
+template <int K>
+__device__ __forceinline__ float mixed_x1(const StepScalars& s, float coef, float g,
+                                          float p0, float& m, float& v) {
+    if (K == kClip) g = __fmul_rn(g, coef);
+    float m1, v1;
+    moments(s, g, m, v, m1, v1);
+    m = m1;
+    v = v1;
+    return __fsub_rn(p0, update_of(s, m1, v1, p0));
+}
+
+// ------------------------------------------------------- chunk walkers ----
+
+// Vectors per thread in flight per stream, and the CTAs per SM the update
+// kernel's register budget is fitted to (0: no constraint).
+#ifndef ADAMW_UNROLL
+#define ADAMW_UNROLL 2
+#endif
+#ifndef ADAMW_MIN_BLOCKS
+#define ADAMW_MIN_BLOCKS 0
+#endif
+constexpr int kUnroll = ADAMW_UNROLL;
+
+template <int K>
+__device__ __forceinline__ void kahan_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll], C[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld16(v + i * kVec);
+                C[u] = ld16(c + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(G[u].x) | bf16x2_nonfinite(G[u].y) |
+                           bf16x2_nonfinite(G[u].z) | bf16x2_nonfinite(G[u].w);
+                kahan_x2<K>(s, coef, G[u].x, P[u].x, M[u].x, V[u].x, C[u].x);
+                kahan_x2<K>(s, coef, G[u].y, P[u].y, M[u].y, V[u].y, C[u].y);
+                kahan_x2<K>(s, coef, G[u].z, P[u].z, M[u].z, V[u].z, C[u].z);
+                kahan_x2<K>(s, coef, G[u].w, P[u].w, M[u].w, V[u].w, C[u].w);
+                st16(p + i * kVec, P[u]);
+                st16(m + i * kVec, M[u]);
+                st16(v + i * kVec, V[u]);
+                st16(c + i * kVec, C[u]);
+            }
+        }
+    }
+    // ragged end of a vector body (< kVec elements)
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i], ch = c[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        kahan_x1<K>(s, coef, gh, ph, mh, vh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vh; c[i] = ch;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i], ch = c[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        kahan_x1<K>(s, coef, gh, ph, mh, vh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vh; c[i] = ch;
+    }
+}
+
+// 8 fp32 of a mixed-mode stream = two 16-byte accesses.
+struct F8 { float x[8]; };
+__device__ __forceinline__ F8 ld32(const float* p) {
+    const uint4 a = ld16(p), b = ld16(p + 4);
+    return {{__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w),
+             __uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w)}};
+}
+__device__ __forceinline__ void st32(float* p, const F8& v) {
+    st16(p, make_uint4(__float_as_uint(v.x[0]), __float_as_uint(v.x[1]),
+                       __float_as_uint(v.x[2]), __float_as_uint(v.x[3])));
+    st16(p + 4, make_uint4(__float_as_uint(v.x[4]), __float_as_uint(v.x[5]),
+                           __float_as_uint(v.x[6]), __float_as_uint(v.x[7])));
+}
+
+template <int K>
+__device__ __forceinline__ void mixed_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* o = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll];
+        F8 P[kUnroll], M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld32(p + i * kVec);
+                M[u] = ld32(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t out[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int a = 2 * j, b = 2 * j + 1;
+                    P[u].x[a] = mixed_x1<K>(s, coef, bf16_lo(gw[j]), P[u].x[a], M[u].x[a], V[u].x[a]);
+                    P[u].x[b] = mixed_x1<K>(s, coef, bf16_hi(gw[j]), P[u].x[b], M[u].x[b], V[u].x[b]);
+                    out[j] = pack_bf16x2(P[u].x[a], P[u].x[b]);
+                }
+                st32(p + i * kVec, P[u]);
+                st32(m + i * kVec, M[u]);
+                st32(v + i * kVec, V[u]);
+                st16(o + i * kVec, make_uint4(out[0], out[1], out[2], out[3]));
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), p[i], mi, vi);
+        p[i] = n; m[i] = mi; v[i] = vi; o[i] = to_bf16(n);
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void mixed_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    float* p = static_cast<float*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* o = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), p[i], mi, vi);
+        p[i] = n; m[i] = mi; v[i] = vi; o[i] = to_bf16(n);
+    }
+}
+
+// bf16 without compensation, two elements per 32-bit word: p' = bf16(p - upd).
+template <int K>
+__device__ __forceinline__ void plain_x2(const StepScalars& s, float coef, uint32_t gw,
+                                         uint32_t& pw, uint32_t& mw, uint32_t& vw) {
+    float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+    if (K == kClip) {
+        g0 = __fmul_rn(g0, coef);
+        g1 = __fmul_rn(g1, coef);
+    }
+    const float p0 = bf16_lo(pw), p1 = bf16_hi(pw);
+    float ma, mb, va, vb;
+    moments(s, g0, bf16_lo(mw), bf16_lo(vw), ma, va);
+    moments(s, g1, bf16_hi(mw), bf16_hi(vw), mb, vb);
+    mw = pack_bf16x2(ma, mb);
+    vw = pack_bf16x2(va, vb);
+    pw = pack_bf16x2(__fsub_rn(p0, update_of(s, bf16_lo(mw), bf16_lo(vw), p0)),
+                     __fsub_rn(p1, update_of(s, bf16_hi(mw), bf16_hi(vw), p1)));
+}
+
+template <int K>
+__device__ __forceinline__ void plain_x1(const StepScalars& s, float coef, uint16_t gh,
+                                         uint16_t& ph, uint16_t& mh, uint16_t& vh) {
+    float g = from_bf16(gh);
+    if (K == kClip) g = __fmul_rn(g, coef);
+    const float p0 = from_bf16(ph);
+    float m1, v1;
+    moments(s, g, from_bf16(mh), from_bf16(vh), m1, v1);
+    mh = to_bf16(m1);
+    vh = to_bf16(v1);
+    ph = to_bf16(__fsub_rn(p0, update_of(s, from_bf16(mh), from_bf16(vh), p0)));
+}
+
+// bf16 Kahan with fp32 variance, one element: v stays fp32.
+template <int K>
+__device__ __forceinline__ void kahan_v32_x1(const StepScalars& s, float coef, float g,
+                                             float p0, float m0, float& v, float c0,
+                                             uint16_t& ph, uint16_t& mh, uint16_t& ch) {
+    if (K == kClip) g = __fmul_rn(g, coef);
+    float m1, v1;
+    moments(s, g, m0, v, m1, v1);
+    mh = to_bf16(m1);
+    v = v1;
+    const float y = __fsub_rn(c0, update_of(s, from_bf16(mh), v1, p0));
+    ph = to_bf16(__fadd_rn(p0, y));
+    ch = to_bf16(__fsub_rn(y, __fsub_rn(from_bf16(ph), p0)));
+}
+
+template <int K>
+__device__ __forceinline__ void plain_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld16(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(G[u].x) | bf16x2_nonfinite(G[u].y) |
+                           bf16x2_nonfinite(G[u].z) | bf16x2_nonfinite(G[u].w);
+                plain_x2<K>(s, coef, G[u].x, P[u].x, M[u].x, V[u].x);
+                plain_x2<K>(s, coef, G[u].y, P[u].y, M[u].y, V[u].y);
+                plain_x2<K>(s, coef, G[u].z, P[u].z, M[u].z, V[u].z);
+                plain_x2<K>(s, coef, G[u].w, P[u].w, M[u].w, V[u].w);
+                st16(p + i * kVec, P[u]);
+                st16(m + i * kVec, M[u]);
+                st16(v + i * kVec, V[u]);
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        plain_x1<K>(s, coef, gh, ph, mh, vh);
+        p[i] = ph; m[i] = mh; v[i] = vh;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void plain_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                 const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    uint16_t* v = static_cast<uint16_t*>(t.v);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        uint16_t gh = g[i], ph = p[i], mh = m[i], vh = v[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        plain_x1<K>(s, coef, gh, ph, mh, vh);
+        p[i] = ph; m[i] = mh; v[i] = vh;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_v32_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                    const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], M[kUnroll], C[kUnroll];
+        F8 V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u] = ld16(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+                C[u] = ld16(c + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                const uint32_t pw[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
+                const uint32_t mw[4] = {M[u].x, M[u].y, M[u].z, M[u].w};
+                const uint32_t cw[4] = {C[u].x, C[u].y, C[u].z, C[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t po[4], mo[4], co[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint16_t ph0, mh0, ch0, ph1, mh1, ch1;
+                    kahan_v32_x1<K>(s, coef, bf16_lo(gw[j]), bf16_lo(pw[j]), bf16_lo(mw[j]),
+                                    V[u].x[2 * j], bf16_lo(cw[j]), ph0, mh0, ch0);
+                    kahan_v32_x1<K>(s, coef, bf16_hi(gw[j]), bf16_hi(pw[j]), bf16_hi(mw[j]),
+                                    V[u].x[2 * j + 1], bf16_hi(cw[j]), ph1, mh1, ch1);
+                    po[j] = uint32_t(ph0) | (uint32_t(ph1) << 16);
+                    mo[j] = uint32_t(mh0) | (uint32_t(mh1) << 16);
+                    co[j] = uint32_t(ch0) | (uint32_t(ch1) << 16);
+                }
+                st16(p + i * kVec, make_uint4(po[0], po[1], po[2], po[3]));
+                st16(m + i * kVec, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+                st32(v + i * kVec, V[u]);
+                st16(c + i * kVec, make_uint4(co[0], co[1], co[2], co[3]));
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float vi = v[i];
+        uint16_t ph, mh, ch;
+        kahan_v32_x1<K>(s, coef, from_bf16(gh), from_bf16(p[i]), from_bf16(m[i]), vi,
+                        from_bf16(c[i]), ph, mh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vi; c[i] = ch;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void kahan_v32_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                     const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    uint16_t* m = static_cast<uint16_t*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* c = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float vi = v[i];
+        uint16_t ph, mh, ch;
+        kahan_v32_x1<K>(s, coef, from_bf16(gh), from_bf16(p[i]), from_bf16(m[i]), vi,
+                        from_bf16(c[i]), ph, mh, ch);
+        p[i] = ph; m[i] = mh; v[i] = vi; c[i] = ch;
+    }
+}
+
+// Remainder mode: the fp32 master is the bf16 parameter (high half) plus a
+// signed 16-bit remainder of the bit pattern.
+__device__ __forceinline__ float join_master(uint32_t hi_bits, uint32_t rem16) {
+    return __uint_as_float(hi_bits + uint32_t(int32_t(int16_t(uint16_t(rem16)))));
+}
+// Nearest bf16 high half (ties away from zero) and the remainder restoring it.
+__device__ __forceinline__ void split_master(float x, uint32_t& hi16, uint32_t& rem16) {
+    const uint32_t u = __float_as_uint(x);
+    hi16 = (u + 0x8000u) >> 16;
+    rem16 = (u - (hi16 << 16)) & 0xffffu;
+}
+
+template <int K>
+__device__ __forceinline__ void remainder_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                    const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* r = static_cast<uint16_t*>(t.a);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll], R[kUnroll];
+        F8 M[kUnroll], V[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                R[u] = ld16(r + i * kVec);
+                M[u] = ld32(m + i * kVec);
+                V[u] = ld32(v + i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                const uint32_t pw[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
+                const uint32_t rw[4] = {R[u].x, R[u].y, R[u].z, R[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t po[4], ro[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int a = 2 * j, b = 2 * j + 1;
+                    const float n0 = mixed_x1<K>(s, coef, bf16_lo(gw[j]),
+                                                 join_master(pw[j] << 16, rw[j]), M[u].x[a], V[u].x[a]);
+                    const float n1 = mixed_x1<K>(s, coef, bf16_hi(gw[j]),
+                                                 join_master(pw[j] & 0xffff0000u, rw[j] >> 16),
+                                                 M[u].x[b], V[u].x[b]);
+                    uint32_t h0, r0, h1, r1;
+                    split_master(n0, h0, r0);
+                    split_master(n1, h1, r1);
+                    po[j] = h0 | (h1 << 16);
+                    ro[j] = r0 | (r1 << 16);
+                }
+                st16(p + i * kVec, make_uint4(po[0], po[1], po[2], po[3]));
+                st16(r + i * kVec, make_uint4(ro[0], ro[1], ro[2], ro[3]));
+                st32(m + i * kVec, M[u]);
+                st32(v + i * kVec, V[u]);
+            }
+        }
+    }
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) {
+        const int64_t i = nvec * kVec + threadIdx.x;
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), join_master(uint32_t(p[i]) << 16, r[i]),
+                                    mi, vi);
+        uint32_t h, rr;
+        split_master(n, h, rr);
+        p[i] = uint16_t(h); r[i] = uint16_t(rr); m[i] = mi; v[i] = vi;
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                     const StepScalars& s, float coef, bool& bad) {
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    float* m = static_cast<float*>(t.m);
+    float* v = static_cast<float*>(t.v);
+    uint16_t* r = static_cast<uint16_t*>(t.a);
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) {
+        const uint16_t gh = g[i];
+        if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+        float mi = m[i], vi = v[i];
+        const float n = mixed_x1<K>(s, coef, from_bf16(gh), join_master(uint32_t(p[i]) << 16, r[i]),
+                                    mi, vi);
+        uint32_t h, rr;
+        split_master(n, h, rr);
+        p[i] = uint16_t(h); r[i] = uint16_t(rr); m[i] = mi; v[i] = vi;
+    }
+}
+
+// The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
+#if ADAMW_MIN_BLOCKS > 0
+#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock, ADAMW_MIN_BLOCKS)
+#else
+#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock)
+#endif
+
+// One chunk descriptor, read through the read-only path.
+__device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
+    const ulonglong2* q = reinterpret_cast<const ulonglong2*>(c);
+    const ulonglong2 a = __ldg(q), b = __ldg(q + 1), d = __ldg(q + 2);
+    ChunkPtr r;
+    r.p = reinterpret_cast<void*>(a.x);
+    r.g = reinterpret_cast<const void*>(a.y);
+    r.m = reinterpret_cast<void*>(b.x);
+    r.v = reinterpret_cast<void*>(b.y);
+    r.a = reinterpret_cast<void*>(d.x);
+    r.len2 = static_cast<int64_t>(d.y);
+    return r;
+}
+
+// ---- the CTA's share of the update: chunks [c0, c1), each chunk's
+// descriptor fetched one ahead.
+template <int MODE, int K>
+__device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                           int32_t c1, const StepScalars& s, float coef,
+                                           bool& bad) {
+    ChunkPtr cur;
+    if (c0 < c1) cur = load_chunk(chunks + c0);
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        ChunkPtr nxt = cur;
+        if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
+        const int64_t len = cur.len2 >> 1;
+        const bool vec = cur.len2 & 1;
+        if (MODE == ADAMW_MODE_BF16_KAHAN) {
+            if (vec) kahan_vec_chunk<K>(cur, len, s, coef, bad);
+            else kahan_elem_chunk<K>(cur, len, s, coef, bad);
+        } else if (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
+            if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
+            else mixed_elem_chunk<K>(cur, len, s, coef, bad);
+        } else if (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
+            if (vec) remainder_vec_chunk<K>(cur, len, s, coef, bad);
+            else remainder_elem_chunk<K>(cur, len, s, coef, bad);
+        } else if (MODE == ADAMW_MODE_BF16_PLAIN) {
+            if (vec) plain_vec_chunk<K>(cur, len, s, coef, bad);
+            else plain_elem_chunk<K>(cur, len, s, coef, bad);
+        } else {
+            if (vec) kahan_v32_vec_chunk<K>(cur, len, s, coef, bad);
+            else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
+        }
+        cur = nxt;
+    }
+}
+
+// Error-free fp32 accumulation of non-negative terms: s + e is the exact sum
+// of everything added since the last flush, up to the rounding of e itself.
+// Squares of bf16 values are exact in fp32 for |g| in [2^-63, 2^64); for
+// a >= b >= 0 the rounding error of a + b is exactly b - ((a + b) - a)
+// (Dekker's Fast2Sum), so no bit of any square is lost; e collects those
+// errors.  A group of at most 64 terms is flushed: s into an fp64 sum, e
+// (at most 2^-18 of s) into an fp32 sum of the errors.
+struct Sum2F32 {
+    float s = 0.0f, e = 0.0f;
+    __device__ __forceinline__ void add(float x) {
+        const float a = fmaxf(s, x), b = fminf(s, x);
+        const float t = __fadd_rn(a, b);
+        e = __fadd_rn(e, __fsub_rn(b, __fsub_rn(t, a)));
+        s = t;
+    }
+    // Adds the group to (acc, err) and restarts it; false when the group left
+    // the range where squares are exact and sums finite.
+    __device__ __forceinline__ bool flush(double& acc, float& err) {
+        const bool ok = s < 0x1p100f;   // also false for inf and NaN
+        acc += double(s);
+        err = __fadd_rn(err, e);
+        s = 0.0f;
+        e = 0.0f;
+        return ok;
+    }
+};
+
+__device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
+
+// Walks the g elements of one CTA's chunks that belong to this thread, in a
+// fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
+// after every group of U vectors.
+template <int U, typename FV, typename FE, typename FI>
+__device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ chunks,
+                                                 int32_t c0, int32_t c1, FV vec, FE elem,
+                                                 FI after_iter) {
+    for (int32_t ci = c0; ci < c1; ++ci) {
+        const ChunkPtr ch = load_chunk(chunks + ci);
+        const uint16_t* g = static_cast<const uint16_t*>(ch.g);
+        const int64_t len = ch.len2 >> 1;
+        int64_t done = 0;
+        if (ch.len2 & 1) {
+            const int64_t nvec = len / kVec;
+            for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+                uint4 w[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t i = base + int64_t(u) * kBlock;
+                    if (i < nvec) w[u] = ld16(g + i * kVec);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (base + int64_t(u) * kBlock < nvec) vec(w[u]);
+                after_iter();
+            }
+            done = nvec * kVec;
+        }
+        for (int64_t i = done + threadIdx.x; i < len; i += kBlock) elem(g[i]);
+    }
+}
+
+// Deterministic fixed-tree reduction of one fp64 per thread to thread 0.
+__device__ __forceinline__ double block_sum(double x) {
+    __shared__ double warp_part[kBlock / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+    const int lane_id = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
+    if (lane_id == 0) warp_part[warp_id] = x;
+    __syncthreads();
+    double r = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kBlock / 32; ++w) r += warp_part[w];
+    __syncthreads();
+    return r;
+}
+
+// Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
+// same partition as the update (so the result depends only on the plan).
+// Fast path: error-free fp32 group sums of the exact squares, flushed every
+// 64 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
+// inf or NaN gradients) recomputes its elements in fp64, which also decides
+// the non-finite flag.
+// The CTA's partial sum of squares and non-finite flag, written to
+// partial[blockIdx.x] and flag[blockIdx.x].
+__device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                                 int32_t c1, double* __restrict__ partial,
+                                                 int32_t* __restrict__ flag) {
+    Sum2F32 grp;
+    double acc = 0.0;
+    float err = 0.0f;
+    bool in_range = true;
+    uint32_t nz = 0;
+    for_thread_grads<8>(
+        chunks, c0, c1,
+        [&](const uint4& w) {
+            nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
+            grp.add(sq(bf16_lo(w.x)));
+            grp.add(sq(bf16_hi(w.x)));
+            grp.add(sq(bf16_lo(w.y)));
+            grp.add(sq(bf16_hi(w.y)));
+            grp.add(sq(bf16_lo(w.z)));
+            grp.add(sq(bf16_hi(w.z)));
+            grp.add(sq(bf16_lo(w.w)));
+            grp.add(sq(bf16_hi(w.w)));
+        },
+        [&](uint16_t h) {
+            nz |= h & 0x7fffu;
+            grp.add(sq(from_bf16(h)));
+            in_range &= grp.flush(acc, err);
+        },
+        [&]() { in_range &= grp.flush(acc, err); });
+    in_range &= grp.flush(acc, err);
+    double tot = acc + double(err);
+    bool bad = false;
+    if (!in_range || (nz != 0 && tot < 0x1p-100)) {
+        double exact = 0.0;
+        for_thread_grads<1>(
+            chunks, c0, c1,
+            [&](const uint4& w) {
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
+                    bad |= !isfinite(lo) || !isfinite(hi);
+                    exact += lo * lo;
+                    exact += hi * hi;
+                }
+            },
+            [&](uint16_t h) {
+                const double x = from_bf16(h);
+                bad |= !isfinite(x);
+                exact += x * x;
+            },
+            [&]() {});
+        tot = exact;
+    }
+    tot = block_sum(tot);
+    const int any = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        partial[blockIdx.x] = tot;
+        flag[blockIdx.x] = any;
+    }
+}
+
+// ---- device-resident step path ----
+
+// beta^t by binary exponentiation, lowest bit of t first, one IEEE fp64
+// rounding per multiplication: the same operations as the host planner's.
+__device__ double beta_power_dev(double beta, int64_t t) {
+    double result = 1.0, square = beta;
+    for (; t > 0; t >>= 1) {
+        if (t & 1) result = __dmul_rn(result, square);
+        square = __dmul_rn(square, square);
+    }
+    return result;
+}
+
+__device__ bool hparams_valid_dev(const adamw_hparams_t& hp) {
+    const float f[6] = {hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm};
+    for (float x : f)
+        if (!isfinite(x)) return false;
+    return hp.lr >= 0.0f && hp.eps > 0.0f && hp.weight_decay >= 0.0f && hp.beta1 >= 0.0f &&
+           hp.beta1 < 1.0f && hp.beta2 >= 0.0f && hp.beta2 < 1.0f;
+}
+
+// The host planner's make_scalars, operation for operation.
+__device__ void make_scalars_dev(const adamw_hparams_t& hp, int64_t t, StepScalars* out) {
+    const double b1 = hp.beta1, b2 = hp.beta2;
+    const double bc1 = __dsub_rn(1.0, beta_power_dev(b1, t));
+    const double bc2 = __dsub_rn(1.0, beta_power_dev(b2, t));
+    out->beta1 = hp.beta1;
+    out->beta2 = hp.beta2;
+    out->omb1 = __double2float_rn(__dsub_rn(1.0, b1));
+    out->omb2 = __double2float_rn(__dsub_rn(1.0, b2));
+    out->step_size = __double2float_rn(__ddiv_rn(double(hp.lr), bc1));
+    out->sbc2 = __double2float_rn(__dsqrt_rn(bc2));
+    out->eps = hp.eps;
+    out->lrwd = __double2float_rn(__dmul_rn(double(hp.lr), double(hp.weight_decay)));
+    out->max_grad_norm = hp.max_grad_norm;
+}
+
+// ---- fused clipped step (one cooperative launch) ----
+//
+// For lists whose gradients fit in L2: stage 1 of the norm, a grid barrier,
+// then every CTA sums all partials itself in the fixed order (no second
+// barrier), decides clip or skip, and updates its share -- the second read
+// of g comes from L2.  Needs every CTA resident at once (cooperative launch).
+// The barrier is a monotonic 64-bit arrival counter: the CTA whose ticket is
+// t waits until the counter reaches the next multiple of the grid.  The wait
+// is bounded: a CTA that gives up sets *status and returns without updating.
+constexpr uint32_t kBarrierSpins = 1u << 21;   // about a second with the sleeps
+
+__device__ __forceinline__ unsigned long long load_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+}  // namespace

@@ -1,0 +1,79 @@
+// launch.h -- the plan object and the per-storage-mode launchers.
+//
+// Each storage mode's update kernels are instantiated in a translation unit of
+// their own (update_m0.cu .. update_m4.cu, all from update_mode.inc), so the
+// five modes compile in parallel; adamw_sm.cu reaches them through the table
+// of launchers that mode_ops<MODE>() returns.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "adamw_internal.h"
+#include "adamw_sm.h"
+
+// One partition of the plan's list on the device: the chunk descriptors of
+// `grid` CTAs and where each CTA's run of chunks begins.
+struct DevPartition {
+    int32_t grid = 0;
+    int64_t n_chunks = 0;
+    adamw::ChunkPtr* chunks = nullptr;
+    int32_t* cta_begin = nullptr;
+};
+
+struct adamw_plan {
+    int device = 0;
+    int32_t mode = 0;
+    int32_t flags = 0;
+    int32_t n_tensors = 0;
+    int64_t total = 0;
+    int64_t scalar_elems = 0;
+    void* block = nullptr;  // one device allocation holding everything below
+    adamw::TensorDev* tensors = nullptr;  // the uploaded tensor table
+    DevPartition upd;                     // update kernel
+    DevPartition nrm;                     // norm partial kernel (its own grid)
+    double* partial = nullptr;
+    int32_t* flag = nullptr;
+    adamw::NormOut* norm = nullptr;
+    adamw::StepRecord* rec = nullptr;  // device-resident step path
+    int32_t* status = nullptr;         // set by a kernel whose bounded wait ran out
+    bool fused = false;                // clipped steps run as one cooperative launch
+    unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
+    unsigned int* done = nullptr;  // finished CTAs of a one-launch device step
+    int32_t* flagword = nullptr;   // its non-finite flag, collected across CTAs
+};
+
+namespace adamw {
+
+// The launchers of one storage mode.  Every pointer is set.
+struct ModeOps {
+    // Resident CTAs per SM of the update kernel for each Kind (occ[Kind]) and
+    // of the fused clipped kernel.  Also sets any kernel attribute a launch
+    // needs, so it runs once per device before the first plan.
+    cudaError_t (*occupancy)(int occ[3], int* occ_fused);
+    // The update over the plan's partition.  dev: the scalars come from the
+    // plan's device-side step record (written by the step prologue) instead
+    // of `s`.  `report` receives the non-finite flag when kind == kReport.
+    cudaError_t (*update)(const adamw_plan* P, int kind, bool dev, const StepScalars& s,
+                          int32_t* report, cudaStream_t st);
+    // The one-launch device-resident step (no norm): kind is kPlain or
+    // kReport (then user_flag receives the non-finite flag).
+    cudaError_t (*self)(const adamw_plan* P, int kind, const adamw_hparams_t* d_hp,
+                        int64_t* d_step, int32_t* user_flag, cudaStream_t st);
+    // The fused clipped step: norm, grid barrier and update in one
+    // cooperative launch over the update grid.
+    cudaError_t (*fused)(const adamw_plan* P, const StepScalars& s, double* user_norm,
+                         int32_t* user_flag, cudaStream_t st);
+};
+
+// mode_ops<MODE>() is defined in update_m<MODE>.cu.
+template <int MODE>
+const ModeOps& mode_ops();
+template <> const ModeOps& mode_ops<0>();
+template <> const ModeOps& mode_ops<1>();
+template <> const ModeOps& mode_ops<2>();
+template <> const ModeOps& mode_ops<3>();
+template <> const ModeOps& mode_ops<4>();
+
+}  // namespace adamw

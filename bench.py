@@ -62,7 +62,9 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = ("adamw_sm.cu", "adamw_internal.h")
+KERNEL_SOURCES = ("adamw_internal.h", "device_common.cuh", "kernels.cuh", "launch.h",
+                  "update_mode.inc", "update_m0.cu", "update_m1.cu", "update_m2.cu",
+                  "update_m3.cu", "update_m4.cu")
 
 
 def kernel_source_hash() -> str:
