@@ -90,6 +90,9 @@ class Oracle:
         L.oracle_adamw_mixed.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_remainder.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
         L.oracle_adamw_bf16_kahan_v32.argtypes = [vp, vp, vp, vp, vp, i64, hp, i64, f32]
+        L.oracle_adamw_anyprec.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.c_int32, hp, i64,
+                                           f32]
+        L.oracle_adamw_anyprec.restype = ctypes.c_int32
         L.oracle_lr_linear_warmup.argtypes = [f32, i64, i64, i64]
         L.oracle_lr_linear_warmup.restype = f32
         L.oracle_split_master.argtypes = [vp, vp, vp, i64]
@@ -161,6 +164,22 @@ class Oracle:
         self.lib.oracle_adamw_bf16_kahan_v32(_ptr(p), _ptr(g), _ptr(m), _ptr(v), _ptr(c), n,
                                              ctypes.byref(hp), t, coef)
 
+    def anyprec(self, p, g, m, v, c, flags: int, hp: Hparams, t: int, coef: float = 1.0):
+        """AnyPrecisionAdamW step; ``flags`` as oracle_adamw_anyprec (1: fp32
+        exp_avg, 2: fp32 exp_avg_sq, 4: fp32 compensation, 8: no Kahan, c is
+        then None)."""
+        n = p.size
+        dm, dv, dc = anyprec_dtypes(flags)
+        for a, dt in ((p, np.uint16), (g, np.uint16), (m, dm), (v, dv)):
+            _check(a, dt, n)
+        if dc is not None:
+            _check(c, dc, n)
+        rc = self.lib.oracle_adamw_anyprec(_ptr(p), _ptr(g), _ptr(m), _ptr(v),
+                                           _ptr(c) if dc is not None else None, n, flags,
+                                           ctypes.byref(hp), t, coef)
+        if rc != 0:
+            raise ValueError(f"invalid any-precision flags {flags}")
+
     def lr_linear_warmup(self, base_lr: float, t: int, warmup: int, total: int) -> float:
         return float(np.float32(self.lib.oracle_lr_linear_warmup(base_lr, t, warmup, total)))
 
@@ -200,8 +219,11 @@ class Oracle:
         arrays.  Returns (skipped: bool, norm: float)."""
         arr = (TensorEntry * max(1, len(tensors)))()
         u16, f32, i16 = np.uint16, np.float32, np.int16
-        want = {0: (u16, u16, u16, u16), 1: (f32, f32, f32, u16), 2: (u16, f32, f32, i16),
-                3: (u16, u16, u16, None), 4: (u16, u16, f32, u16)}[mode]
+        if mode >= ANYPREC:
+            want = (u16, *anyprec_dtypes(mode - ANYPREC))
+        else:
+            want = {0: (u16, u16, u16, u16), 1: (f32, f32, f32, u16), 2: (u16, f32, f32, i16),
+                    3: (u16, u16, u16, None), 4: (u16, u16, f32, u16)}[mode]
         for k, (p, g, m, v, a) in enumerate(tensors):
             n = g.size
             _check(p, want[0], n); _check(g, np.uint16, n); _check(m, want[1], n)
@@ -214,7 +236,23 @@ class Oracle:
         rc = self.lib.oracle_adamw_list_step(arr, len(tensors), mode,
                                              ctypes.byref(hp), t,
                                              ctypes.byref(norm))
+        if rc < 0:
+            raise ValueError(f"unknown mode {mode}")
         return bool(rc), norm.value
+
+
+# Mode numbers of the any-precision step: ANYPREC + flags.
+ANYPREC = 16
+
+
+def anyprec_dtypes(flags: int):
+    """Storage types of exp_avg, exp_avg_sq and the compensation (None without
+    Kahan summation) for any-precision flags."""
+    if flags & ~15 or (flags & 12) == 12:
+        raise ValueError(f"invalid any-precision flags {flags}")
+    f32, u16 = np.float32, np.uint16
+    return (f32 if flags & 1 else u16, f32 if flags & 2 else u16,
+            None if flags & 8 else (f32 if flags & 4 else u16))
 
 
 def load(path: str | None = None) -> Oracle:

@@ -50,6 +50,9 @@
  *
  *   bf16 without compensation (use_kahan_summation=false): p' = bf16(p - upd)
  *   bf16 Kahan with fp32 variance (variance_dtype=float32): v' kept in fp32
+ *   any precision (momentum_dtype, variance_dtype, compensation_buffer_dtype
+ *   each bfloat16 or float32, Kahan on or off): the same step, each buffer
+ *   rounded to its own type when stored and used as stored
  *
  *   remainder mode (the same update; the fp32 master is stored as the bf16
  *   parameter plus a 16-bit remainder, 10 B/param of optimizer state: "2 FP32
@@ -264,6 +267,74 @@ void oracle_adamw_bf16_kahan_v32(uint16_t* p, const uint16_t* g, uint16_t* m,
     }
 }
 
+/* AnyPrecisionAdamW with a bf16 parameter and gradient and a storage type
+ * chosen per optimizer buffer -- the run recipe's optim_args
+ * momentum_dtype, variance_dtype, compensation_buffer_dtype (bfloat16 or
+ * float32 each) and use_kahan_summation ("[pure bf16 training] w/
+ * AnyPrecisionAdamW and Kahan summation", "Train from scratch").
+ *
+ * flags: 1 = exp_avg is fp32, 2 = exp_avg_sq is fp32, 4 = compensation is
+ * fp32, 8 = no Kahan summation (no compensation buffer; flag 4 then invalid).
+ * A bf16 buffer holds bf16 bits (uint16_t), an fp32 buffer floats.  Each
+ * buffer is rounded to its own type when stored, and the value stored is the
+ * value the rest of the step uses.  Flags 0, 2 and 8 are the bf16 Kahan, bf16
+ * Kahan with fp32 variance and bf16 without compensation steps above.
+ * Returns -1 (and writes nothing) for flag 4 together with flag 8. */
+static float load_any(const void* buf, int fp32, int64_t i)
+{
+    return fp32 ? ((const float*)buf)[i]
+                : bf16_bits_to_f32(((const uint16_t*)buf)[i]);
+}
+
+/* Stores x in the buffer's type; returns the value stored. */
+static float store_any(void* buf, int fp32, int64_t i, float x)
+{
+    if (fp32) {
+        ((float*)buf)[i] = x;
+        return x;
+    }
+    uint16_t h = f32_to_bf16_rne(x);
+    ((uint16_t*)buf)[i] = h;
+    return bf16_bits_to_f32(h);
+}
+
+int32_t oracle_adamw_anyprec(uint16_t* p, const uint16_t* g, void* m, void* v,
+                             void* c, int64_t n, int32_t flags,
+                             const oracle_hparams_t* hp, int64_t t, float coef)
+{
+    const int m32 = (flags & 1) != 0, v32 = (flags & 2) != 0;
+    const int c32 = (flags & 4) != 0, kahan = (flags & 8) == 0;
+    if ((flags & ~15) || (!kahan && c32)) return -1;
+    step_scalars_t s = make_scalars(hp, t);
+    const float b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps;
+    const int clip = hp->max_grad_norm > 0.0f;
+
+    for (int64_t i = 0; i < n; ++i) {
+        float gi = bf16_bits_to_f32(g[i]);
+        if (clip) gi = gi * coef;
+        float p0 = bf16_bits_to_f32(p[i]);
+
+        float m1 = (b1 * load_any(m, m32, i)) + (s.omb1 * gi);
+        float v1 = (b2 * load_any(v, v32, i)) + ((s.omb2 * gi) * gi);
+        float ms = store_any(m, m32, i, m1);
+        float vs = store_any(v, v32, i, v1);
+
+        float den = (sqrtf(vs) / s.sbc2) + eps;
+        float upd = (s.step_size * (ms / den)) + (s.lrwd * p0);
+
+        if (kahan) {
+            float y = load_any(c, c32, i) - upd;
+            uint16_t pnh = f32_to_bf16_rne(p0 + y);
+            float pn = bf16_bits_to_f32(pnh);
+            store_any(c, c32, i, y - (pn - p0));
+            p[i] = pnh;
+        } else {
+            p[i] = f32_to_bf16_rne(p0 - upd);
+        }
+    }
+    return 0;
+}
+
 /* ----------------------------------------------------- learning rate -- */
 
 /* The recipe's --lr_scheduler_type linear --warmup_steps W for T training
@@ -430,15 +501,19 @@ typedef struct {
 
 /* The whole optimizer step over a tensor list (host buffers), mode 0 = bf16
  * Kahan, 1 = mixed, 2 = remainder, 3 = bf16 without compensation (aux
- * unused), 4 = bf16 Kahan with fp32 variance.  With clipping, the norm is taken first over every
+ * unused), 4 = bf16 Kahan with fp32 variance, 16 + flags = the
+ * any-precision step of oracle_adamw_anyprec (aux = compensation).  With clipping, the norm is taken first over every
  * tensor; a non-finite gradient anywhere makes the call write nothing and
- * return 1 (the caller must not advance t).  Returns 0 after an applied step.
+ * return 1 (the caller must not advance t).  Returns 0 after an applied step,
+ * -1 for an unknown mode.
  * norm_out (nullable) receives the fp64 norm when clipping. */
 int32_t oracle_adamw_list_step(const oracle_tensor_t* list, int32_t n_tensors,
                                int32_t mode, const oracle_hparams_t* hp,
                                int64_t t, double* norm_out)
 {
     float coef = 1.0f;
+    const int anyprec_ok = mode >= 16 && mode < 32 && (mode & 12) != 12;
+    if (!(mode >= 0 && mode <= 4) && !anyprec_ok) return -1;
     if (hp->max_grad_norm > 0.0f) {
         double acc[2] = {0.0, 0.0};
         int32_t bad = 0;
@@ -464,6 +539,10 @@ int32_t oracle_adamw_list_step(const oracle_tensor_t* list, int32_t n_tensors,
             oracle_adamw_bf16_plain((uint16_t*)e->param, (const uint16_t*)e->grad,
                                     (uint16_t*)e->exp_avg, (uint16_t*)e->exp_avg_sq,
                                     e->numel, hp, t, coef);
+        else if (mode >= 16)
+            oracle_adamw_anyprec((uint16_t*)e->param, (const uint16_t*)e->grad,
+                                 e->exp_avg, e->exp_avg_sq, e->aux, e->numel,
+                                 mode - 16, hp, t, coef);
         else if (mode == 4)
             oracle_adamw_bf16_kahan_v32((uint16_t*)e->param, (const uint16_t*)e->grad,
                                         (uint16_t*)e->exp_avg, (float*)e->exp_avg_sq,

@@ -536,7 +536,165 @@ def pin_remainder_equals_mixed_master(o: O.Oracle, steps: int = 12):
     assert np.all(np.abs(bf16_to_f64(p16) - joined) <= 0.5 * ulp_bf16(joined))
 
 
+# ---------------------------------------------- any-precision storage --
+
+# Every valid combination of the any-precision flags (1: fp32 exp_avg, 2: fp32
+# exp_avg_sq, 4: fp32 compensation, 8: no Kahan summation; 4 needs Kahan).
+ANY_FLAGS = [f for f in range(16) if (f & 12) != 12]
+
+
+# Half a bf16 ulp, with room for the fp64 evaluation of the expected value.
+HALF_ULP = 0.5 * (1.0 + 2.0 ** -10)
+
+
+def _anyprec_state(flags: int, ph: np.ndarray):
+    dm, dv, dc = O.anyprec_dtypes(flags)
+    n = ph.size
+    return (ph.copy(), np.zeros(n, dm), np.zeros(n, dv),
+            None if dc is None else np.zeros(n, dc))
+
+
+def _f64(a: np.ndarray) -> np.ndarray:
+    return bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def _anyprec_params(r, n: int) -> np.ndarray:
+    """Half of the elements in [0.5, 2) in magnitude, where updates of about
+    lr = 3e-3 are below half a bf16 ulp and only the compensation moves them;
+    half around N(0, 0.02), where every update moves the bf16 parameter."""
+    big = r.uniform(0.5, 2.0, n // 2) * r.choice([-1.0, 1.0], n // 2)
+    small = r.standard_normal(n - n // 2) * 0.02
+    return torch_bf16_bits(np.concatenate([big, small]).astype(F32))
+
+
+def pin_anyprec_matches_named_modes(o: O.Oracle, steps: int = 20):
+    """Flags 0, 2 and 8 store exactly what the all-bf16 Kahan step, the
+    fp32-variance Kahan step and the uncompensated step store (each pinned on
+    its own above), with and without a clip coefficient."""
+    r = _rng(21)
+    n = 257
+    ph = _anyprec_params(r, n)
+    grads = [torch_bf16_bits((r.standard_normal(n) * 1e-2).astype(F32)) for _ in range(steps)]
+    for coef, max_norm in ((1.0, 0.0), (0.37, 1.0)):
+        hp = O.hparams(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
+                       max_grad_norm=max_norm)
+        for flags in (0, 2, 8):
+            a = _anyprec_state(flags, ph)
+            b = _anyprec_state(flags, ph)
+            for t, gh in enumerate(grads, 1):
+                o.anyprec(a[0], gh, a[1], a[2], a[3], flags, hp, t, coef)
+                if flags == 0:
+                    o.bf16_kahan(b[0], gh, b[1], b[2], b[3], hp, t, coef)
+                elif flags == 2:
+                    o.bf16_kahan_v32(b[0], gh, b[1], b[2], b[3], hp, t, coef)
+                else:
+                    o.bf16_plain(b[0], gh, b[1], b[2], hp, t, coef)
+            for x, y in zip(a, b):
+                if x is not None:
+                    assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), \
+                        f"flags {flags} differ from the named mode"
+
+
+def pin_anyprec_step_definition(o: O.Oracle, steps: int = 40):
+    """Every combination, every step, against the textbook update in fp64
+    evaluated on the values the step stored:
+      m_t = b1 m_{t-1} + (1-b1) g,  v_t = b2 v_{t-1} + (1-b2) g^2
+      upd = lr/(1-b1^t) * m_t / (sqrt(v_t)/sqrt(1-b2^t) + eps) + lr wd p_{t-1}
+    Kahan: p_t + c_t = p_{t-1} + c_{t-1} - upd; otherwise p_t is the nearest
+    bf16 to p_{t-1} - upd.  Allowed error: the fp32 roundings of the step (a
+    few units of 2^-24 relative) plus half a bf16 ulp for each value stored
+    as bf16 (attained at ties, hence HALF_ULP a hair above 1/2, against a
+    full ulp for a wrong rounding) -- so a buffer stored in the wrong type, a
+    wrong sign or a dropped term fails."""
+    r = _rng(22)
+    n = 64
+    ph = _anyprec_params(r, n)
+    grads = []
+    for _ in range(steps):
+        g = r.standard_normal(n) * 1e-2
+        g[r.random(n) < 0.05] *= 100.0
+        grads.append(torch_bf16_bits(g.astype(F32)))
+    lr, b1, b2, eps, wd = f32(3e-3), f32(0.9), f32(0.95), f32(1e-8), f32(0.1)
+    hp = O.hparams(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    for flags in ANY_FLAGS:
+        p, m, v, c = _anyprec_state(flags, ph)
+        m32, v32, c32, kahan = flags & 1, flags & 2, flags & 4, not flags & 8
+        for t, gh in enumerate(grads, 1):
+            p0, m0, v0 = _f64(p), _f64(m), _f64(v)
+            c0 = _f64(c) if kahan else None
+            o.anyprec(p, gh, m, v, c, flags, hp, t)
+            g = bf16_to_f64(gh)
+            m1, v1 = _f64(m), _f64(v)
+            # moments, each in its own storage type
+            want = b1 * m0 + (1.0 - b1) * g
+            tol = 4 * EPS32 * (np.abs(b1 * m0) + np.abs((1.0 - b1) * g))
+            tol = tol + (0.0 if m32 else HALF_ULP * ulp_bf16(m1))
+            assert np.all(np.abs(m1 - want) <= tol + 1e-45), f"exp_avg, flags {flags}, t {t}"
+            want = b2 * v0 + (1.0 - b2) * g * g
+            tol = 5 * EPS32 * (np.abs(b2 * v0) + np.abs((1.0 - b2) * g * g))
+            tol = tol + (0.0 if v32 else HALF_ULP * ulp_bf16(v1))
+            assert np.all(np.abs(v1 - want) <= tol + 1e-45), f"exp_avg_sq, flags {flags}, t {t}"
+            # the update from the stored moments
+            bc1 = 1.0 - float(b1) ** t
+            bc2 = 1.0 - float(b2) ** t
+            adam = (lr / bc1) * m1 / (np.sqrt(v1) / math.sqrt(bc2) + eps)
+            decay = lr * wd * p0
+            upd = adam + decay
+            tol_upd = 12 * EPS32 * (np.abs(adam) + np.abs(decay))
+            p1 = bf16_to_f64(p)
+            if kahan:
+                c1 = _f64(c)
+                y = c0 - upd
+                err = np.abs((p1 + c1) - (p0 + c0 - upd))
+                tol = (tol_upd + 2 * EPS32 * np.abs(y) + 2 * EPS32 * np.abs(p1 - p0)
+                       + (2 * ulp_f32(c1) if c32 else HALF_ULP * ulp_bf16(c1) + ulp_f32(c1)))
+                assert np.all(err <= tol), \
+                    f"p + c, flags {flags}, t {t}: off by {np.max(err / tol):.3g} x tol"
+            else:
+                err = np.abs(p1 - (p0 - upd))
+                tol = HALF_ULP * ulp_bf16(p1) + ulp_f32(p0 - upd) + tol_upd
+                assert np.all(err <= tol), \
+                    f"p, flags {flags}, t {t}: off by {np.max(err / tol):.3g} x tol"
+
+
+def pin_anyprec_fp32_state_vs_torch(o: O.Oracle, steps: int = 200):
+    """fp32 momentum, variance and compensation on a bf16 parameter behave as
+    an fp32-master AdamW: over 200 steps p + c follows torch.optim.AdamW in
+    fp64 (no weight decay, so the bf16 parameter's decay term cannot differ
+    from the master's) to within the fp32 rounding of the update, although
+    no update is large enough to move a bf16 parameter of magnitude >= 0.5
+    by itself -- the same step without Kahan summation never moves them."""
+    r = _rng(23)
+    n = 64
+    mag = r.uniform(0.5, 2.0, n) * r.choice([-1.0, 1.0], n)
+    ph = torch_bf16_bits(mag.astype(F32))
+    grads = [torch_bf16_bits((r.standard_normal(n) * 1e-2).astype(F32)) for _ in range(steps)]
+    hp = O.hparams(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
+    p, m, v, c = _anyprec_state(7, ph)
+    q, mq, vq, _ = _anyprec_state(8 | 3, ph)
+    for t, gh in enumerate(grads, 1):
+        o.anyprec(p, gh, m, v, c, 7, hp, t)
+        o.anyprec(q, gh, mq, vq, None, 8 | 3, hp, t)
+    assert np.array_equal(q, ph), "without compensation the bf16 parameters stall"
+    assert np.array_equal(m, mq) and np.array_equal(v, vq), "moments do not depend on p"
+    tg = [torch.from_numpy(bf16_to_f64(gh)) for gh in grads]
+    tp, tm, tv = _torch_adamw(torch.from_numpy(bf16_to_f64(ph)), tg, f32(1e-3),
+                              (f32(0.9), f32(0.95)), f32(1e-8), 0.0)
+    tp, tm, tv = tp.numpy(), tm.numpy(), tv.numpy()
+    _close(m, tm, 2e-5, "fp32 exp_avg vs fp64")
+    _close(v, tv, 2e-5, "fp32 exp_avg_sq vs fp64")
+    got = bf16_to_f64(p) + c.astype(np.float64)
+    moved = np.abs(tp - bf16_to_f64(ph))
+    assert np.min(moved) > 0.0 and np.max(moved) > 0.02, "the trajectory must move"
+    err = np.abs(got - tp)
+    tol = steps * f32(1e-3) * 2e-5
+    assert np.all(err <= tol), f"p + c vs fp64 master: off by {np.max(err / tol):.3g} x tol"
+
+
 ALL_PINS = [
+    pin_anyprec_matches_named_modes,
+    pin_anyprec_step_definition,
+    pin_anyprec_fp32_state_vs_torch,
     pin_first_step_bf16_plain_and_v32,
     pin_torch_adamw_fp64_vs_v32,
     pin_lr_linear_warmup,

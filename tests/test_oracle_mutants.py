@@ -74,6 +74,27 @@ MUTANTS = [
      "        f = (double)(total - k - 1) / span;\n"),
     ("clip_scale_ignored_mixed", "float p0 = master[i];\n",
      "float p0 = master[i]; gi = bf16_bits_to_f32(g[i]);\n"),
+    ("anyprec_fp32_store_rounds", "        ((float*)buf)[i] = x;\n        return x;\n",
+     "        x = bf16_bits_to_f32(f32_to_bf16_rne(x));\n        ((float*)buf)[i] = x;\n"
+     "        return x;\n"),
+    ("anyprec_unrounded_moment_used", "        float ms = store_any(m, m32, i, m1);\n",
+     "        float ms = m1; store_any(m, m32, i, m1);\n"),
+    ("anyprec_unrounded_variance_used", "        float vs = store_any(v, v32, i, v1);\n",
+     "        float vs = v1; store_any(v, v32, i, v1);\n"),
+    ("anyprec_comp_sign", "            store_any(c, c32, i, y - (pn - p0));\n",
+     "            store_any(c, c32, i, y + (pn - p0));\n"),
+    ("anyprec_update_sign", "            float y = load_any(c, c32, i) - upd;\n",
+     "            float y = load_any(c, c32, i) + upd;\n"),
+    ("anyprec_comp_not_read", "            float y = load_any(c, c32, i) - upd;\n",
+     "            float y = 0.0f - upd;\n"),
+    ("anyprec_plain_sign", "            p[i] = f32_to_bf16_rne(p0 - upd);\n",
+     "            p[i] = f32_to_bf16_rne(p0 + upd);\n"),
+    ("anyprec_m_type_ignored", "    const int m32 = (flags & 1) != 0,", "    const int m32 = 0 * (flags & 1),"),
+    ("anyprec_v_type_ignored", "v32 = (flags & 2) != 0;", "v32 = 0 * (flags & 2);"),
+    ("anyprec_c_type_ignored", "    const int c32 = (flags & 4) != 0,", "    const int c32 = 0 * (flags & 4),"),
+    ("anyprec_kahan_ignored", "kahan = (flags & 8) == 0;", "kahan = 0 * (flags & 8);"),
+    ("anyprec_no_decay", "        float upd = (s.step_size * (ms / den)) + (s.lrwd * p0);\n\n        if (kahan)",
+     "        float upd = (s.step_size * (ms / den));\n\n        if (kahan)"),
 ]
 
 
