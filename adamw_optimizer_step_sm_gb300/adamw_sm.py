@@ -24,6 +24,14 @@ MODE_MIXED_FP32_MASTER = 1
 MODE_MIXED_BF16_REMAINDER = 2
 MODE_BF16_PLAIN = 3
 MODE_BF16_KAHAN_FP32_VAR = 4
+# AnyPrecisionAdamW storage: MODE_ANYPREC | ANYPREC_* flags (bf16 param and
+# grad; each flag makes one optimizer buffer fp32, or drops the compensation).
+MODE_ANYPREC = 16
+ANYPREC_M_FP32 = 1
+ANYPREC_V_FP32 = 2
+ANYPREC_C_FP32 = 4
+ANYPREC_NO_KAHAN = 8
+ANYPREC_MODES = tuple(MODE_ANYPREC | f for f in range(16) if (f & 12) != 12)
 PLAN_NORM = 1
 PLAN_NO_FUSE = 2
 STEP_CLIP = 1
@@ -254,13 +262,33 @@ def hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1,
 
 # --------------------------------------------------------- torch wrapper --
 
+def buffer_dtypes(mode: int):
+    """torch dtypes of param, grad, exp_avg, exp_avg_sq and aux in a storage
+    mode (None: the mode does not use that buffer)."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    named = {MODE_BF16_KAHAN: (bf,) * 5,
+             MODE_MIXED_FP32_MASTER: (f32, bf, f32, f32, bf),
+             MODE_MIXED_BF16_REMAINDER: (bf, bf, f32, f32, torch.int16),
+             MODE_BF16_PLAIN: (bf,) * 4 + (None,),
+             MODE_BF16_KAHAN_FP32_VAR: (bf, bf, bf, f32, bf)}
+    if mode in named:
+        return named[mode]
+    if mode not in ANYPREC_MODES:
+        raise ValueError(f"unknown storage mode {mode}")
+    f = mode & 15
+    return (bf, bf, f32 if f & ANYPREC_M_FP32 else bf, f32 if f & ANYPREC_V_FP32 else bf,
+            None if f & ANYPREC_NO_KAHAN else (f32 if f & ANYPREC_C_FP32 else bf))
+
+
 class Plan:
     """A plan over lists of torch CUDA tensors (one list per buffer kind).
 
     bf16 Kahan mode: params, exp_avg, exp_avg_sq, aux (= compensation) bf16.
     Mixed mode: params (= fp32 master), exp_avg, exp_avg_sq fp32; aux = bf16
     param out.  Remainder mode: params bf16, exp_avg, exp_avg_sq fp32, aux =
-    int16 remainder of the fp32 master.  grads are bf16 in all modes.  The tensors must stay alive and in
+    int16 remainder of the fp32 master.  Any-precision modes: as
+    ``buffer_dtypes(mode)``.  grads are bf16 in all modes.  The tensors must stay alive and in
     place for the plan's lifetime (the plan holds references to them).
     """
 
@@ -273,14 +301,7 @@ class Plan:
         n = len(lists[0])
         if any(len(x) != n for x in lists):
             raise ValueError("tensor lists differ in length")
-        want = {MODE_BF16_KAHAN: (torch.bfloat16,) * 5,
-                MODE_MIXED_FP32_MASTER: (torch.float32, torch.bfloat16, torch.float32,
-                                         torch.float32, torch.bfloat16),
-                MODE_MIXED_BF16_REMAINDER: (torch.bfloat16, torch.bfloat16, torch.float32,
-                                            torch.float32, torch.int16),
-                MODE_BF16_PLAIN: (torch.bfloat16,) * 4 + (None,),
-                MODE_BF16_KAHAN_FP32_VAR: (torch.bfloat16, torch.bfloat16, torch.bfloat16,
-                                           torch.float32, torch.bfloat16)}[mode]
+        want = buffer_dtypes(mode)
         entries = []
         for k in range(n):
             ts = [x[k] for x in lists]

@@ -97,7 +97,18 @@ enum Kind { kPlain = 0, kClip = 1, kReport = 2 };
 
 // ---- host planner (plan_build.cpp) ----
 
-constexpr int kModes = 5;
+// Kernel variants: one per storage mode 0..4 and one per any-precision mode
+// that is not one of those under another number.
+constexpr int kModes = 14;
+constexpr int32_t kVariantModes[kModes] = {
+    ADAMW_MODE_BF16_KAHAN, ADAMW_MODE_MIXED_FP32_MASTER, ADAMW_MODE_MIXED_BF16_REMAINDER,
+    ADAMW_MODE_BF16_PLAIN, ADAMW_MODE_BF16_KAHAN_FP32_VAR,
+    ADAMW_MODE_ANYPREC | 1, ADAMW_MODE_ANYPREC | 3, ADAMW_MODE_ANYPREC | 4,
+    ADAMW_MODE_ANYPREC | 5, ADAMW_MODE_ANYPREC | 6, ADAMW_MODE_ANYPREC | 7,
+    ADAMW_MODE_ANYPREC | 9, ADAMW_MODE_ANYPREC | 10, ADAMW_MODE_ANYPREC | 11};
+// The variant (index into kVariantModes) that runs a storage mode; -1 for an
+// invalid mode.  The any-precision modes 16, 18 and 24 run variants 0, 4, 3.
+int mode_variant(int32_t mode);
 bool valid_mode(int32_t mode);
 // Bytes per element of param, grad, exp_avg, exp_avg_sq, aux in a mode.
 void element_sizes(int32_t mode, int64_t es[5]);

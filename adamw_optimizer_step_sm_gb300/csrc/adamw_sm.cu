@@ -1,8 +1,8 @@
 // adamw_sm.cu -- the C ABI: plans, the step entry points, the norm pass and
 // its finalize, the device-resident step's prologue, the on-device learning
 // rate schedule, the copy probe and the allocation-free norm entry.  The
-// update kernels of the five storage modes live in update_m0.cu ..
-// update_m4.cu and are reached through mode_ops<MODE>() (launch.h).
+// update kernels of each storage mode live in update_m<MODE>.cu and are
+// reached through mode_ops<MODE>() (launch.h).
 //
 // The step is a streaming elementwise update: per element it reads p, g, m, v
 // and c (bf16 Kahan mode, 10 B), master, m, v and g (mixed mode, 14 B) or p,
@@ -175,15 +175,26 @@ bool cuda_ok(cudaError_t e, const char* where) {
     return false;
 }
 
-const ModeOps& ops(int mode) {
-    switch (mode) {
-        case 0: return mode_ops<0>();
-        case 1: return mode_ops<1>();
-        case 2: return mode_ops<2>();
-        case 3: return mode_ops<3>();
-        default: return mode_ops<4>();
+// The launchers of a kernel variant (an index into kVariantModes).
+const ModeOps& ops(int variant) {
+    switch (variant) {
+        case 0: return mode_ops<kVariantModes[0]>();
+        case 1: return mode_ops<kVariantModes[1]>();
+        case 2: return mode_ops<kVariantModes[2]>();
+        case 3: return mode_ops<kVariantModes[3]>();
+        case 4: return mode_ops<kVariantModes[4]>();
+        case 5: return mode_ops<kVariantModes[5]>();
+        case 6: return mode_ops<kVariantModes[6]>();
+        case 7: return mode_ops<kVariantModes[7]>();
+        case 8: return mode_ops<kVariantModes[8]>();
+        case 9: return mode_ops<kVariantModes[9]>();
+        case 10: return mode_ops<kVariantModes[10]>();
+        case 11: return mode_ops<kVariantModes[11]>();
+        case 12: return mode_ops<kVariantModes[12]>();
+        default: return mode_ops<kVariantModes[13]>();
     }
 }
+static_assert(kModes == 14, "ops() lists every kernel variant");
 
 int device_info(int dev, DeviceInfo* out) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -260,8 +271,9 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     rc = device_info(dev, &di);
     if (rc != ADAMW_OK) return rc;
 
-    int occ = di.occ[mode][kPlain];
-    for (int k = 0; k < 3; ++k) occ = occ < di.occ[mode][k] ? occ : di.occ[mode][k];
+    const int var = mode_variant(mode);
+    int occ = di.occ[var][kPlain];
+    for (int k = 0; k < 3; ++k) occ = occ < di.occ[var][k] ? occ : di.occ[var][k];
     if (occ < 1) occ = 1;
     const int occ_norm = di.occ_norm > 0 ? di.occ_norm : 1;
 
@@ -270,9 +282,9 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     // Lists whose gradients fit in half of L2 run clipped steps as one fused
     // cooperative launch (the norm pass leaves g in L2 for the update).
     const bool fused = (flags & ADAMW_PLAN_NORM) && !(flags & ADAMW_PLAN_NO_FUSE) &&
-                       di.cooperative && di.occ_fused[mode] > 0 &&
+                       di.cooperative && di.occ_fused[var] > 0 &&
                        total * 2 <= kFusedMaxGradBytes;
-    if (fused) occ = occ < di.occ_fused[mode] ? occ : di.occ_fused[mode];
+    if (fused) occ = occ < di.occ_fused[var] ? occ : di.occ_fused[var];
     const int32_t grid = choose_grid(total, di.sms * occ);
     // the fused kernel's norm pass uses the update grid; plans without it
     // give the norm pass its own, larger grid
@@ -296,6 +308,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     adamw_plan* P = new adamw_plan();
     P->device = dev;
     P->mode = mode;
+    P->variant = var;
     P->flags = flags;
     P->n_tensors = n_tensors;
     P->total = total;
@@ -387,7 +400,7 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
     }
 
     if (clip && plan->fused) {
-        if (!cuda_ok(ops(plan->mode).fused(plan, s, d_grad_norm, d_nonfinite, st), "fused launch"))
+        if (!cuda_ok(ops(plan->variant).fused(plan, s, d_grad_norm, d_nonfinite, st), "fused launch"))
             return ADAMW_ERR_CUDA;
         return ADAMW_OK;
     }
@@ -404,7 +417,7 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
         kind = kReport;
         report = d_nonfinite;
     }
-    if (!cuda_ok(ops(plan->mode).update(plan, kind, false, s, report, st), "update launch"))
+    if (!cuda_ok(ops(plan->variant).update(plan, kind, false, s, report, st), "update launch"))
         return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }
@@ -448,7 +461,7 @@ extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
     if (!want_norm && plan->upd.grid > 0) {
         // one launch: every CTA computes the scalars, the last one advances
         // the counter
-        const cudaError_t e = ops(plan->mode).self(plan, d_nonfinite ? kReport : kPlain, d_hp,
+        const cudaError_t e = ops(plan->variant).self(plan, d_nonfinite ? kReport : kPlain, d_hp,
                                                    d_step, d_nonfinite, st);
         return cuda_ok(e, "update launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
     }
@@ -468,7 +481,7 @@ extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
     if (plan->upd.grid == 0) return ADAMW_OK;
     const int kind = clip ? kClip : (!want_norm && d_nonfinite) ? kReport : kPlain;
     int32_t* report = (kind == kReport) ? d_nonfinite : nullptr;
-    if (!cuda_ok(ops(plan->mode).update(plan, kind, true, StepScalars{}, report, st), "update launch"))
+    if (!cuda_ok(ops(plan->variant).update(plan, kind, true, StepScalars{}, report, st), "update launch"))
         return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }

@@ -512,6 +512,183 @@ __device__ __forceinline__ void kahan_v32_elem_chunk(const ChunkPtr& t, int64_t 
     }
 }
 
+// ---- any precision: bf16 p and g; exp_avg, exp_avg_sq and the
+// compensation each bf16 or fp32, Kahan summation on or off (FLAGS = the
+// ADAMW_ANYPREC_* bits of the storage mode).
+
+// The float holding the bf16 nearest to x (round to nearest even).
+__device__ __forceinline__ float round_bf16(float x) { return from_bf16(to_bf16(x)); }
+
+// One element.  m, v, c come in as stored and leave as stored (rounded to
+// their own type); pn is the new parameter (a bf16 value).
+template <int FLAGS, int K>
+__device__ __forceinline__ void anyprec_x1(const StepScalars& s, float coef, float g, float p0,
+                                           float& m, float& v, float& c, float& pn) {
+    constexpr bool kM32 = (FLAGS & ADAMW_ANYPREC_M_FP32) != 0;
+    constexpr bool kV32 = (FLAGS & ADAMW_ANYPREC_V_FP32) != 0;
+    constexpr bool kC32 = (FLAGS & ADAMW_ANYPREC_C_FP32) != 0;
+    constexpr bool kKahan = (FLAGS & ADAMW_ANYPREC_NO_KAHAN) == 0;
+    if (K == kClip) g = __fmul_rn(g, coef);
+    float m1, v1;
+    moments(s, g, m, v, m1, v1);
+    m = kM32 ? m1 : round_bf16(m1);
+    v = kV32 ? v1 : round_bf16(v1);
+    const float upd = update_of(s, m, v, p0);
+    if (kKahan) {
+        const float y = __fsub_rn(c, upd);
+        pn = round_bf16(__fadd_rn(p0, y));
+        const float cn = __fsub_rn(y, __fsub_rn(pn, p0));
+        c = kC32 ? cn : round_bf16(cn);
+    } else {
+        pn = round_bf16(__fsub_rn(p0, upd));
+    }
+}
+
+// Eight consecutive elements of one stream as loaded: bf16 (one 16-byte
+// access) or fp32 (two).  set2 takes values that are already of the
+// stream's type.
+template <bool F32>
+struct Raw8;
+template <>
+struct Raw8<false> {
+    uint4 r;
+    __device__ __forceinline__ void load(const void* b, int64_t e) {
+        r = ld16(static_cast<const uint16_t*>(b) + e);
+    }
+    __device__ __forceinline__ void store(void* b, int64_t e) const {
+        st16(static_cast<uint16_t*>(b) + e, r);
+    }
+    __device__ __forceinline__ uint32_t word(int w) const {
+        return w == 0 ? r.x : w == 1 ? r.y : w == 2 ? r.z : r.w;
+    }
+    __device__ __forceinline__ float get(int j) const {
+        return (j & 1) ? bf16_hi(word(j >> 1)) : bf16_lo(word(j >> 1));
+    }
+    __device__ __forceinline__ void set2(int w, float lo, float hi) {
+        const uint32_t u = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+        if (w == 0) r.x = u;
+        else if (w == 1) r.y = u;
+        else if (w == 2) r.z = u;
+        else r.w = u;
+    }
+};
+template <>
+struct Raw8<true> {
+    F8 r;
+    __device__ __forceinline__ void load(const void* b, int64_t e) {
+        r = ld32(static_cast<const float*>(b) + e);
+    }
+    __device__ __forceinline__ void store(void* b, int64_t e) const {
+        st32(static_cast<float*>(b) + e, r);
+    }
+    __device__ __forceinline__ float get(int j) const { return r.x[j]; }
+    __device__ __forceinline__ void set2(int w, float lo, float hi) {
+        r.x[2 * w] = lo;
+        r.x[2 * w + 1] = hi;
+    }
+};
+
+// One element of a bf16 or fp32 stream; the value stored must already be of
+// the stream's type.
+template <bool F32>
+__device__ __forceinline__ float ld1(const void* b, int64_t i) {
+    if constexpr (F32) return static_cast<const float*>(b)[i];
+    else return from_bf16(static_cast<const uint16_t*>(b)[i]);
+}
+template <bool F32>
+__device__ __forceinline__ void st1(void* b, int64_t i, float x) {
+    if constexpr (F32) static_cast<float*>(b)[i] = x;
+    else static_cast<uint16_t*>(b)[i] = uint16_t(__float_as_uint(x) >> 16);
+}
+
+template <int FLAGS, int K>
+__device__ __forceinline__ void anyprec_one(const ChunkPtr& t, int64_t i, const StepScalars& s,
+                                            float coef, bool& bad) {
+    constexpr bool kM32 = (FLAGS & ADAMW_ANYPREC_M_FP32) != 0;
+    constexpr bool kV32 = (FLAGS & ADAMW_ANYPREC_V_FP32) != 0;
+    constexpr bool kC32 = (FLAGS & ADAMW_ANYPREC_C_FP32) != 0;
+    constexpr bool kKahan = (FLAGS & ADAMW_ANYPREC_NO_KAHAN) == 0;
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t gh = static_cast<const uint16_t*>(t.g)[i];
+    if (K == kReport) bad |= (gh & 0x7f80u) == 0x7f80u;
+    float m = ld1<kM32>(t.m, i), v = ld1<kV32>(t.v, i);
+    float c = kKahan ? ld1<kC32>(t.a, i) : 0.0f;
+    float pn;
+    anyprec_x1<FLAGS, K>(s, coef, from_bf16(gh), from_bf16(p[i]), m, v, c, pn);
+    p[i] = uint16_t(__float_as_uint(pn) >> 16);
+    st1<kM32>(t.m, i, m);
+    st1<kV32>(t.v, i, v);
+    if (kKahan) st1<kC32>(t.a, i, c);
+}
+
+template <int FLAGS, int K>
+__device__ __forceinline__ void anyprec_vec_chunk(const ChunkPtr& t, int64_t len,
+                                                  const StepScalars& s, float coef, bool& bad) {
+    constexpr bool kM32 = (FLAGS & ADAMW_ANYPREC_M_FP32) != 0;
+    constexpr bool kV32 = (FLAGS & ADAMW_ANYPREC_V_FP32) != 0;
+    constexpr bool kC32 = (FLAGS & ADAMW_ANYPREC_C_FP32) != 0;
+    constexpr bool kKahan = (FLAGS & ADAMW_ANYPREC_NO_KAHAN) == 0;
+    uint16_t* p = static_cast<uint16_t*>(t.p);
+    const uint16_t* g = static_cast<const uint16_t*>(t.g);
+    const int64_t nvec = len / kVec;
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
+        uint4 G[kUnroll], P[kUnroll];
+        Raw8<kM32> M[kUnroll];
+        Raw8<kV32> V[kUnroll];
+        Raw8<kC32> C[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                G[u] = ld16(g + i * kVec);
+                P[u] = ld16(p + i * kVec);
+                M[u].load(t.m, i * kVec);
+                V[u].load(t.v, i * kVec);
+                if (kKahan) C[u].load(t.a, i * kVec);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = base + int64_t(u) * kBlock;
+            if (i < nvec) {
+                const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
+                const uint32_t pw[4] = {P[u].x, P[u].y, P[u].z, P[u].w};
+                if (K == kReport)
+                    bad |= bf16x2_nonfinite(gw[0]) | bf16x2_nonfinite(gw[1]) |
+                           bf16x2_nonfinite(gw[2]) | bf16x2_nonfinite(gw[3]);
+                uint32_t po[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    float m0 = M[u].get(2 * w), m1 = M[u].get(2 * w + 1);
+                    float v0 = V[u].get(2 * w), v1 = V[u].get(2 * w + 1);
+                    float c0 = kKahan ? C[u].get(2 * w) : 0.0f;
+                    float c1 = kKahan ? C[u].get(2 * w + 1) : 0.0f;
+                    float pn0, pn1;
+                    anyprec_x1<FLAGS, K>(s, coef, bf16_lo(gw[w]), bf16_lo(pw[w]), m0, v0, c0, pn0);
+                    anyprec_x1<FLAGS, K>(s, coef, bf16_hi(gw[w]), bf16_hi(pw[w]), m1, v1, c1, pn1);
+                    po[w] = (__float_as_uint(pn0) >> 16) | (__float_as_uint(pn1) & 0xffff0000u);
+                    M[u].set2(w, m0, m1);
+                    V[u].set2(w, v0, v1);
+                    if (kKahan) C[u].set2(w, c0, c1);
+                }
+                st16(p + i * kVec, make_uint4(po[0], po[1], po[2], po[3]));
+                M[u].store(t.m, i * kVec);
+                V[u].store(t.v, i * kVec);
+                if (kKahan) C[u].store(t.a, i * kVec);
+            }
+        }
+    }
+    // ragged end of a vector body (< kVec elements)
+    const int64_t tail = len - nvec * kVec;
+    if (threadIdx.x < tail) anyprec_one<FLAGS, K>(t, nvec * kVec + threadIdx.x, s, coef, bad);
+}
+
+template <int FLAGS, int K>
+__device__ __forceinline__ void anyprec_elem_chunk(const ChunkPtr& t, int64_t len,
+                                                   const StepScalars& s, float coef, bool& bad) {
+    for (int64_t i = threadIdx.x; i < len; i += kBlock) anyprec_one<FLAGS, K>(t, i, s, coef, bad);
+}
+
 // Remainder mode: the fp32 master is the bf16 parameter (high half) plus a
 // signed 16-bit remainder of the bit pattern.
 __device__ __forceinline__ float join_master(uint32_t hi_bits, uint32_t rem16) {
@@ -647,21 +824,25 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
         if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
         const int64_t len = cur.len2 >> 1;
         const bool vec = cur.len2 & 1;
-        if (MODE == ADAMW_MODE_BF16_KAHAN) {
+        if constexpr (MODE == ADAMW_MODE_BF16_KAHAN) {
             if (vec) kahan_vec_chunk<K>(cur, len, s, coef, bad);
             else kahan_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
+        } else if constexpr (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
             if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
             else mixed_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
+        } else if constexpr (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
             if (vec) remainder_vec_chunk<K>(cur, len, s, coef, bad);
             else remainder_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if (MODE == ADAMW_MODE_BF16_PLAIN) {
+        } else if constexpr (MODE == ADAMW_MODE_BF16_PLAIN) {
             if (vec) plain_vec_chunk<K>(cur, len, s, coef, bad);
             else plain_elem_chunk<K>(cur, len, s, coef, bad);
-        } else {
+        } else if constexpr (MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR) {
             if (vec) kahan_v32_vec_chunk<K>(cur, len, s, coef, bad);
             else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
+        } else {
+            constexpr int kFlags = MODE & ~ADAMW_MODE_ANYPREC;
+            if (vec) anyprec_vec_chunk<kFlags, K>(cur, len, s, coef, bad);
+            else anyprec_elem_chunk<kFlags, K>(cur, len, s, coef, bad);
         }
         cur = nxt;
     }

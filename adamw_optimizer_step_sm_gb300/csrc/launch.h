@@ -1,8 +1,8 @@
 // launch.h -- the plan object and the per-storage-mode launchers.
 //
 // Each storage mode's update kernels are instantiated in a translation unit of
-// their own (update_m0.cu .. update_m4.cu, all from update_mode.inc), so the
-// five modes compile in parallel; adamw_sm.cu reaches them through the table
+// their own (update_m<MODE>.cu, all from update_mode.inc), so the modes
+// compile in parallel; adamw_sm.cu reaches them through the table
 // of launchers that mode_ops<MODE>() returns.
 #pragma once
 
@@ -25,6 +25,7 @@ struct DevPartition {
 struct adamw_plan {
     int device = 0;
     int32_t mode = 0;
+    int variant = 0;  // index of the mode's kernels in adamw::kVariantModes
     int32_t flags = 0;
     int32_t n_tensors = 0;
     int64_t total = 0;
@@ -75,5 +76,14 @@ template <> const ModeOps& mode_ops<1>();
 template <> const ModeOps& mode_ops<2>();
 template <> const ModeOps& mode_ops<3>();
 template <> const ModeOps& mode_ops<4>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 1>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 3>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 4>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 5>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 6>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 7>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 9>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 10>();
+template <> const ModeOps& mode_ops<ADAMW_MODE_ANYPREC | 11>();
 
 }  // namespace adamw

@@ -45,17 +45,37 @@ int vector_head(const adamw_tensor_t& t, int32_t mode) {
 
 void element_sizes(int32_t mode, int64_t es[5]) {
     // param, grad, exp_avg, exp_avg_sq, aux (0: aux unused)
-    static const int64_t table[kModes][5] = {
+    static const int64_t table[5][5] = {
         {2, 2, 2, 2, 2},  // bf16 Kahan
         {4, 2, 4, 4, 2},  // mixed fp32 master
         {2, 2, 4, 4, 2},  // mixed bf16 + remainder
         {2, 2, 2, 2, 0},  // bf16 without compensation
         {2, 2, 2, 4, 2},  // bf16 Kahan, fp32 variance
     };
+    if (mode >= ADAMW_MODE_ANYPREC) {
+        es[0] = 2;
+        es[1] = 2;
+        es[2] = (mode & ADAMW_ANYPREC_M_FP32) ? 4 : 2;
+        es[3] = (mode & ADAMW_ANYPREC_V_FP32) ? 4 : 2;
+        es[4] = (mode & ADAMW_ANYPREC_NO_KAHAN) ? 0 : (mode & ADAMW_ANYPREC_C_FP32) ? 4 : 2;
+        return;
+    }
     for (int s = 0; s < 5; ++s) es[s] = table[mode][s];
 }
 
-bool valid_mode(int32_t mode) { return mode >= 0 && mode < kModes; }
+int mode_variant(int32_t mode) {
+    if (mode >= 0 && mode < 5) return mode;
+    if (mode < ADAMW_MODE_ANYPREC || mode >= 2 * ADAMW_MODE_ANYPREC) return -1;
+    if ((mode & ADAMW_ANYPREC_NO_KAHAN) && (mode & ADAMW_ANYPREC_C_FP32)) return -1;
+    if (mode == ADAMW_MODE_ANYPREC) return ADAMW_MODE_BF16_KAHAN;
+    if (mode == (ADAMW_MODE_ANYPREC | ADAMW_ANYPREC_V_FP32)) return ADAMW_MODE_BF16_KAHAN_FP32_VAR;
+    if (mode == (ADAMW_MODE_ANYPREC | ADAMW_ANYPREC_NO_KAHAN)) return ADAMW_MODE_BF16_PLAIN;
+    for (int k = 5; k < kModes; ++k)
+        if (kVariantModes[k] == mode) return k;
+    return -1;
+}
+
+bool valid_mode(int32_t mode) { return mode_variant(mode) >= 0; }
 
 void set_cuda_error(const char* where, const char* what) {
     g_cuda_error = std::string(where) + ": " + what;

@@ -46,6 +46,18 @@ MODE_DTYPES = {
     MODE_BF16_KAHAN_V32: (torch.bfloat16, torch.bfloat16, torch.float32, torch.bfloat16),
 }
 
+# AnyPrecisionAdamW storage modes: MODE_ANYPREC + flags (1: fp32 exp_avg,
+# 2: fp32 exp_avg_sq, 4: fp32 compensation, 8: no compensation).
+MODE_ANYPREC = 16
+ANYPREC_MODES = tuple(MODE_ANYPREC | f for f in range(16) if (f & 12) != 12)
+for _m in ANYPREC_MODES:
+    _f = _m & 15
+    MODE_DTYPES[_m] = (torch.bfloat16,
+                       torch.float32 if _f & 1 else torch.bfloat16,
+                       torch.float32 if _f & 2 else torch.bfloat16,
+                       None if _f & 8 else (torch.float32 if _f & 4 else torch.bfloat16))
+del _m, _f
+
 
 @dataclass(frozen=True)
 class TensorSpec:
@@ -169,6 +181,15 @@ WORKLOADS: dict[str, Workload] = {
         "opt1.3b_bf16_kahan_v32", MODE_BF16_KAHAN_V32, OPT_1_3B, 5,
         lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, g_std=1e-2,
         heavy_tail=True, description="OPT-1.3b tensor list, bf16 Kahan with fp32 variance"),
+    "opt1.3b_anyprec_fp32_state": Workload(
+        "opt1.3b_anyprec_fp32_state", MODE_ANYPREC | 7, OPT_1_3B, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, g_std=1e-2,
+        heavy_tail=True, description="OPT-1.3b tensor list, bf16 param with fp32 momentum, "
+                                     "variance and Kahan compensation"),
+    "opt1.3b_anyprec_m32": Workload(
+        "opt1.3b_anyprec_m32", MODE_ANYPREC | 1, OPT_1_3B, 5,
+        lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, g_std=1e-2,
+        heavy_tail=True, description="OPT-1.3b tensor list, bf16 Kahan with fp32 momentum"),
     # profiling-size case of the clipped mixed step (2 GB of state, > L2)
     "opt125m_mixed_clip": Workload(
         "opt125m_mixed_clip", MODE_MIXED, OPT_125M, 5,

@@ -46,11 +46,33 @@ def bytes_per_param(w: W.Workload) -> int:
     mixed: read master, m, v (12) + g (2), write master, m, v (12) + p_out (2)
     = 28.  remainder: read p, r (4) + m, v (8) + g (2), write p, r, m, v (12)
     = 26.  bf16 plain: read p, g, m, v (8), write p, m, v (6) = 14.  bf16
-    Kahan with fp32 v: read 12, write 10 = 22.  With clipping the norm pass
-    reads g once more: +2."""
-    base = {W.MODE_BF16_KAHAN: 18, W.MODE_MIXED: 28, W.MODE_REMAINDER: 26,
-            W.MODE_BF16_PLAIN: 14, W.MODE_BF16_KAHAN_V32: 22}[w.mode]
+    Kahan with fp32 v: read 12, write 10 = 22.  Any precision: p and g (read
+    4, write 2) plus each of m, v, c read and written in its own width, so
+    6 + 2 * (m + v + c) bytes, c = 0 without Kahan summation (all-fp32 state:
+    30).  With clipping the norm pass reads g once more: +2."""
+    if w.mode >= W.MODE_ANYPREC:
+        f = w.mode - W.MODE_ANYPREC
+        mvc = (4 if f & 1 else 2) + (4 if f & 2 else 2) + (0 if f & 8 else (4 if f & 4 else 2))
+        base = 6 + 2 * mvc
+    else:
+        base = {W.MODE_BF16_KAHAN: 18, W.MODE_MIXED: 28, W.MODE_REMAINDER: 26,
+                W.MODE_BF16_PLAIN: 14, W.MODE_BF16_KAHAN_V32: 22}[w.mode]
     return base + (2 if w.max_grad_norm > 0 else 0)
+
+
+def mode_name(mode: int) -> tuple[str, str]:
+    """Name and buffer layout of a storage mode, for the JSON line."""
+    named = {0: ("bf16_kahan", "bf16 p/g/m/v/c"),
+             1: ("mixed_fp32_master", "fp32 master/m/v, bf16 g and param out"),
+             2: ("mixed_bf16_remainder", "bf16 p + int16 remainder, fp32 m/v, bf16 g"),
+             3: ("bf16_plain", "bf16 p/g/m/v, no compensation"),
+             4: ("bf16_kahan_fp32_variance", "bf16 p/g/m/c, fp32 v")}
+    if mode in named:
+        return named[mode]
+    f = mode - W.MODE_ANYPREC
+    m, v = ("fp32" if f & 1 else "bf16"), ("fp32" if f & 2 else "bf16")
+    c = "no compensation" if f & 8 else ("fp32" if f & 4 else "bf16") + " c"
+    return (f"anyprecision_{f}", f"bf16 p/g, {m} m, {v} v, {c}")
 
 
 def load_peaks() -> dict:
@@ -64,7 +86,9 @@ def load_peaks() -> dict:
 
 KERNEL_SOURCES = ("adamw_internal.h", "device_common.cuh", "kernels.cuh", "launch.h",
                   "update_mode.inc", "update_m0.cu", "update_m1.cu", "update_m2.cu",
-                  "update_m3.cu", "update_m4.cu")
+                  "update_m3.cu", "update_m4.cu", "update_m17.cu", "update_m19.cu",
+                  "update_m20.cu", "update_m21.cu", "update_m22.cu", "update_m23.cu",
+                  "update_m25.cu", "update_m26.cu", "update_m27.cu")
 
 
 def kernel_source_hash() -> str:
@@ -199,8 +223,11 @@ def oracle_throughput(w: W.Workload, n_elems: int, steps: int, threads: int, arr
                 o.remainder(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
             elif ws.mode == W.MODE_BF16_PLAIN:
                 o.bf16_plain(p[sl], g[sl], m[sl], v[sl], hp, t, coef)
-            else:
+            elif ws.mode == W.MODE_BF16_KAHAN_V32:
                 o.bf16_kahan_v32(p[sl], g[sl], m[sl], v[sl], a[sl], hp, t, coef)
+            else:
+                o.anyprec(p[sl], g[sl], m[sl], v[sl], None if a is None else a[sl],
+                          ws.mode - W.MODE_ANYPREC, hp, t, coef)
 
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, pieces))
@@ -503,12 +530,8 @@ def run_gpu(args):
         "config": {
             "workload": w.name, "description": w.description, "n_params": N,
             "n_tensors": w.n_tensors,
-            "mode": {0: "bf16_kahan", 1: "mixed_fp32_master", 2: "mixed_bf16_remainder",
-                     3: "bf16_plain", 4: "bf16_kahan_fp32_variance"}[w.mode],
-            "storage": {0: "bf16 p/g/m/v/c", 1: "fp32 master/m/v, bf16 g and param out",
-                        2: "bf16 p + int16 remainder, fp32 m/v, bf16 g",
-                        3: "bf16 p/g/m/v, no compensation",
-                        4: "bf16 p/g/m/c, fp32 v"}[w.mode],
+            "mode": mode_name(w.mode)[0],
+            "storage": mode_name(w.mode)[1],
             "clip": clip, "bytes_per_param": bpp, "hparams": w.hparams(),
             "l2": (f"256 MiB written before every timed step (L2 flushed; {bpp * N / 1e6:.1f} MB "
                    "moved per step)") if flush else

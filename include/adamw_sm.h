@@ -32,6 +32,17 @@
  *   ADAMW_MODE_BF16_KAHAN_FP32_VAR  AnyPrecisionAdamW with bf16 momentum and
  *       compensation and variance_dtype=float32: bf16 p, g, m, c, fp32 v.
  *
+ *   ADAMW_MODE_ANYPREC | flags  AnyPrecisionAdamW with every buffer type the
+ *       recipe's optim_args name: momentum_dtype, variance_dtype and
+ *       compensation_buffer_dtype each bfloat16 or float32, and
+ *       use_kahan_summation on or off.  bf16 p and g; ADAMW_ANYPREC_M_FP32,
+ *       ADAMW_ANYPREC_V_FP32 and ADAMW_ANYPREC_C_FP32 make exp_avg, exp_avg_sq
+ *       and the compensation (aux) fp32, ADAMW_ANYPREC_NO_KAHAN drops the
+ *       compensation (aux unused; C_FP32 is then invalid).  Twelve modes,
+ *       16..27 less 28..31; 16, 18 and 24 are the same steps as
+ *       ADAMW_MODE_BF16_KAHAN, ADAMW_MODE_BF16_KAHAN_FP32_VAR and
+ *       ADAMW_MODE_BF16_PLAIN and run those modes' kernels.
+ *
  * Arithmetic (identical in both modes up to storage; fp32, one IEEE
  * round-to-nearest per operation, no fused multiply-add):
  *   host, fp64 rounded once to fp32:  step_size = lr / (1 - beta1^t),
@@ -47,6 +58,8 @@
  *       (p16', r16') = split(master')
  *   bf16 plain: p' = bf16(p - upd)
  *   bf16 Kahan fp32 variance: as bf16 mode with v' kept in fp32
+ *   any precision: as bf16 mode (or bf16 plain without Kahan), each of
+ *       m', v', c' rounded to its own storage type and used as stored
  *   clipping:   norm = sqrt(sum g^2) over every tensor of the plan;
  *       coef = min(1, max_grad_norm / (norm + 1e-6)); a non-finite gradient
  *       anywhere sets the non-finite flag and the step writes no state.
@@ -74,6 +87,11 @@ typedef struct CUstream_st* adamw_stream_t;
 #define ADAMW_MODE_MIXED_BF16_REMAINDER 2
 #define ADAMW_MODE_BF16_PLAIN 3
 #define ADAMW_MODE_BF16_KAHAN_FP32_VAR 4
+#define ADAMW_MODE_ANYPREC 16      /* | the ADAMW_ANYPREC_* flags below */
+#define ADAMW_ANYPREC_M_FP32 1     /* exp_avg stored as fp32             */
+#define ADAMW_ANYPREC_V_FP32 2     /* exp_avg_sq stored as fp32          */
+#define ADAMW_ANYPREC_C_FP32 4     /* compensation (aux) stored as fp32  */
+#define ADAMW_ANYPREC_NO_KAHAN 8   /* no compensation; aux unused        */
 
 /* adamw_plan_create flags. */
 #define ADAMW_PLAN_NORM 1     /* allocate the global-norm workspace (clipping)  */
@@ -108,6 +126,12 @@ typedef struct CUstream_st* adamw_stream_t;
  *   exp_avg    bf16 m (r/w)        | bf16 m (r/w)
  *   exp_avg_sq bf16 v (r/w)        | fp32 v (r/w)
  *   aux        unused (NULL ok)    | bf16 Kahan c (r/w)
+ *              any precision (ADAMW_MODE_ANYPREC | flags)
+ *   param      bf16 p (r/w)
+ *   exp_avg    bf16 m, fp32 with ADAMW_ANYPREC_M_FP32 (r/w)
+ *   exp_avg_sq bf16 v, fp32 with ADAMW_ANYPREC_V_FP32 (r/w)
+ *   aux        bf16 Kahan c, fp32 with ADAMW_ANYPREC_C_FP32 (r/w);
+ *              unused (NULL ok) with ADAMW_ANYPREC_NO_KAHAN
  * Element alignment is required (2 B for 16-bit, 4 B for fp32 buffers).  Tensors whose
  * five bases are all 16-byte aligned take the vectorised path; others are
  * still updated correctly, more slowly.  numel may be 0. */

@@ -165,8 +165,10 @@ class OracleRun:
             self.o.remainder(p, g, m, v, a, hp, t, coef)
         elif self.w.mode == W.MODE_BF16_PLAIN:
             self.o.bf16_plain(p, g, m, v, hp, t, coef)
-        else:
+        elif self.w.mode == W.MODE_BF16_KAHAN_V32:
             self.o.bf16_kahan_v32(p, g, m, v, a, hp, t, coef)
+        else:
+            self.o.anyprec(p, g, m, v, a, self.w.mode - W.MODE_ANYPREC, hp, t, coef)
 
     def views(self, name, k):
         o, n = self.offsets[k], self.numels[k]

@@ -34,6 +34,12 @@ def test_library_exports_every_declared_symbol():
 
 
 ELEM_SIZES = {0: (2, 2, 2, 2, 2), 1: (4, 2, 4, 4, 2), 2: (2, 2, 4, 4, 2)}
+# any-precision modes: bf16 param and grad; the flags make m, v, c fp32 or
+# drop c (written out from the header's table, not from the library)
+for _f in range(16):
+    if (_f & 12) != 12:
+        ELEM_SIZES[16 + _f] = (2, 2, 4 if _f & 1 else 2, 4 if _f & 2 else 2,
+                               0 if _f & 8 else (4 if _f & 4 else 2))
 
 
 def _fake(base, n, mode=0, skew=(0, 0, 0, 0, 0)):
@@ -98,6 +104,58 @@ def test_partition_misaligned_bases_take_head_or_element_path():
     with pytest.raises(A.AdamWError) as e:
         A.adamw_plan_chunks([(16, 16, 34, 48, 64, 10)], 2, 2)
     assert e.value.status == A.ADAMW_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("mode", A.ANYPREC_MODES)
+def test_anyprec_partition_respects_each_stream_type(mode):
+    """Every any-precision mode partitions like the others, with 16-byte
+    aligned vector chunks under its own element sizes, whatever the skew of
+    each base (a skew no head can fix sends the tensor down the element
+    path)."""
+    sizes = [1, 9, 4095, 65537, 0, 257, 1 << 20]
+    for skew in ((0, 0, 0, 0, 0), (1, 0, 0, 0, 0), (0, 3, 1, 1, 1), (5, 5, 5, 5, 5)):
+        es = ELEM_SIZES[mode]
+        entries = [_fake(i << 30, n, mode, skew) for i, n in enumerate(sizes)]
+        if es[4] == 0:
+            entries = [e[:4] + (0,) + e[5:] for e in entries]
+        for grid in (1, 7, 456):
+            _check_partition(entries, mode, grid)
+
+
+def test_anyprec_mode_validation():
+    """Modes 16..27 are valid except 28..31 (fp32 compensation without Kahan
+    summation); 5..15 and 32 are not modes; an fp32 buffer must be 4-byte
+    aligned; without Kahan summation aux may be NULL."""
+    for mode in list(range(5, 16)) + [28, 29, 30, 31, 32, -1]:
+        with pytest.raises(A.AdamWError) as e:
+            A.adamw_plan_chunks([_fake(0, 10, 0)], mode, 2)
+        assert e.value.status == A.ADAMW_ERR_INVALID_ARG, mode
+    assert len(A.ANYPREC_MODES) == 12
+    for mode in A.ANYPREC_MODES:
+        es = ELEM_SIZES[mode]
+        ent = _fake(0, 10, mode)
+        if es[4] == 0:
+            ent = ent[:4] + (0,) + ent[5:]
+        assert len(A.adamw_plan_chunks([ent], mode, 2)) >= 1
+        for s in (2, 3, 4):
+            if es[s] == 4:
+                bad = list(ent)
+                bad[s] += 2
+                with pytest.raises(A.AdamWError) as e:
+                    A.adamw_plan_chunks([tuple(bad)], mode, 2)
+                assert e.value.status == A.ADAMW_ERR_MISALIGNED
+
+
+def test_buffer_dtypes_follow_the_flags():
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    assert A.buffer_dtypes(A.MODE_ANYPREC) == A.buffer_dtypes(A.MODE_BF16_KAHAN)
+    assert A.buffer_dtypes(A.MODE_ANYPREC | A.ANYPREC_NO_KAHAN) == A.buffer_dtypes(A.MODE_BF16_PLAIN)
+    assert A.buffer_dtypes(A.MODE_ANYPREC | A.ANYPREC_V_FP32) == A.buffer_dtypes(A.MODE_BF16_KAHAN_FP32_VAR)
+    assert A.buffer_dtypes(A.MODE_ANYPREC | 7) == (bf, bf, f32, f32, f32)
+    assert A.buffer_dtypes(A.MODE_ANYPREC | 9) == (bf, bf, f32, bf, None)
+    with pytest.raises(ValueError):
+        A.buffer_dtypes(A.MODE_ANYPREC | 12)
 
 
 def test_opt_1_3b_partition():

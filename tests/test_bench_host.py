@@ -107,3 +107,14 @@ def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1"])
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_every_storage_mode_has_a_name_and_a_byte_count():
+    for mode in list(range(5)) + list(W.ANYPREC_MODES):
+        name, storage = bench.mode_name(mode)
+        assert name and storage
+        w = W.Workload("x", mode, (W.TensorSpec("a", 8),), 1, lr=1e-3, beta1=0.9, beta2=0.95,
+                       eps=1e-8, weight_decay=0.0)
+        assert 14 <= bench.bytes_per_param(w) <= 30
+    assert bench.bytes_per_param(W.WORKLOADS["opt1.3b_anyprec_fp32_state"]) == 30
+    assert bench.mode_name(W.MODE_ANYPREC | 9)[1] == "bf16 p/g, fp32 m, bf16 v, no compensation"
