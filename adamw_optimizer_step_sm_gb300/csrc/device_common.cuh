@@ -154,17 +154,48 @@ __device__ __forceinline__ float mixed_x1(const StepScalars& s, float coef, floa
 
 // ------------------------------------------------------- chunk walkers ----
 
-// Vectors per thread in flight per stream, and the CTAs per SM the update
-// kernel's register budget is fitted to (0: no constraint).
-#ifndef ADAMW_UNROLL
-#define ADAMW_UNROLL 2
+// Per storage mode: U, the 16-byte vectors each thread has in flight per
+// stream, and B, the resident CTAs per SM the update kernel's register budget
+// is fitted to (0: no constraint).  Chosen by measurement on GB300 over the
+// OPT-1.3b list (every mode at U = 1..3 and B = none, 2, 3, 4): the modes
+// with fp32 streams favour fewer vectors and more CTAs (or the reverse)
+// according to their mix of 2- and 4-byte streams.  ADAMW_UNROLL and
+// ADAMW_MIN_BLOCKS, when defined, override the table for every mode.
+template <int MODE>
+struct UpdateTuning {
+    static constexpr int kU =
+        MODE == ADAMW_MODE_MIXED_FP32_MASTER ? 1
+        : MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR ? 1
+        : MODE == (ADAMW_MODE_ANYPREC | 1) ? 1
+        : MODE == (ADAMW_MODE_ANYPREC | 3) ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 4) ? 1
+        : MODE == (ADAMW_MODE_ANYPREC | 5) ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 6) ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 7) ? 1
+        : MODE == (ADAMW_MODE_ANYPREC | 11) ? 3
+        : 2;
+    static constexpr int kB =
+        MODE == ADAMW_MODE_MIXED_FP32_MASTER ? 2
+        : MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 1) ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 3) ? 2
+        : MODE == (ADAMW_MODE_ANYPREC | 4) ? 3
+        : MODE == (ADAMW_MODE_ANYPREC | 7) ? 2
+        : MODE == (ADAMW_MODE_ANYPREC | 11) ? 2
+        : 0;
+#ifdef ADAMW_UNROLL
+    static constexpr int kUnroll = ADAMW_UNROLL;
+#else
+    static constexpr int kUnroll = kU;
 #endif
-#ifndef ADAMW_MIN_BLOCKS
-#define ADAMW_MIN_BLOCKS 0
+#ifdef ADAMW_MIN_BLOCKS
+    static constexpr int kMinBlocks = ADAMW_MIN_BLOCKS;
+#else
+    static constexpr int kMinBlocks = kB;
 #endif
-constexpr int kUnroll = ADAMW_UNROLL;
+};
 
-template <int K>
+template <int K, int U>
 __device__ __forceinline__ void kahan_vec_chunk(const ChunkPtr& t, int64_t len,
                                                 const StepScalars& s, float coef, bool& bad) {
     uint16_t* p = static_cast<uint16_t*>(t.p);
@@ -173,10 +204,10 @@ __device__ __forceinline__ void kahan_vec_chunk(const ChunkPtr& t, int64_t len,
     uint16_t* v = static_cast<uint16_t*>(t.v);
     uint16_t* c = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll], C[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U], P[U], M[U], V[U], C[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -187,7 +218,7 @@ __device__ __forceinline__ void kahan_vec_chunk(const ChunkPtr& t, int64_t len,
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 if (K == kReport)
@@ -245,7 +276,7 @@ __device__ __forceinline__ void st32(float* p, const F8& v) {
                            __float_as_uint(v.x[6]), __float_as_uint(v.x[7])));
 }
 
-template <int K>
+template <int K, int U>
 __device__ __forceinline__ void mixed_vec_chunk(const ChunkPtr& t, int64_t len,
                                                 const StepScalars& s, float coef, bool& bad) {
     float* p = static_cast<float*>(t.p);
@@ -254,11 +285,11 @@ __device__ __forceinline__ void mixed_vec_chunk(const ChunkPtr& t, int64_t len,
     float* v = static_cast<float*>(t.v);
     uint16_t* o = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll];
-        F8 P[kUnroll], M[kUnroll], V[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U];
+        F8 P[U], M[U], V[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -268,7 +299,7 @@ __device__ __forceinline__ void mixed_vec_chunk(const ChunkPtr& t, int64_t len,
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
@@ -365,7 +396,7 @@ __device__ __forceinline__ void kahan_v32_x1(const StepScalars& s, float coef, f
     ch = to_bf16(__fsub_rn(y, __fsub_rn(from_bf16(ph), p0)));
 }
 
-template <int K>
+template <int K, int U>
 __device__ __forceinline__ void plain_vec_chunk(const ChunkPtr& t, int64_t len,
                                                 const StepScalars& s, float coef, bool& bad) {
     uint16_t* p = static_cast<uint16_t*>(t.p);
@@ -373,10 +404,10 @@ __device__ __forceinline__ void plain_vec_chunk(const ChunkPtr& t, int64_t len,
     uint16_t* m = static_cast<uint16_t*>(t.m);
     uint16_t* v = static_cast<uint16_t*>(t.v);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll], P[kUnroll], M[kUnroll], V[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U], P[U], M[U], V[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -386,7 +417,7 @@ __device__ __forceinline__ void plain_vec_chunk(const ChunkPtr& t, int64_t len,
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 if (K == kReport)
@@ -427,7 +458,7 @@ __device__ __forceinline__ void plain_elem_chunk(const ChunkPtr& t, int64_t len,
     }
 }
 
-template <int K>
+template <int K, int U>
 __device__ __forceinline__ void kahan_v32_vec_chunk(const ChunkPtr& t, int64_t len,
                                                     const StepScalars& s, float coef, bool& bad) {
     uint16_t* p = static_cast<uint16_t*>(t.p);
@@ -436,11 +467,11 @@ __device__ __forceinline__ void kahan_v32_vec_chunk(const ChunkPtr& t, int64_t l
     float* v = static_cast<float*>(t.v);
     uint16_t* c = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll], P[kUnroll], M[kUnroll], C[kUnroll];
-        F8 V[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U], P[U], M[U], C[U];
+        F8 V[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -451,7 +482,7 @@ __device__ __forceinline__ void kahan_v32_vec_chunk(const ChunkPtr& t, int64_t l
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
@@ -621,7 +652,7 @@ __device__ __forceinline__ void anyprec_one(const ChunkPtr& t, int64_t i, const 
     if (kKahan) st1<kC32>(t.a, i, c);
 }
 
-template <int FLAGS, int K>
+template <int FLAGS, int K, int U>
 __device__ __forceinline__ void anyprec_vec_chunk(const ChunkPtr& t, int64_t len,
                                                   const StepScalars& s, float coef, bool& bad) {
     constexpr bool kM32 = (FLAGS & ADAMW_ANYPREC_M_FP32) != 0;
@@ -631,13 +662,13 @@ __device__ __forceinline__ void anyprec_vec_chunk(const ChunkPtr& t, int64_t len
     uint16_t* p = static_cast<uint16_t*>(t.p);
     const uint16_t* g = static_cast<const uint16_t*>(t.g);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll], P[kUnroll];
-        Raw8<kM32> M[kUnroll];
-        Raw8<kV32> V[kUnroll];
-        Raw8<kC32> C[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U], P[U];
+        Raw8<kM32> M[U];
+        Raw8<kV32> V[U];
+        Raw8<kC32> C[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -648,7 +679,7 @@ __device__ __forceinline__ void anyprec_vec_chunk(const ChunkPtr& t, int64_t len
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
@@ -701,7 +732,7 @@ __device__ __forceinline__ void split_master(float x, uint32_t& hi16, uint32_t& 
     rem16 = (u - (hi16 << 16)) & 0xffffu;
 }
 
-template <int K>
+template <int K, int U>
 __device__ __forceinline__ void remainder_vec_chunk(const ChunkPtr& t, int64_t len,
                                                     const StepScalars& s, float coef, bool& bad) {
     uint16_t* p = static_cast<uint16_t*>(t.p);
@@ -710,11 +741,11 @@ __device__ __forceinline__ void remainder_vec_chunk(const ChunkPtr& t, int64_t l
     float* v = static_cast<float*>(t.v);
     uint16_t* r = static_cast<uint16_t*>(t.a);
     const int64_t nvec = len / kVec;
-    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * kUnroll) {
-        uint4 G[kUnroll], P[kUnroll], R[kUnroll];
-        F8 M[kUnroll], V[kUnroll];
+    for (int64_t base = threadIdx.x; base < nvec; base += int64_t(kBlock) * U) {
+        uint4 G[U], P[U], R[U];
+        F8 M[U], V[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 G[u] = ld16(g + i * kVec);
@@ -725,7 +756,7 @@ __device__ __forceinline__ void remainder_vec_chunk(const ChunkPtr& t, int64_t l
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t i = base + int64_t(u) * kBlock;
             if (i < nvec) {
                 const uint32_t gw[4] = {G[u].x, G[u].y, G[u].z, G[u].w};
@@ -791,11 +822,7 @@ __device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t 
 }
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
-#if ADAMW_MIN_BLOCKS > 0
-#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock, ADAMW_MIN_BLOCKS)
-#else
-#define ADAMW_UPDATE_BOUNDS __launch_bounds__(kBlock)
-#endif
+#define ADAMW_UPDATE_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kMinBlocks)
 
 // One chunk descriptor, read through the read-only path.
 __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
@@ -817,6 +844,7 @@ template <int MODE, int K>
 __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                            int32_t c1, const StepScalars& s, float coef,
                                            bool& bad) {
+    constexpr int kU = UpdateTuning<MODE>::kUnroll;
     ChunkPtr cur;
     if (c0 < c1) cur = load_chunk(chunks + c0);
     for (int32_t ci = c0; ci < c1; ++ci) {
@@ -825,23 +853,23 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
         const int64_t len = cur.len2 >> 1;
         const bool vec = cur.len2 & 1;
         if constexpr (MODE == ADAMW_MODE_BF16_KAHAN) {
-            if (vec) kahan_vec_chunk<K>(cur, len, s, coef, bad);
+            if (vec) kahan_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else kahan_elem_chunk<K>(cur, len, s, coef, bad);
         } else if constexpr (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
-            if (vec) mixed_vec_chunk<K>(cur, len, s, coef, bad);
+            if (vec) mixed_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else mixed_elem_chunk<K>(cur, len, s, coef, bad);
         } else if constexpr (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
-            if (vec) remainder_vec_chunk<K>(cur, len, s, coef, bad);
+            if (vec) remainder_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else remainder_elem_chunk<K>(cur, len, s, coef, bad);
         } else if constexpr (MODE == ADAMW_MODE_BF16_PLAIN) {
-            if (vec) plain_vec_chunk<K>(cur, len, s, coef, bad);
+            if (vec) plain_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else plain_elem_chunk<K>(cur, len, s, coef, bad);
         } else if constexpr (MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR) {
-            if (vec) kahan_v32_vec_chunk<K>(cur, len, s, coef, bad);
+            if (vec) kahan_v32_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
         } else {
             constexpr int kFlags = MODE & ~ADAMW_MODE_ANYPREC;
-            if (vec) anyprec_vec_chunk<kFlags, K>(cur, len, s, coef, bad);
+            if (vec) anyprec_vec_chunk<kFlags, K, kU>(cur, len, s, coef, bad);
             else anyprec_elem_chunk<kFlags, K>(cur, len, s, coef, bad);
         }
         cur = nxt;

@@ -11,7 +11,7 @@ namespace {
 // DEV: the scalars, clip coefficient and skip decision come from the
 // StepRecord the device-resident step path's prologue wrote.
 template <int MODE, int K, bool DEV>
-__global__ void ADAMW_UPDATE_BOUNDS
+__global__ void ADAMW_UPDATE_BOUNDS(MODE)
 adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
                     const NormOut* __restrict__ norm, int32_t* __restrict__ report,
@@ -40,7 +40,7 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
 // the non-finite flag, so no CTA can read a counter that was already
 // advanced.  Invalid hyperparameters: nothing is updated, the flag is -1.
 template <int MODE, int K>
-__global__ void ADAMW_UPDATE_BOUNDS
+__global__ void ADAMW_UPDATE_BOUNDS(MODE)
 adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
                          const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
                          unsigned int* __restrict__ done, int32_t* __restrict__ flagword,
@@ -76,7 +76,7 @@ adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
 }
 
 template <int MODE>
-__global__ void ADAMW_UPDATE_BOUNDS
+__global__ void ADAMW_UPDATE_BOUNDS(MODE)
 adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         const int32_t* __restrict__ upd_begin,
                         const ChunkPtr* __restrict__ nrm_chunks,

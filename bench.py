@@ -60,6 +60,22 @@ def bytes_per_param(w: W.Workload) -> int:
     return base + (2 if w.max_grad_norm > 0 else 0)
 
 
+def workload_of(args) -> W.Workload:
+    """The named workload, in the storage mode --mode asks for (renamed
+    <list>_mode<N>, same tensors, hyperparameters and inputs)."""
+    w = W.WORKLOADS[args.workload]
+    mode = getattr(args, "mode", None)
+    if mode is None or mode == w.mode:
+        return w
+    if mode not in W.MODE_DTYPES:
+        raise SystemExit(f"unknown storage mode {mode}")
+    import dataclasses
+    base = w.name.split("_")[0]
+    return dataclasses.replace(w, name=f"{base}_mode{mode}", mode=mode,
+                               description=f"{w.description}; run in storage mode {mode} "
+                                           f"({mode_name(mode)[1]})")
+
+
 def mode_name(mode: int) -> tuple[str, str]:
     """Name and buffer layout of a storage mode, for the JSON line."""
     named = {0: ("bf16_kahan", "bf16 p/g/m/v/c"),
@@ -413,7 +429,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     A.load()
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     from dataclasses import replace
     w_bench = replace(w, inf_at=None)   # timing steps carry no injected inf
     clip = w.max_grad_norm > 0
@@ -577,7 +593,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     thr = host_threads()
     n = min(args.ref_sample, w.total)
     oracle_throughput(w, min(n, 1 << 20), max(1, min(args.warmup, 3)), thr)  # warm-up
@@ -610,6 +626,9 @@ def main(argv=None):
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--no-fuse", action="store_true",
                     help="run clipped steps as three launches even where one fused launch fits")
+    ap.add_argument("--mode", type=int, default=None,
+                    help="run the workload's tensor list in another storage mode (0-4, or "
+                         "16 + any-precision flags)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed steps
     if args.impl == "reference":

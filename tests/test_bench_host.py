@@ -118,3 +118,13 @@ def test_every_storage_mode_has_a_name_and_a_byte_count():
         assert 14 <= bench.bytes_per_param(w) <= 30
     assert bench.bytes_per_param(W.WORKLOADS["opt1.3b_anyprec_fp32_state"]) == 30
     assert bench.mode_name(W.MODE_ANYPREC | 9)[1] == "bf16 p/g, fp32 m, bf16 v, no compensation"
+
+
+def test_mode_override_keeps_the_list_and_renames_the_workload():
+    import argparse
+    a = argparse.Namespace(workload="opt1.3b_bf16_kahan", mode=W.MODE_ANYPREC | 7)
+    w = bench.workload_of(a)
+    base = W.WORKLOADS["opt1.3b_bf16_kahan"]
+    assert w.name == "opt1.3b_mode23" and w.mode == 23 and w.tensors == base.tensors
+    assert w.hparams() == base.hparams() and bench.bytes_per_param(w) == 30
+    assert bench.workload_of(argparse.Namespace(workload="opt1.3b_bf16_kahan", mode=None)) is base
