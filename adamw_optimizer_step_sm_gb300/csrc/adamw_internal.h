@@ -56,15 +56,28 @@ struct alignas(16) ChunkPtr {
 };
 static_assert(sizeof(ChunkPtr) == 48, "chunk layout");
 
-// Elements per round-robin tile of the interleaved partition of the update
-// kernel (measured on GB300: round-robin tiles beat contiguous per-CTA ranges
-// by ~6 % on the 1.3B-parameter list, because the whole grid then streams one
-// narrow window of each buffer; 8192 is 1 % faster than 16384 and 32768).  Lists with fewer than two tiles per CTA, and the
+// Nominal elements per round-robin tile of the interleaved partition of the
+// update kernel (measured on GB300: round-robin tiles beat contiguous per-CTA
+// ranges by ~6 % on the 1.3B-parameter list, because the whole grid then
+// streams one narrow window of each buffer; 8192 is 1 % faster than 16384 and
+// 32768).  The tile actually used is stretched so that every CTA gets the
+// same number of tiles.  Lists with fewer than two tiles per CTA, and the
 // read-only norm pass, use contiguous ranges.
 #ifndef ADAMW_TILE_ELEMS
 #define ADAMW_TILE_ELEMS 8192
 #endif
+// 1: tiles cut in the flattened list and stretched so every CTA gets the
+// same number (cuts inside a tensor at multiples of ADAMW_CUT_ALIGN elements
+// from its vector body's start); 0: fixed tiles cut per tensor.
+#ifndef ADAMW_TILE_BALANCE
+#define ADAMW_TILE_BALANCE 1
+#endif
+#ifndef ADAMW_CUT_ALIGN
+#define ADAMW_CUT_ALIGN 2048
+#endif
 constexpr int64_t kTileElems = ADAMW_TILE_ELEMS;
+constexpr int64_t kCutAlign = ADAMW_CUT_ALIGN;
+static_assert(kCutAlign % kVec == 0 && kTileElems % kCutAlign == 0, "tile cut alignment");
 
 // Output of the norm finalize kernel, read by the clipped update.
 struct NormOut {
@@ -137,7 +150,9 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
 int32_t choose_grid(int64_t total, int32_t max_grid);
 
 // Tile size of the update kernel's partition for a list of `total` elements
-// on `grid` CTAs (0: contiguous ranges).
+// on `grid` CTAs (0: contiguous ranges): the multiple of kVec nearest above
+// total / (k * grid), k = the whole number of kTileElems tiles per CTA
+// nearest to total / (grid * kTileElems).
 int64_t update_tile_elems(int64_t total, int32_t grid);
 
 // Every buffer the mode uses can be dereferenced by `device` (device_access.cpp).

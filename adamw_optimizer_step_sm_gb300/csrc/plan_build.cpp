@@ -157,7 +157,18 @@ int32_t choose_grid(int64_t total, int32_t max_grid) {
 
 int64_t update_tile_elems(int64_t total, int32_t grid) {
     if (kTileElems <= 0 || grid <= 0) return 0;
-    return (total >= 2 * int64_t(grid) * kTileElems) ? kTileElems : 0;
+    if (total < 2 * int64_t(grid) * kTileElems) return 0;
+    // k tiles per CTA, k the nearest whole number to total / (grid * tile);
+    // the tile then stretches (or shrinks) so that k * grid tiles cover the
+    // list: every CTA gets k tiles, and no CTA a (k+1)-th one.
+#if ADAMW_TILE_BALANCE
+    const int64_t per_row = int64_t(grid) * kTileElems;
+    const int64_t k = (total + per_row / 2) / per_row;
+    const int64_t t = (total + k * grid - 1) / (k * grid);
+    return (t + kCutAlign - 1) / kCutAlign * kCutAlign;
+#else
+    return kTileElems;
+#endif
 }
 
 int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
@@ -193,11 +204,10 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
     P.cta_begin.assign(size_t(grid) + 1, 0);
     if (P.total == 0) return ADAMW_OK;
 
+#if !ADAMW_TILE_BALANCE
     if (tile_elems > 0) {
-        // Interleaved: cut every segment into tiles of tile_elems (a multiple
-        // of kVec, so vector tiles stay 16-byte aligned) and deal the tiles
-        // round-robin to the CTAs in list order, so that at any moment the
-        // whole grid streams one narrow window of each buffer.
+        // Interleaved, fixed tiles: cut every segment into tiles of
+        // tile_elems and deal the tiles round-robin to the CTAs in list order.
         std::vector<ChunkDev> pieces;
         for (const Seg& s : segs)
             for (int64_t pos = 0; pos < s.len; pos += tile_elems)
@@ -211,6 +221,53 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
         std::vector<int64_t> fill(count.begin(), count.end() - 1);
         for (size_t j = 0; j < pieces.size(); ++j) {
             const int32_t b = int32_t(j % grid);
+            P.chunks[fill[b]] = pieces[j];
+            P.chunk_cta[fill[b]] = b;
+            ++fill[b];
+        }
+        for (int32_t b = 0; b <= grid; ++b) P.cta_begin[b] = int32_t(count[b]);
+        return ADAMW_OK;
+    }
+#endif
+    if (tile_elems > 0) {
+        // Interleaved: cut the flattened list (all segments in order) into
+        // tiles of tile_elems and deal them round-robin to the CTAs, so that
+        // at any moment the whole grid streams one narrow window of each
+        // buffer.  A tile that spans a tensor boundary is several chunks of
+        // one CTA.  A cut inside a vector body moves up to the next multiple
+        // of kCutAlign elements from the body's start (a whole number of
+        // 16-byte vectors; coarser alignment keeps warps' accesses on whole
+        // cache lines) and the next tile is shorter by as much.
+        std::vector<ChunkDev> pieces;
+        std::vector<int32_t> owner;
+        int64_t flat = 0, boundary = tile_elems, tile = 0;
+        for (const Seg& s : segs) {
+            int64_t pos = 0;
+            while (pos < s.len) {
+                int64_t take = s.len - pos;
+                if (take > boundary - flat) {
+                    take = boundary - flat;
+                    if (s.vec) take = (pos + take + kCutAlign - 1) / kCutAlign * kCutAlign - pos;
+                    if (take > s.len - pos) take = s.len - pos;
+                }
+                pieces.push_back({s.k, s.vec, s.off + pos, take});
+                owner.push_back(int32_t(tile % grid));
+                pos += take;
+                flat += take;
+                while (flat >= boundary) {
+                    ++tile;
+                    boundary += tile_elems;
+                }
+            }
+        }
+        std::vector<int64_t> count(size_t(grid) + 1, 0);
+        for (int32_t b : owner) ++count[size_t(b) + 1];
+        for (int32_t b = 0; b < grid; ++b) count[b + 1] += count[b];
+        P.chunks.resize(pieces.size());
+        P.chunk_cta.resize(pieces.size());
+        std::vector<int64_t> fill(count.begin(), count.end() - 1);
+        for (size_t j = 0; j < pieces.size(); ++j) {
+            const int32_t b = owner[j];
             P.chunks[fill[b]] = pieces[j];
             P.chunk_cta[fill[b]] = b;
             ++fill[b];
