@@ -206,6 +206,25 @@ def test_ragged_lists(mode, clip, layout):
     assert rep.exact == rep.n
 
 
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_MIXED, 0.5),
+                                       (W.MODE_ANYPREC | 7, 0.0), (W.MODE_BF16_PLAIN, 0.5)])
+@pytest.mark.parametrize("layout", [(8, 0), (1, 3)])
+def test_interleaved_partition_over_ragged_tensors(mode, clip, layout):
+    """A list long enough for the interleaved partition (at least two tiles
+    per CTA) made of ragged tensors: tiles span tensor boundaries, cuts fall
+    inside tensors, and with the skewed layout every tensor has an
+    element-path head before its vector body.  Every element checked."""
+    sizes = [3_000_001, 7, 2_500_003, 65_537, 1_999_999, 1, 4_194_304, 257, 1_048_583, 9]
+    w = _small("interleaved", mode=mode, sizes=sizes, max_grad_norm=clip, steps=3)
+    gpu = H.GpuSide(w)
+    info = gpu.plan.info
+    assert info.n_chunks >= 2 * info.grid, "list too short for the interleaved partition"
+    gpu.plan.close()
+    rep, log = H.run_parity(w, align_elems=layout[0], skew=layout[1])
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
 @pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
 def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     w = _small("skip", mode=mode, max_grad_norm=1.0, inf_at=(2, 8, 777), steps=4)
