@@ -5,10 +5,12 @@ Tolerances (checked in ``compare``):
   * bf16 state (p, m, v, c, bf16 param out): at most 1 bf16 ulp apart; NaN
     only where the other side has NaN;
   * fp32 state (master, m, v): relative error <= 1e-6, with an absolute floor
-    of 1e-6 * max|x| of the tensor for values near zero;
+    of 1e-6 * max|x| of the finite values of the tensor for values near
+    zero; NaN and +-inf at the same places on both sides;
   * the non-finite flag: identical.
 Both sides evaluate the same fp32 operation sequence, so the results are
-expected to be bit-identical; the report counts exact matches.
+expected to be bit-identical; the report counts exact matches (a NaN on both
+sides counts as a match whatever its payload).
 """
 from __future__ import annotations
 
@@ -96,16 +98,22 @@ def compare(rep: Report, name: str, gpu: np.ndarray, ref: np.ndarray):
     else:
         g64, r64 = gpu.astype(np.float64), ref.astype(np.float64)
         nan_g, nan_r = np.isnan(g64), np.isnan(r64)
-        ok = ~(nan_g | nan_r)
+        # infinities must sit at the same places with the same sign
+        inf_g, inf_r = np.isinf(g64), np.isinf(r64)
+        inf_ok = np.array_equal(inf_g, inf_r) and np.array_equal(g64[inf_g], r64[inf_r])
+        ok = ~(nan_g | nan_r | inf_g | inf_r)
         floor = 1e-6 * (np.max(np.abs(r64[ok])) if ok.any() else 0.0)
         err = np.abs(g64[ok] - r64[ok])
         tol = 1e-6 * np.abs(r64[ok]) + floor
         rel = float(np.max(err / np.maximum(np.abs(r64[ok]), floor if floor > 0 else 1e-300))) if err.size else 0.0
         rep.max_rel = max(rep.max_rel, rel)
         rep.n += gpu.size
-        rep.exact += int(np.sum(gpu.view(np.uint32) == ref.view(np.uint32)))
-        if not np.array_equal(nan_g, nan_r) or np.any(err > tol):
-            rep.failures.append(f"{name}: max rel {rel:.3g} beyond 1e-6 (or NaN mismatch)")
+        # a NaN's payload and sign are not part of the result (IEEE leaves the
+        # payload of a generated NaN open; x86, Arm and CUDA differ): NaN
+        # pairs count as matching, as in the bf16 comparison
+        rep.exact += int(np.sum((gpu.view(np.uint32) == ref.view(np.uint32)) | (nan_g & nan_r)))
+        if not np.array_equal(nan_g, nan_r) or not inf_ok or np.any(err > tol):
+            rep.failures.append(f"{name}: max rel {rel:.3g} beyond 1e-6 (or NaN / inf mismatch)")
 
 
 # -------------------------------------------------------------- the GPU side --
