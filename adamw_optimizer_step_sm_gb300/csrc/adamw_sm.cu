@@ -10,9 +10,10 @@
 // with about twenty fp32 operations in between.
 // That is far below the GPU's ridge point, so HBM bandwidth bounds it and the
 // kernels are built to keep DRAM streaming: a persistent grid (SMs x resident
-// CTAs) dealt 8K-element tiles of the flattened parameter space round-robin
-// (so the grid sweeps every buffer together), chunk descriptors prefetched one
-// ahead, 16-byte vector loads issued U vectors ahead of the arithmetic, fp32
+// CTAs) dealt tiles of about 8K elements of the flattened parameter space,
+// cut on 2048-element boundaries, round-robin (so the grid sweeps every
+// buffer together), chunk descriptors prefetched one ahead, 16-byte vector
+// loads issued U vectors ahead of the arithmetic (U per storage mode), fp32
 // math, 16-byte stores.  No tensor cores: nothing here is a contraction.
 //
 // Sources of the method: "[pure bf16 training] w/ AnyPrecisionAdamW and Kahan

@@ -2,7 +2,7 @@
  * adamw_sm.h -- C ABI of the GB300 (sm_103a) AdamW optimizer-step library.
  *
  * One optimizer step of decoupled-weight-decay Adam with bias correction over
- * a list of parameter tensors, in one of two storage modes:
+ * a list of parameter tensors, in one of these storage modes:
  *
  *   ADAMW_MODE_BF16_KAHAN  pure-bf16 AnyPrecisionAdamW with Kahan summation:
  *       bf16 param p, grad g, exp_avg m, exp_avg_sq v and compensation c.
@@ -43,7 +43,7 @@
  *       ADAMW_MODE_BF16_KAHAN, ADAMW_MODE_BF16_KAHAN_FP32_VAR and
  *       ADAMW_MODE_BF16_PLAIN and run those modes' kernels.
  *
- * Arithmetic (identical in both modes up to storage; fp32, one IEEE
+ * Arithmetic (identical in every mode up to storage; fp32, one IEEE
  * round-to-nearest per operation, no fused multiply-add):
  *   host, fp64 rounded once to fp32:  step_size = lr / (1 - beta1^t),
  *       sbc2 = sqrt(1 - beta2^t), omb1 = 1 - beta1, omb2 = 1 - beta2,
