@@ -1,0 +1,223 @@
+"""``AnyPrecisionAdamW``: a ``torch.optim.Optimizer`` whose step is one call
+into the adamw_sm library (``adamw_step_device``) per parameter group.
+
+It takes the options the pure-bf16 recipe passes to its optimizer ("[pure
+bf16 training] w/ AnyPrecisionAdamW and Kahan summation", "Train from
+scratch": ``--optim adamw_anyprecision --optim_args 'use_kahan_summation=true,
+momentum_dtype=bfloat16, variance_dtype=bfloat16,
+compensation_buffer_dtype=bfloat16'`` with ``--learning_rate 0.0002
+--adam_beta1 0.9 --adam_beta2 0.95 --weight_decay 0.1``); those values are the
+defaults here.  Parameters are bf16 CUDA tensors; each of the three optimizer
+buffers may be bf16 or fp32, and Kahan summation on or off (the library's
+``ADAMW_MODE_ANYPREC`` storage modes).  ``max_grad_norm > 0`` clips by the
+global norm of the group's gradients inside the step and skips a step whose
+gradients hold inf or NaN (no state written, counter not advanced);
+``track_grad_norm`` reports the norm without clipping (one more read of the
+gradients).
+
+Layout: the optimizer owns one flat buffer per kind (gradient, exp_avg,
+exp_avg_sq, compensation) for each group, every tensor at a 2048-element
+boundary, and points each ``p.grad`` at its slice of the gradient buffer;
+``zero_grad`` zeroes that buffer in place (it never sets gradients to None),
+so backward passes accumulate straight into it and a step copies nothing.
+A gradient found elsewhere at step time (the first step, or a ``p.grad``
+assigned by the caller) is copied in once and re-pointed.  The step counter
+and the hyperparameters live in device memory, so ``step`` never waits for
+the GPU; ``last_grad_norm`` and ``last_nonfinite`` are device tensors.
+
+Every parameter of a group is stepped on every call: a parameter whose
+``p.grad`` is None is an error (a zero gradient still decays the moments and
+the weight, which is not what skipping a parameter means).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import adamw_sm as A
+
+# Each tensor of a group starts at a multiple of this many elements in the
+# group's flat buffers (4 KB of a bf16 stream), the boundaries the library's
+# partition cuts tiles on.
+_ALIGN = 2048
+
+_DTYPES = {torch.bfloat16: False, torch.float32: True}
+
+
+def storage_mode(use_kahan_summation: bool, momentum_dtype: torch.dtype,
+                 variance_dtype: torch.dtype, compensation_buffer_dtype: torch.dtype) -> int:
+    """The library's storage mode for AnyPrecisionAdamW's options."""
+    for name, dt in (("momentum_dtype", momentum_dtype), ("variance_dtype", variance_dtype),
+                     ("compensation_buffer_dtype", compensation_buffer_dtype)):
+        if dt not in _DTYPES:
+            raise ValueError(f"{name} must be torch.bfloat16 or torch.float32, not {dt}")
+    flags = (A.ANYPREC_M_FP32 if _DTYPES[momentum_dtype] else 0) \
+        | (A.ANYPREC_V_FP32 if _DTYPES[variance_dtype] else 0)
+    if use_kahan_summation:
+        flags |= A.ANYPREC_C_FP32 if _DTYPES[compensation_buffer_dtype] else 0
+    else:
+        flags |= A.ANYPREC_NO_KAHAN
+    return A.MODE_ANYPREC | flags
+
+
+class _GroupBuffers:
+    """A group's flat buffers, views, plan and device-side step state."""
+
+    def __init__(self, params, mode: int):
+        dts = A.buffer_dtypes(mode)
+        dev = params[0].device
+        numels = [p.numel() for p in params]
+        offs, n = [], 0
+        for k in numels:
+            offs.append(n)
+            n += -(-k // _ALIGN) * _ALIGN
+        n = max(n, 1)
+        flat = lambda dt: None if dt is None else torch.zeros(n, dtype=dt, device=dev)
+        self.grad, self.exp_avg, self.exp_avg_sq, self.comp = (flat(torch.bfloat16), flat(dts[2]),
+                                                              flat(dts[3]), flat(dts[4]))
+        view = lambda buf, p, o: None if buf is None else buf[o:o + p.numel()].view(p.shape)
+        self.grads = [view(self.grad, p, o) for p, o in zip(params, offs)]
+        self.exp_avgs = [view(self.exp_avg, p, o) for p, o in zip(params, offs)]
+        self.exp_avg_sqs = [view(self.exp_avg_sq, p, o) for p, o in zip(params, offs)]
+        self.comps = [view(self.comp, p, o) for p, o in zip(params, offs)]
+        self.plan = A.Plan(params, self.grads, self.exp_avgs, self.exp_avg_sqs,
+                           self.comps if self.comp is not None else None, mode, norm=True)
+        self.step = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.grad_norm = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.d_hp = torch.zeros(len(bytes(A.hparams())), dtype=torch.uint8, device=dev)
+        self.hp_key = None
+
+
+class AnyPrecisionAdamW(torch.optim.Optimizer):
+    def __init__(self, params, lr: float = 2e-4, betas=(0.9, 0.95), eps: float = 1e-8,
+                 weight_decay: float = 0.1, use_kahan_summation: bool = True,
+                 momentum_dtype: torch.dtype = torch.bfloat16,
+                 variance_dtype: torch.dtype = torch.bfloat16,
+                 compensation_buffer_dtype: torch.dtype = torch.bfloat16,
+                 max_grad_norm: float = 0.0, track_grad_norm: bool = False):
+        if not lr >= 0.0 or not eps > 0.0 or not weight_decay >= 0.0:
+            raise ValueError("want lr >= 0, eps > 0 and weight_decay >= 0")
+        if not (0.0 <= betas[0] < 1.0 and 0.0 <= betas[1] < 1.0):
+            raise ValueError("want betas in [0, 1)")
+        self.mode = storage_mode(use_kahan_summation, momentum_dtype, variance_dtype,
+                                 compensation_buffer_dtype)
+        self.track_grad_norm = track_grad_norm
+        defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
+                        max_grad_norm=max_grad_norm)
+        self._buffers: dict[int, _GroupBuffers] = {}
+        super().__init__(params, defaults)
+        for group in self.param_groups:
+            self._buffers_of(group)
+
+    # -- set-up -------------------------------------------------------------
+    def _buffers_of(self, group) -> _GroupBuffers:
+        key = id(group)
+        b = self._buffers.get(key)
+        if b is None:
+            params = group["params"]
+            if not params:
+                raise ValueError("empty parameter group")
+            dev = params[0].device
+            for p in params:
+                if not p.is_cuda or p.dtype != torch.bfloat16 or not p.is_contiguous() \
+                        or p.device != dev:
+                    raise TypeError("AnyPrecisionAdamW steps contiguous bf16 CUDA parameters "
+                                    "of one device")
+            with torch.cuda.device(dev):
+                b = _GroupBuffers(params, self.mode)
+            for k, (p, g) in enumerate(zip(params, b.grads)):
+                if p.grad is not None:
+                    g.copy_(p.grad)
+                p.grad = g
+                st = self.state[p]
+                st["exp_avg"] = b.exp_avgs[k]
+                st["exp_avg_sq"] = b.exp_avg_sqs[k]
+                if b.comp is not None:
+                    st["compensation"] = b.comps[k]
+                st["step"] = b.step
+            self._buffers[key] = b
+        return b
+
+    def add_param_group(self, param_group):
+        super().add_param_group(param_group)
+        if hasattr(self, "_buffers"):
+            self._buffers_of(self.param_groups[-1])
+
+    # -- the step -----------------------------------------------------------
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for group in self.param_groups:
+            b = self._buffers_of(group)
+            for k, (p, g) in enumerate(zip(group["params"], b.grads)):
+                if p.grad is None:
+                    raise RuntimeError(f"parameter {k} of a group has no gradient; "
+                                       "AnyPrecisionAdamW steps every parameter")
+                if p.grad.data_ptr() != g.data_ptr():
+                    g.copy_(p.grad)
+                    p.grad = g
+            beta1, beta2 = group["betas"]
+            key = (group["lr"], beta1, beta2, group["eps"], group["weight_decay"],
+                   group["max_grad_norm"])
+            if key != b.hp_key:
+                hp = A.hparams(lr=key[0], beta1=key[1], beta2=key[2], eps=key[3],
+                               weight_decay=key[4], max_grad_norm=key[5])
+                host = torch.frombuffer(bytearray(bytes(hp)), dtype=torch.uint8)
+                b.d_hp.copy_(host.pin_memory(), non_blocking=True)
+                b.hp_key = key
+            clip = group["max_grad_norm"] > 0
+            norm = clip or self.track_grad_norm
+            b.plan.step_device(b.d_hp, b.step, A.STEP_CLIP if clip else 0,
+                               grad_norm=b.grad_norm if norm else None, nonfinite=b.nonfinite)
+        return loss
+
+    def zero_grad(self, set_to_none: bool = True):
+        """Zeroes the gradient buffers in place; ``set_to_none`` is ignored
+        (the gradients stay views of the optimizer's buffer)."""
+        for group in self.param_groups:
+            b = self._buffers_of(group)
+            b.grad.zero_()
+            for p, g in zip(group["params"], b.grads):
+                p.grad = g
+
+    # -- observation and checkpoints ----------------------------------------
+    @property
+    def last_grad_norm(self) -> list[torch.Tensor]:
+        """Per group, the global gradient norm of the last step (fp64, device;
+        computed when clipping or with ``track_grad_norm``)."""
+        return [self._buffers_of(g).grad_norm for g in self.param_groups]
+
+    @property
+    def last_nonfinite(self) -> list[torch.Tensor]:
+        """Per group, 1 when the last step's gradients held inf or NaN, else 0
+        (int32, device).  With clipping on such a step wrote nothing and the
+        step counter stayed; without clipping the values went through."""
+        return [self._buffers_of(g).nonfinite for g in self.param_groups]
+
+    def load_state_dict(self, state_dict):
+        """Loads hyperparameters and state into this optimizer's own buffers
+        (values are copied, each in its buffer's type)."""
+        groups = state_dict["param_groups"]
+        if len(groups) != len(self.param_groups):
+            raise ValueError("loaded state has a different number of parameter groups")
+        saved = state_dict["state"]
+        for group, sg in zip(self.param_groups, groups):
+            if len(sg["params"]) != len(group["params"]):
+                raise ValueError("loaded state has a different group size")
+            for name in ("lr", "betas", "eps", "weight_decay", "max_grad_norm"):
+                if name in sg:
+                    group[name] = tuple(sg[name]) if name == "betas" else sg[name]
+            b = self._buffers_of(group)
+            for idx, p in zip(sg["params"], group["params"]):
+                s = saved.get(idx)
+                if s is None:
+                    continue
+                for name in ("exp_avg", "exp_avg_sq", "compensation"):
+                    if name in s and name in self.state[p]:
+                        self.state[p][name].copy_(s[name])
+                if "step" in s:
+                    b.step.copy_(torch.as_tensor(s["step"]).reshape(1))
+            b.hp_key = None

@@ -262,3 +262,22 @@ def test_lr_schedule_agrees_with_the_oracle(warmup, total):
         a = np.float32(A.adamw_lr_linear_warmup(np.float32(2e-4), t, warmup, total))
         b = np.float32(o.lr_linear_warmup(np.float32(2e-4), t, warmup, total))
         assert a.view(np.uint32) == b.view(np.uint32), (t, a, b)
+
+
+def test_optimizer_options_map_to_storage_modes():
+    import torch
+    from adamw_optimizer_step_sm_gb300 import optim as OPT
+    bf, f32 = torch.bfloat16, torch.float32
+    assert OPT.storage_mode(True, bf, bf, bf) == A.MODE_ANYPREC
+    assert OPT.storage_mode(True, f32, f32, f32) == A.MODE_ANYPREC | 7
+    assert OPT.storage_mode(False, f32, bf, f32) == A.MODE_ANYPREC | 9   # c type unused
+    assert all(OPT.storage_mode(k, m, v, c) in A.ANYPREC_MODES
+               for k in (True, False) for m in (bf, f32) for v in (bf, f32) for c in (bf, f32))
+    with pytest.raises(ValueError):
+        OPT.storage_mode(True, torch.float16, bf, bf)
+    with pytest.raises(ValueError):
+        OPT.AnyPrecisionAdamW([torch.zeros(2, dtype=bf)], lr=-1.0)
+    with pytest.raises(ValueError):
+        OPT.AnyPrecisionAdamW([torch.zeros(2, dtype=bf)], betas=(0.9, 1.0))
+    with pytest.raises(TypeError):   # parameters must be bf16 CUDA tensors
+        OPT.AnyPrecisionAdamW([torch.zeros(2, dtype=bf)])

@@ -1,0 +1,174 @@
+"""AnyPrecisionAdamW (the torch.optim front end) against the oracle: every
+step of its device-resident path bit-identical to the oracle's list step on
+the same bytes, for each buffer-type option, with clipping and a skipped
+step, with an LR scheduler, through real backward passes, and across a
+checkpoint."""
+import io
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import parity_harness as H
+from adamw_optimizer_step_sm_gb300 import optim as OPT
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(256, 96), (96,), (7,), (1000, 33), (1,), (4097,), (64, 64, 3)]
+OPTIONS = {
+    "recipe_bf16_kahan": dict(),
+    "fp32_state": dict(momentum_dtype=torch.float32, variance_dtype=torch.float32,
+                       compensation_buffer_dtype=torch.float32),
+    "fp32_momentum_no_kahan": dict(momentum_dtype=torch.float32, use_kahan_summation=False),
+    "fp32_variance": dict(variance_dtype=torch.float32),
+}
+
+
+def _params(seed=3):
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    return [(torch.randn(s, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            .requires_grad_() for s in SHAPES]
+
+
+def _grad(k, seed=5, inf_at=None):
+    gen = torch.Generator(device="cuda").manual_seed(seed * 1000 + k)
+    gs = [(torch.randn(s, generator=gen, device="cuda") * 1e-2).to(torch.bfloat16) for s in SHAPES]
+    if inf_at == k:
+        gs[3].view(-1)[77] = float("inf")
+    return gs
+
+
+class _OracleSide:
+    """The same parameters and state as host arrays, stepped by the oracle."""
+
+    def __init__(self, params, mode):
+        self.o = O.load()
+        self.mode = mode
+        dm, dv, dc = O.anyprec_dtypes(mode - O.ANYPREC)
+        self.p = [H.to_u16(p.detach()).reshape(-1).copy() for p in params]
+        self.m = [np.zeros(p.numel(), dm) for p in params]
+        self.v = [np.zeros(p.numel(), dv) for p in params]
+        self.c = [None if dc is None else np.zeros(p.numel(), dc) for p in params]
+        self.t = 0
+
+    def step(self, grads, hp):
+        gs = [H.to_u16(g).reshape(-1).copy() for g in grads]
+        tens = [(p, g, m, v, c) for p, g, m, v, c in zip(self.p, gs, self.m, self.v, self.c)]
+        skipped, norm = self.o.list_step(tens, self.mode, hp, self.t + 1)
+        if not skipped:
+            self.t += 1
+        return skipped, norm
+
+    def check(self, opt, params):
+        for k, p in enumerate(params):
+            st = opt.state[p]
+            assert np.array_equal(H.to_u16(p.detach()).reshape(-1), self.p[k]), f"param {k}"
+            for name, ref in (("exp_avg", self.m[k]), ("exp_avg_sq", self.v[k]),
+                              ("compensation", self.c[k])):
+                if ref is None:
+                    assert name not in st
+                    continue
+                got = H.to_np(st[name]).reshape(-1)
+                assert np.array_equal(got.view(np.uint8), ref.view(np.uint8)), f"{name} {k}"
+
+
+def _hp(group):
+    return O.hparams(lr=group["lr"], beta1=group["betas"][0], beta2=group["betas"][1],
+                     eps=group["eps"], weight_decay=group["weight_decay"],
+                     max_grad_norm=group["max_grad_norm"])
+
+
+@pytest.mark.parametrize("option", sorted(OPTIONS))
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_optimizer_steps_match_the_oracle(option, clip):
+    params = _params()
+    opt = OPT.AnyPrecisionAdamW(params, max_grad_norm=clip, **OPTIONS[option])
+    ref = _OracleSide(params, opt.mode)
+    for k in range(1, 6):
+        opt.zero_grad()
+        gs = _grad(k, inf_at=3 if clip else None)
+        for p, g in zip(params, gs):
+            p.grad.copy_(g)
+        opt.step()
+        skipped, norm = ref.step(gs, _hp(opt.param_groups[0]))
+        torch.cuda.synchronize()
+        assert int(opt.last_nonfinite[0].item()) == int(skipped)
+        assert skipped == (clip > 0 and k == 3)
+        if clip:
+            assert abs(opt.last_grad_norm[0].item() - norm) <= 1e-13 * norm or skipped
+        assert int(opt.state[params[0]]["step"].item()) == ref.t
+    ref.check(opt, params)
+
+
+def test_lr_scheduler_and_two_groups():
+    """A LambdaLR changes lr every step (uploaded to the device between
+    steps); two groups with different weight decay step independently."""
+    params = _params()
+    opt = OPT.AnyPrecisionAdamW([{"params": params[:3]},
+                                 {"params": params[3:], "weight_decay": 0.0}])
+    sched = torch.optim.lr_scheduler.LambdaLR(opt, lambda s: 1.0 / (1 + s))
+    refs = [_OracleSide(params[:3], opt.mode), _OracleSide(params[3:], opt.mode)]
+    for k in range(1, 5):
+        gs = _grad(k)
+        for p, g in zip(params, gs):
+            p.grad.copy_(g)
+        opt.step()
+        refs[0].step(gs[:3], _hp(opt.param_groups[0]))
+        refs[1].step(gs[3:], _hp(opt.param_groups[1]))
+        sched.step()
+    torch.cuda.synchronize()
+    refs[0].check(opt, params[:3])
+    refs[1].check(opt, params[3:])
+
+
+def test_backward_accumulates_into_the_optimizer_buffer():
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(64, 128), torch.nn.GELU(),
+                                torch.nn.Linear(128, 8)).cuda().to(torch.bfloat16)
+    params = list(model.parameters())
+    opt = OPT.AnyPrecisionAdamW(params, momentum_dtype=torch.float32)
+    ptrs = [p.grad.data_ptr() for p in params]
+    ref = _OracleSide(params, opt.mode)
+    for k in range(3):
+        x = torch.randn(32, 64, device="cuda", dtype=torch.bfloat16)
+        opt.zero_grad()
+        model(x).float().pow(2).mean().backward()
+        model(x * 0.5).float().pow(2).mean().backward()   # accumulates
+        assert [p.grad.data_ptr() for p in params] == ptrs, "gradients moved out of the buffer"
+        gs = [p.grad.detach().clone() for p in params]
+        opt.step()
+        ref.step(gs, _hp(opt.param_groups[0]))
+    torch.cuda.synchronize()
+    ref.check(opt, params)
+
+
+def test_checkpoint_round_trip_continues_identically():
+    pa, pb = _params(), _params()
+    opt_a = OPT.AnyPrecisionAdamW(pa, max_grad_norm=1.0, momentum_dtype=torch.float32)
+    opt_b = OPT.AnyPrecisionAdamW(pb, max_grad_norm=1.0, momentum_dtype=torch.float32)
+    for k in range(1, 3):
+        for p, g in zip(pa, _grad(k)):
+            p.grad.copy_(g)
+        opt_a.step()
+    buf = io.BytesIO()
+    torch.save({"params": [p.detach().clone() for p in pa], "opt": opt_a.state_dict()}, buf)
+    buf.seek(0)
+    ck = torch.load(buf, weights_only=False)
+    with torch.no_grad():
+        for p, q in zip(pb, ck["params"]):
+            p.copy_(q)
+    opt_b.load_state_dict(ck["opt"])
+    for k in range(3, 6):
+        for p, q, g in zip(pa, pb, _grad(k)):
+            p.grad.copy_(g)
+            q.grad.copy_(g)
+        opt_a.step()
+        opt_b.step()
+    torch.cuda.synchronize()
+    for p, q in zip(pa, pb):
+        assert torch.equal(p.view(torch.int16), q.view(torch.int16))
+        for name in ("exp_avg", "exp_avg_sq", "compensation"):
+            assert torch.equal(opt_a.state[p][name].view(torch.uint8),
+                               opt_b.state[q][name].view(torch.uint8))
+    assert opt_a.state[pa[0]]["step"].item() == opt_b.state[pb[0]]["step"].item() == 5
