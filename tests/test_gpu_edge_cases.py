@@ -10,7 +10,6 @@ import pytest
 import torch
 
 import parity_harness as H
-from adamw_optimizer_step_sm_gb300 import adamw_sm as A
 from adamw_optimizer_step_sm_gb300 import workloads as W
 from test_gpu_parity import _assert, _small
 

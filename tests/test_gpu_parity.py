@@ -426,7 +426,6 @@ def test_buffers_of_another_kind_are_refused_before_any_launch():
 def test_step_table_over_a_device_table_matches_a_plan():
     """adamw_step_table takes the tensor table from device memory, caches one
     plan for it, and updates exactly like an explicit plan."""
-    import ctypes
     w = _small("table", mode=W.MODE_MIXED, max_grad_norm=0.5, steps=3)
     a = H.GpuSide(w)
     b = W.make_state(w, "cuda")
