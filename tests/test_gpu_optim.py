@@ -172,3 +172,40 @@ def test_checkpoint_round_trip_continues_identically():
             assert torch.equal(opt_a.state[p][name].view(torch.uint8),
                                opt_b.state[q][name].view(torch.uint8))
     assert opt_a.state[pa[0]]["step"].item() == opt_b.state[pb[0]]["step"].item() == 5
+
+
+@pytest.mark.parametrize("clip", [0.0, 1.0])
+def test_step_replays_from_a_cuda_graph(clip):
+    """The step needs no host synchronisation, so it can be captured once and
+    replayed: replays of the captured step (new gradients copied into the
+    optimizer's gradient buffer before each) give the same bytes as eager
+    steps of a twin optimizer, including the step counter."""
+    pa, pb = _params(), _params()
+    kw = dict(max_grad_norm=clip, variance_dtype=torch.float32)
+    opt_a, opt_b = OPT.AnyPrecisionAdamW(pa, **kw), OPT.AnyPrecisionAdamW(pb, **kw)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in (1, 2):                       # warm-up steps, eager on both
+            for p, q, g in zip(pa, pb, _grad(k)):
+                p.grad.copy_(g)
+                q.grad.copy_(g)
+            opt_a.step()
+            opt_b.step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt_a.step()
+    for k in (3, 4, 5):
+        for p, q, g in zip(pa, pb, _grad(k)):
+            p.grad.copy_(g)
+            q.grad.copy_(g)
+        graph.replay()
+        opt_b.step()
+    torch.cuda.synchronize()
+    for p, q in zip(pa, pb):
+        assert torch.equal(p.view(torch.int16), q.view(torch.int16))
+        for name in ("exp_avg", "exp_avg_sq", "compensation"):
+            assert torch.equal(opt_a.state[p][name].view(torch.uint8),
+                               opt_b.state[q][name].view(torch.uint8))
+    assert opt_a.state[pa[0]]["step"].item() == opt_b.state[pb[0]]["step"].item() == 5
