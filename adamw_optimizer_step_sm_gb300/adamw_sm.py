@@ -33,6 +33,10 @@ ANYPREC_C_FP32 = 4
 ANYPREC_NO_KAHAN = 8
 ANYPREC_MODES = tuple(MODE_ANYPREC | f for f in range(16) if (f & 12) != 12)
 PLAN_NORM = 1
+BUILD_CHECK_BOUNDS = 1
+BUILD_BULK_STAGING = 2
+STATUS_WAIT_RAN_OUT = 1
+STATUS_BOUNDS = 2
 PLAN_NO_FUSE = 2
 STEP_CLIP = 1
 STEP_NORM = 2
@@ -99,6 +103,9 @@ def load() -> ctypes.CDLL:
             L.adamw_plan_destroy.argtypes = [vp]
             L.adamw_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
             L.adamw_plan_test_skew_barrier.argtypes = [vp, i64]
+            L.adamw_plan_test_corrupt_chunk.argtypes = [vp, i64, i64]
+            L.adamw_build_flags.argtypes = []
+            L.adamw_build_flags.restype = i32
             L.adamw_lr_linear_warmup.argtypes = [ctypes.c_float, i64, i64, i64]
             L.adamw_lr_linear_warmup.restype = ctypes.c_float
             L.adamw_lr_linear_warmup_device.argtypes = [vp, vp, ctypes.c_float, i64, i64, vp]
@@ -120,7 +127,7 @@ def load() -> ctypes.CDLL:
                          "adamw_step_scalars", "adamw_copy_probe", "adamw_grad_norm_noalloc",
                          "adamw_step_table", "adamw_step_table_cache_clear",
                          "adamw_plan_device_status", "adamw_lr_linear_warmup_device",
-                         "adamw_plan_test_skew_barrier"):
+                         "adamw_plan_test_skew_barrier", "adamw_plan_test_corrupt_chunk"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -220,6 +227,16 @@ def adamw_plan_device_status(plan: int) -> int:
     out = ctypes.c_int32(0)
     _check(load().adamw_plan_device_status(plan, ctypes.byref(out)), "adamw_plan_device_status")
     return out.value
+
+
+def adamw_build_flags() -> int:
+    """BUILD_CHECK_BOUNDS / BUILD_BULK_STAGING bits of the loaded library."""
+    return int(load().adamw_build_flags())
+
+
+def adamw_plan_test_corrupt_chunk(plan: int, chunk: int, delta: int) -> None:
+    """Bounds-checked builds only: lengthen update chunk ``chunk`` by ``delta``."""
+    _check(load().adamw_plan_test_corrupt_chunk(plan, chunk, delta), "adamw_plan_test_corrupt_chunk")
 
 
 def adamw_plan_test_skew_barrier(plan: int, delta: int) -> None:

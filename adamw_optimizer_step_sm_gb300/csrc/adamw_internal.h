@@ -43,6 +43,21 @@ struct ChunkDev {
     int64_t len;
 };
 
+// Bounds-checked build: every chunk also carries the extent of each of its
+// tensor's buffers, and the kernels check the chunk against them before any
+// access; a chunk that falls outside is skipped and bit 1 (value 2) of the
+// plan's device status word is set.  A debugging aid (compute-sanitizer
+// stand-in), off by default.
+#ifndef ADAMW_CHECK_BOUNDS
+#define ADAMW_CHECK_BOUNDS 0
+#endif
+// 1: the bf16 Kahan update stages its inputs in shared memory with
+// cp.async.bulk (a measured alternative, slower on GB300; off by default).
+#ifndef ADAMW_BULK
+#define ADAMW_BULK 0
+#endif
+constexpr int32_t kStatusBounds = 2;
+
 // Device form of a chunk: the five stream pointers already offset to the
 // chunk's first element, so a CTA can prefetch its next chunk with one
 // independent 48-byte load.
@@ -53,8 +68,14 @@ struct alignas(16) ChunkPtr {
     void* v;
     void* a;
     int64_t len2;    // 2 * len + vec
+#if ADAMW_CHECK_BOUNDS
+    const void* lo[5];   // first byte of each of the tensor's buffers
+    const void* hi[5];   // one past its last byte
+    int32_t* status;     // the plan's device status word
+    int64_t pad_;
+#endif
 };
-static_assert(sizeof(ChunkPtr) == 48, "chunk layout");
+static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout");
 
 // Nominal elements per round-robin tile of the interleaved partition of the
 // update kernel (measured on GB300: round-robin tiles beat contiguous per-CTA

@@ -353,6 +353,10 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->done = reinterpret_cast<unsigned int*>(b + o_d);
     P->flagword = reinterpret_cast<int32_t*>(b + o_d + sizeof(uint32_t));
     P->fused = fused;
+#if ADAMW_CHECK_BOUNDS
+    for (ChunkPtr& c : cp) c.status = P->status;
+    for (ChunkPtr& c : cp_norm) c.status = P->status;
+#endif
 
     auto up = [&](void* dst, const void* src, size_t bytes, const char* what) {
         return bytes == 0 || cuda_ok(cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice), what);
@@ -531,6 +535,28 @@ extern "C" int adamw_plan_test_skew_barrier(adamw_plan_t plan, int64_t delta) {
     v += static_cast<unsigned long long>(delta);
     return cuda_ok(cudaMemcpy(plan->arrivals, &v, sizeof(v), cudaMemcpyHostToDevice),
                    "cudaMemcpy(arrivals)") ? ADAMW_OK : ADAMW_ERR_CUDA;
+}
+
+extern "C" int32_t adamw_build_flags(void) {
+    return (ADAMW_CHECK_BOUNDS ? ADAMW_BUILD_CHECK_BOUNDS : 0) |
+           (ADAMW_BULK ? ADAMW_BUILD_BULK_STAGING : 0);
+}
+
+extern "C" int adamw_plan_test_corrupt_chunk(adamw_plan_t plan, int64_t chunk, int64_t delta) {
+    // Only a bounds-checked build may run a chunk that lies: there the
+    // kernels refuse it before touching memory.
+    if (!ADAMW_CHECK_BOUNDS || !plan || chunk < 0 || chunk >= plan->upd.n_chunks)
+        return ADAMW_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return ADAMW_ERR_CUDA;
+    int64_t len2 = 0;
+    int64_t* at = &plan->upd.chunks[chunk].len2;
+    if (!cuda_ok(cudaDeviceSynchronize(), "cudaDeviceSynchronize") ||
+        !cuda_ok(cudaMemcpy(&len2, at, sizeof(len2), cudaMemcpyDeviceToHost), "cudaMemcpy(chunk)"))
+        return ADAMW_ERR_CUDA;
+    len2 += 2 * delta;
+    return cuda_ok(cudaMemcpy(at, &len2, sizeof(len2), cudaMemcpyHostToDevice), "cudaMemcpy(chunk)")
+               ? ADAMW_OK : ADAMW_ERR_CUDA;
 }
 
 extern "C" int adamw_plan_destroy(adamw_plan_t plan) {

@@ -826,6 +826,9 @@ __device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t 
 
 // One chunk descriptor, read through the read-only path.
 __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
+#if ADAMW_CHECK_BOUNDS
+    return *c;
+#else
     const ulonglong2* q = reinterpret_cast<const ulonglong2*>(c);
     const ulonglong2 a = __ldg(q), b = __ldg(q + 1), d = __ldg(q + 2);
     ChunkPtr r;
@@ -836,7 +839,46 @@ __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
     r.a = reinterpret_cast<void*>(d.x);
     r.len2 = static_cast<int64_t>(d.y);
     return r;
+#endif
 }
+
+#if ADAMW_CHECK_BOUNDS
+// Bytes per element of stream s (param, grad, exp_avg, exp_avg_sq, aux) in
+// storage mode MODE, 0 for a stream the mode does not use; written out here
+// independently of the host planner's table, so the check cross-checks it.
+template <int MODE>
+__device__ constexpr int stream_bytes(int s) {
+    if (MODE >= ADAMW_MODE_ANYPREC) {
+        constexpr int f = MODE & 15;
+        return s < 2 ? 2 : s == 2 ? ((f & 1) ? 4 : 2) : s == 3 ? ((f & 2) ? 4 : 2)
+                                                      : ((f & 8) ? 0 : (f & 4) ? 4 : 2);
+    }
+    if (MODE == ADAMW_MODE_MIXED_FP32_MASTER) return s == 0 || s == 2 || s == 3 ? 4 : 2;
+    if (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) return s == 2 || s == 3 ? 4 : 2;
+    if (MODE == ADAMW_MODE_BF16_PLAIN) return s == 4 ? 0 : 2;
+    if (MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR) return s == 3 ? 4 : 2;
+    return 2;
+}
+
+// Whether the chunk's `len` elements lie inside its tensor's buffers, for
+// every stream of MODE selected by `mask` (bit s = stream s).  A chunk that
+// does not is reported in the plan's status word; the caller skips it.
+template <int MODE>
+__device__ __forceinline__ bool chunk_in_bounds(const ChunkPtr& c, int64_t len, int mask = 31) {
+    const void* ptr[5] = {c.p, c.g, c.m, c.v, c.a};
+    bool ok = len >= 0;
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int es = stream_bytes<MODE>(s);
+        if (es == 0 || !((mask >> s) & 1)) continue;
+        const char* b = static_cast<const char*>(ptr[s]);
+        ok = ok && b >= static_cast<const char*>(c.lo[s]) &&
+             b + len * es <= static_cast<const char*>(c.hi[s]);
+    }
+    if (!ok && threadIdx.x == 0) atomicOr(c.status, kStatusBounds);
+    return ok;
+}
+#endif
 
 // ---- the CTA's share of the update: chunks [c0, c1), each chunk's
 // descriptor fetched one ahead.
@@ -852,6 +894,12 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
         if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
         const int64_t len = cur.len2 >> 1;
         const bool vec = cur.len2 & 1;
+#if ADAMW_CHECK_BOUNDS
+        if (!chunk_in_bounds<MODE>(cur, len)) {
+            cur = nxt;
+            continue;
+        }
+#endif
         if constexpr (MODE == ADAMW_MODE_BF16_KAHAN) {
             if (vec) kahan_vec_chunk<K, kU>(cur, len, s, coef, bad);
             else kahan_elem_chunk<K>(cur, len, s, coef, bad);
@@ -916,6 +964,9 @@ __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ ch
         const ChunkPtr ch = load_chunk(chunks + ci);
         const uint16_t* g = static_cast<const uint16_t*>(ch.g);
         const int64_t len = ch.len2 >> 1;
+#if ADAMW_CHECK_BOUNDS
+        if (!chunk_in_bounds<ADAMW_MODE_BF16_KAHAN>(ch, len, 1 << 1)) continue;  // g only
+#endif
         int64_t done = 0;
         if (ch.len2 & 1) {
             const int64_t nvec = len / kVec;

@@ -99,7 +99,7 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
             }
             __nanosleep(256);
         }
-        if (!ok) atomicExch(status, 1);
+        if (!ok) atomicOr(status, 1);
         passed = ok;
     }
     __syncthreads();
@@ -142,10 +142,8 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
 // stage j + NS while the CTA computes stage j from shared memory; results
 // go straight to global memory with 16-byte stores.  Every mbarrier wait is
 // bounded: a wait that does not complete sets *err and the CTA returns.
-#ifndef ADAMW_BULK
-#define ADAMW_BULK 0
-#endif
 #if ADAMW_BULK
+static_assert(!ADAMW_CHECK_BOUNDS, "the bulk-copy variant has no bounds-checked build");
 #ifndef ADAMW_BULK_STAGES
 #define ADAMW_BULK_STAGES 2
 #endif
@@ -308,7 +306,7 @@ adamw_update_bulk_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
         // a wait ran out: report it, let the copies already issued land
         // (bounded), and leave without touching anything else
         if (threadIdx.x == 0) {
-            atomicExch(err, 1);
+            atomicOr(err, 1);
             for (int32_t k = j; k < njobs && k < j + kBulkStages; ++k)
                 mbar_wait_bounded(&bar[k % kBulkStages], uint32_t(k / kBulkStages) & 1u);
         }

@@ -328,6 +328,15 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
         d.v = at(t.exp_avg_sq, es[3]);
         d.a = es[4] ? at(t.aux, es[4]) : nullptr;
         d.len2 = 2 * c.len + c.vec;
+#if ADAMW_CHECK_BOUNDS
+        const void* bases[5] = {t.param, t.grad, t.exp_avg, t.exp_avg_sq, t.aux};
+        for (int s = 0; s < 5; ++s) {
+            d.lo[s] = es[s] ? bases[s] : nullptr;
+            d.hi[s] = es[s] ? static_cast<const char*>(bases[s]) + t.numel * es[s] : nullptr;
+        }
+        d.status = nullptr;   // set when the plan's device block exists
+        d.pad_ = 0;
+#endif
     }
 }
 

@@ -268,9 +268,12 @@ int adamw_grad_norm(adamw_plan_t plan, double* d_grad_norm,
                     int32_t* d_nonfinite, adamw_stream_t stream);
 
 /* Reads and clears the plan's device status word (synchronises the plan's
- * device first): 0, or 1 when a kernel of this plan gave up on a bounded wait
- * (every device-side wait in this library is bounded, about a second; the
- * launch then left its CTA's work undone, so the step is partly applied).
+ * device first): 0, or a combination of
+ *   1  a kernel of this plan gave up on a bounded wait (every device-side
+ *      wait in this library is bounded, about a second; the launch then left
+ *      its CTA's work undone, so the step is partly applied);
+ *   2  (bounds-checked builds only, ADAMW_BUILD_CHECK_BOUNDS) a chunk of the
+ *      plan fell outside its tensor's buffers and was skipped.
  * Clearing also realigns the fused step's barrier counter, so the plan is
  * usable again.  Errors: INVALID_ARG, CUDA. */
 int adamw_plan_device_status(adamw_plan_t plan, int32_t* out);
@@ -280,6 +283,21 @@ int adamw_plan_device_status(adamw_plan_t plan, int32_t* out);
  * CTA's bounded barrier wait runs out and sets the device status.  Never
  * needed in normal use.  Errors: INVALID_ARG, CUDA. */
 int adamw_plan_test_skew_barrier(adamw_plan_t plan, int64_t delta);
+
+/* How the library was built: ADAMW_BUILD_CHECK_BOUNDS when every kernel
+ * checks each chunk against its tensor's buffers before touching it (a
+ * debugging build, compiled with -DADAMW_CHECK_BOUNDS=1), and
+ * ADAMW_BUILD_BULK_STAGING when the bf16 Kahan update stages its inputs with
+ * cp.async.bulk (-DADAMW_BULK=1). */
+#define ADAMW_BUILD_CHECK_BOUNDS 1
+#define ADAMW_BUILD_BULK_STAGING 2
+int32_t adamw_build_flags(void);
+
+/* For tests of the bounds-checked build only: lengthens update chunk `chunk`
+ * of the plan by `delta` elements (synchronous), so that the next update
+ * finds it outside its tensor, skips it and sets status bit 2.  Other builds
+ * refuse (INVALID_ARG), as they do not check.  Errors: INVALID_ARG, CUDA. */
+int adamw_plan_test_corrupt_chunk(adamw_plan_t plan, int64_t chunk, int64_t delta);
 
 /* Releases the plan's device memory (synchronises the plan's device first).
  * NULL is accepted. */
