@@ -400,6 +400,44 @@ def pin_skip_on_nonfinite(o: O.Oracle):
         assert changed
 
 
+def pin_list_step_clipped_equals_torch(o: O.Oracle, steps: int = 5):
+    """The list step with clipping: one coefficient from the global norm over
+    every tensor of the list (torch.nn.utils.clip_grad_norm_ over the
+    parameter list), then the mixed-mode step on each tensor
+    (torch.optim.AdamW over the list), and the norm it reports is the square
+    root of the sum of squares over all tensors."""
+    r = _rng(24)
+    sizes = [100, 37, 2048]
+    ps = [(r.standard_normal(n) * 0.02).astype(F32) for n in sizes]
+    grads = [[torch_bf16_bits((r.standard_normal(n) * 1e-2).astype(F32)) for n in sizes]
+             for _ in range(steps)]
+    hp = O.hparams(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_grad_norm=0.05)
+    tens = [[p.copy(), None, np.zeros(n, F32), np.zeros(n, F32), np.zeros(n, np.uint16)]
+            for p, n in zip(ps, sizes)]
+    for t, gs in enumerate(grads, 1):
+        for e, g in zip(tens, gs):
+            e[1] = g
+        skipped, norm = o.list_step([tuple(e) for e in tens], 1, hp, t)
+        assert not skipped
+        want = math.sqrt(math.fsum(float(x) ** 2 for g in gs for x in bf16_to_f64(g)))
+        assert abs(norm - want) <= 1e-14 * want, (norm, want)
+        assert want > 0.05, "the clip must be active"
+    tp = [torch.nn.Parameter(torch.from_numpy(p.copy())) for p in ps]
+    opt = torch.optim.AdamW(tp, lr=f32(2e-4), betas=(f32(0.9), f32(0.95)), eps=f32(1e-8),
+                            weight_decay=f32(0.1), foreach=False, fused=False)
+    for gs in grads:
+        for q, g in zip(tp, gs):
+            q.grad = torch.from_numpy(bf16_to_f64(g).astype(F32))
+        torch.nn.utils.clip_grad_norm_(tp, 0.05, foreach=False)
+        opt.step()
+    for e, q in zip(tens, tp):
+        st = opt.state[q]
+        _close(e[0], q.detach().numpy(), 1e-6, "master")
+        _close(e[2], st["exp_avg"].numpy(), 2e-6, "exp_avg")
+        _close(e[3], st["exp_avg_sq"].numpy(), 2e-6, "exp_avg_sq")
+        assert np.array_equal(e[4], torch_bf16_bits(e[0])), "p_out must be bf16(master')"
+
+
 def pin_bias_correction_powers(o: O.Oracle):
     """The per-step scalars against the closed forms with the library's fp64
     pow: step_size = lr/(1-b1^t), sbc2 = sqrt(1-b2^t), 1-b1, 1-b2, lr*wd,
@@ -692,6 +730,7 @@ def pin_anyprec_fp32_state_vs_torch(o: O.Oracle, steps: int = 200):
 
 
 ALL_PINS = [
+    pin_list_step_clipped_equals_torch,
     pin_anyprec_matches_named_modes,
     pin_anyprec_step_definition,
     pin_anyprec_fp32_state_vs_torch,

@@ -74,6 +74,14 @@ MUTANTS = [
      "        f = (double)(total - k - 1) / span;\n"),
     ("clip_scale_ignored_mixed", "float p0 = master[i];\n",
      "float p0 = master[i]; gi = bf16_bits_to_f32(g[i]);\n"),
+    ("list_norm_first_tensor_only",
+     "        for (int32_t k = 0; k < n_tensors; ++k)\n            oracle_grad_sumsq(",
+     "        for (int32_t k = 0; k < 1; ++k)\n            oracle_grad_sumsq("),
+    ("list_coef_ignored", "        coef = oracle_clip_coef(acc[0] + acc[1], hp->max_grad_norm, norm_out);",
+     "        (void)oracle_clip_coef(acc[0] + acc[1], hp->max_grad_norm, norm_out);"),
+    ("list_steps_first_tensor_only",
+     "    for (int32_t k = 0; k < n_tensors; ++k) {\n        const oracle_tensor_t* e = &list[k];",
+     "    for (int32_t k = 0; k < 1; ++k) {\n        const oracle_tensor_t* e = &list[k];"),
     ("anyprec_fp32_store_rounds", "        ((float*)buf)[i] = x;\n        return x;\n",
      "        x = bf16_bits_to_f32(f32_to_bf16_rne(x));\n        ((float*)buf)[i] = x;\n"
      "        return x;\n"),
