@@ -17,9 +17,17 @@ namespace adamw {
 constexpr int kBlock = ADAMW_BLOCK;
 // Elements per vector: 8 bf16 = one 16-byte load; 8 fp32 = two.
 constexpr int kVec = 8;
-// Largest gradient list (bytes) whose clipped steps run as one fused
-// launch: half of GB300's 129 MB L2, so the norm pass leaves g in L2.
-constexpr int64_t kFusedMaxGradBytes = int64_t(64) << 20;
+// Largest gradient list (MiB of bf16 gradients) whose clipped steps run as
+// one fused launch.  Measured on GB300 with the fp32-master mode: the fused
+// step saves about 6 us up to 40M parameters (the update re-reads g from
+// L2) and still 2-3 us at 56M and 80M (launches saved), but at 1.3B it is
+// 0.7 % slower (its norm pass runs on the update grid, half the CTAs of the
+// norm pass's own grid).  160 MiB = 80M parameters, the largest size
+// measured as a win.
+#ifndef ADAMW_FUSED_MAX_GRAD_MB
+#define ADAMW_FUSED_MAX_GRAD_MB 160
+#endif
+constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.
 constexpr int64_t kMinElemsPerCta = int64_t(kBlock) * kVec;

@@ -280,8 +280,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
 
     int64_t total = 0;
     for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;
-    // Lists whose gradients fit in half of L2 run clipped steps as one fused
-    // cooperative launch (the norm pass leaves g in L2 for the update).
+    // Lists whose gradients are at most kFusedMaxGradBytes run clipped steps
+    // as one fused cooperative launch (measured faster up to that size).
     const bool fused = (flags & ADAMW_PLAN_NORM) && !(flags & ADAMW_PLAN_NO_FUSE) &&
                        di.cooperative && di.occ_fused[var] > 0 &&
                        total * 2 <= kFusedMaxGradBytes;
