@@ -33,7 +33,8 @@ def test_library_exports_every_declared_symbol():
     assert not missing, f"declared but not exported: {missing}"
 
 
-ELEM_SIZES = {0: (2, 2, 2, 2, 2), 1: (4, 2, 4, 4, 2), 2: (2, 2, 4, 4, 2)}
+ELEM_SIZES = {0: (2, 2, 2, 2, 2), 1: (4, 2, 4, 4, 2), 2: (2, 2, 4, 4, 2), 3: (2, 2, 2, 2, 0),
+              4: (2, 2, 2, 4, 2)}
 # any-precision modes: bf16 param and grad; the flags make m, v, c fp32 or
 # drop c (written out from the header's table, not from the library)
 for _f in range(16):
@@ -281,3 +282,41 @@ def test_optimizer_options_map_to_storage_modes():
         OPT.AnyPrecisionAdamW([torch.zeros(2, dtype=bf)], betas=(0.9, 1.0))
     with pytest.raises(TypeError):   # parameters must be bf16 CUDA tensors
         OPT.AnyPrecisionAdamW([torch.zeros(2, dtype=bf)])
+
+
+def test_partition_properties_on_random_lists():
+    """200 random lists (1-60 tensors of 0 to 300,000 elements, a random
+    storage mode, each stream's base skewed by a random number of elements,
+    a random grid from 1 to 1216): every element lands in exactly one chunk,
+    chunks come in CTA order, vector chunks start 16-byte aligned in every
+    stream, and interleaved cuts inside a vector body fall on the
+    2048-element grid from the body's start."""
+    rng = np.random.default_rng(2024)
+    modes = [0, 1, 2, 3, 4] + list(A.ANYPREC_MODES)
+    for case in range(200):
+        mode = int(rng.choice(modes))
+        es = ELEM_SIZES[mode]
+        n_t = int(rng.integers(1, 61))
+        sizes = rng.integers(0, 300_001, n_t)
+        sizes[rng.random(n_t) < 0.2] = rng.integers(0, 9, int(np.sum(rng.random(n_t) < 0.2)) or 1)[0]
+        entries = []
+        for k, n in enumerate(sizes):
+            skew = [int(rng.integers(0, 8)) if rng.random() < 0.3 else 0 for _ in range(5)]
+            base = (k + 1) << 36
+            e = tuple(base + (s + 1) * (1 << 32) + sk * max(es[s], 1) for s, sk in enumerate(skew))
+            if es[4] == 0:
+                e = e[:4] + (0,)
+            entries.append(e + (int(n),))
+        grid = int(rng.integers(1, 1217))
+        chunks = _check_partition(entries, mode, grid)
+        # cuts inside a vector body: on the 2048-element grid of the body
+        # (interleaved partition) or on whole vectors (contiguous ranges)
+        interleaved = int(sizes.sum()) >= 2 * grid * 8192
+        step = 2048 if interleaved else 8
+        heads = {}
+        for c in chunks:
+            if c.vec:
+                heads.setdefault(c.tensor, []).append(c.offset)
+        for k, offs in heads.items():
+            head = min(offs)
+            assert all((o - head) % step == 0 for o in offs), (case, k, step, sorted(offs)[:5])
