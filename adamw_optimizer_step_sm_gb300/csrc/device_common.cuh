@@ -157,20 +157,18 @@ __device__ __forceinline__ float mixed_x1(const StepScalars& s, float coef, floa
 // Per storage mode: U, the 16-byte vectors each thread has in flight per
 // stream, and B, the resident CTAs per SM the update kernel's register budget
 // is fitted to (0: no constraint).  Chosen by measurement on GB300 over the
-// OPT-1.3b list (every mode at U = 1..3 and B = none, 2, 3, 4): the modes
-// with fp32 streams favour fewer vectors and more CTAs (or the reverse)
-// according to their mix of 2- and 4-byte streams.  ADAMW_UNROLL and
-// ADAMW_MIN_BLOCKS, when defined, override the table for every mode.
+// OPT-1.3b list (every mode at U = 1..3 and B = none, 2, 3), with the
+// interleaved partition cut on 2048-element boundaries: the modes with fp32
+// streams favour fewer vectors and more CTAs (or the reverse) according to
+// their mix of 2- and 4-byte streams.  ADAMW_UNROLL and ADAMW_MIN_BLOCKS,
+// when defined, override the table for every mode.
 template <int MODE>
 struct UpdateTuning {
     static constexpr int kU =
         MODE == ADAMW_MODE_MIXED_FP32_MASTER ? 1
         : MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR ? 1
         : MODE == (ADAMW_MODE_ANYPREC | 1) ? 1
-        : MODE == (ADAMW_MODE_ANYPREC | 3) ? 3
         : MODE == (ADAMW_MODE_ANYPREC | 4) ? 1
-        : MODE == (ADAMW_MODE_ANYPREC | 5) ? 3
-        : MODE == (ADAMW_MODE_ANYPREC | 6) ? 3
         : MODE == (ADAMW_MODE_ANYPREC | 7) ? 1
         : MODE == (ADAMW_MODE_ANYPREC | 11) ? 3
         : 2;
@@ -178,7 +176,6 @@ struct UpdateTuning {
         MODE == ADAMW_MODE_MIXED_FP32_MASTER ? 2
         : MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR ? 3
         : MODE == (ADAMW_MODE_ANYPREC | 1) ? 3
-        : MODE == (ADAMW_MODE_ANYPREC | 3) ? 2
         : MODE == (ADAMW_MODE_ANYPREC | 4) ? 3
         : MODE == (ADAMW_MODE_ANYPREC | 7) ? 2
         : MODE == (ADAMW_MODE_ANYPREC | 11) ? 2
