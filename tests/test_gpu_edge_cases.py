@@ -139,3 +139,16 @@ def test_tensor_longer_than_2_to_the_31():
     rep, log = H.run_sampled(w, per_tensor=1 << 16)
     _assert(rep, log)
     assert rep.exact == rep.n
+
+
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_ANYPREC | 7])
+def test_two_hundred_clipped_steps_stay_bit_identical(mode):
+    """A long run with clipping on: 200 steps of a ragged 1.2M-element list,
+    an inf injected at step 77 (skipped on both sides), fresh gradients every
+    step.  The clip coefficient is an fp32 rounding of a norm both sides sum
+    exactly, so no step may flip a bit, and nothing may drift."""
+    w = _small("long_run", mode=mode, steps=200, max_grad_norm=0.5, inf_at=(77, 8, 4321))
+    rep, log = H.run_parity(w)
+    _assert(rep, log)
+    assert rep.exact == rep.n
+    assert [k for (k, s, *_r) in log if s] == [77]
