@@ -21,7 +21,9 @@ boundary, and points each ``p.grad`` at its slice of the gradient buffer;
 ``zero_grad`` zeroes that buffer in place (it never sets gradients to None),
 so backward passes accumulate straight into it and a step copies nothing.
 A gradient found elsewhere at step time (the first step, or a ``p.grad``
-assigned by the caller) is copied in once and re-pointed.  The step counter
+assigned by the caller) is copied in once and re-pointed; so use this
+optimizer's ``zero_grad`` (``Module.zero_grad`` sets the gradients to None,
+and each step would then copy them in).  The step counter
 and the hyperparameters live in device memory, so ``step`` never waits for
 the GPU; ``last_grad_norm`` and ``last_nonfinite`` are device tensors.
 
