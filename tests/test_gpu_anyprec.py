@@ -135,3 +135,36 @@ def test_anyprec_canaries_stay_untouched(mode):
         assert bool((b.view(torch.uint8).view(-1, b.element_size())[gaps] == 0xA5).all()), \
             f"a {b.dtype} canary changed"
     gpu.plan.close()
+
+
+@pytest.mark.parametrize("mode", [W.MODE_ANYPREC | 7, W.MODE_ANYPREC | 9])
+def test_anyprec_step_table_matches_a_plan(mode):
+    """adamw_step_table with an any-precision mode (aux NULL without Kahan
+    summation) updates exactly like an explicit plan, one cached plan."""
+    w = _small("anytable", mode=mode, max_grad_norm=0.5, steps=3)
+    a = H.GpuSide(w)
+    b = W.make_state(w, "cuda")
+    g = torch.zeros_like(a.g)
+    v = b.views
+    aux = v(b.aux) if b.aux is not None else [None] * len(w.numels)
+    entries = [A.adamw_tensor_t(*(t.data_ptr() if t is not None else None for t in ts),
+                                ts[0].numel())
+               for ts in zip(v(b.param), v(g), v(b.exp_avg), v(b.exp_avg_sq), aux)]
+    raw = bytes((A.adamw_tensor_t * len(entries))(*entries))
+    d_table = torch.frombuffer(bytearray(raw), dtype=torch.uint8).cuda()
+    hp, _ = H.hp_pair(w)
+    A.adamw_step_table_cache_clear()
+    norm_a = torch.zeros(1, dtype=torch.float64, device="cuda")
+    norm_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    for k in (1, 2, 3):
+        a.set_grad(k)
+        g.copy_(a.g)
+        a.plan.step(hp, k, grad_norm=norm_a)
+        A.adamw_step_table(d_table.data_ptr(), len(entries), w.mode, hp, k, norm_b.data_ptr(), 0,
+                           stream)
+    torch.cuda.synchronize()
+    assert A.adamw_step_table_cache_clear() == 1
+    _same_state(a.st, b)
+    assert norm_a.item() == norm_b.item()
+    a.plan.close()
