@@ -162,11 +162,15 @@ class AnyPrecisionAdamW(torch.optim.Optimizer):
                     g.copy_(p.grad)
                     p.grad = g
             beta1, beta2 = group["betas"]
-            key = (group["lr"], beta1, beta2, group["eps"], group["weight_decay"],
-                   group["max_grad_norm"])
+            # plain floats (a scheduler may keep lr as a tensor)
+            key = tuple(float(x) for x in (group["lr"], beta1, beta2, group["eps"],
+                                           group["weight_decay"], group["max_grad_norm"]))
             if key != b.hp_key:
                 hp = A.hparams(lr=key[0], beta1=key[1], beta2=key[2], eps=key[3],
                                weight_decay=key[4], max_grad_norm=key[5])
+                # refuse out-of-range values here: on the device they would
+                # only make the step skip
+                A.adamw_step_scalars(hp, 1)
                 host = torch.frombuffer(bytearray(bytes(hp)), dtype=torch.uint8)
                 b.d_hp.copy_(host.pin_memory(), non_blocking=True)
                 b.hp_key = key

@@ -209,3 +209,28 @@ def test_step_replays_from_a_cuda_graph(clip):
             assert torch.equal(opt_a.state[p][name].view(torch.uint8),
                                opt_b.state[q][name].view(torch.uint8))
     assert opt_a.state[pa[0]]["step"].item() == opt_b.state[pb[0]]["step"].item() == 5
+
+
+def test_tensor_lr_works_and_out_of_range_values_are_refused():
+    """A scheduler may keep lr as a 0-d tensor: the step takes its value.
+    An out-of-range value set between steps is refused on the host (on the
+    device it could only make the step skip)."""
+    from adamw_optimizer_step_sm_gb300 import adamw_sm as A
+    params = _params()
+    opt = OPT.AnyPrecisionAdamW(params)
+    ref = _OracleSide(params, opt.mode)
+    opt.param_groups[0]["lr"] = torch.tensor(1e-4)
+    gs = _grad(1)
+    for p, g in zip(params, gs):
+        p.grad.copy_(g)
+    opt.step()
+    ref.step(gs, O.hparams(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1))
+    torch.cuda.synchronize()
+    ref.check(opt, params)
+    opt.param_groups[0]["lr"] = -1.0
+    with pytest.raises(A.AdamWError):
+        opt.step()
+    opt.param_groups[0]["lr"] = 1e-4
+    opt.param_groups[0]["betas"] = (0.9, 1.0)
+    with pytest.raises(A.AdamWError):
+        opt.step()
