@@ -7,8 +7,9 @@
 // update a whole model's parameter list in fused launches); this partition is
 // this library's own design.  Every CTA of a persistent grid gets the same
 // number of elements whatever the tensor sizes: large lists are cut into
-// fixed tiles dealt round-robin (the grid sweeps the buffers together), small
-// lists and the norm pass into one contiguous range per CTA.
+// tiles of about 8K elements on 2048-element boundaries of the flattened list
+// and dealt round-robin (the grid sweeps the buffers together), small lists
+// and the norm pass into one contiguous range per CTA.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
