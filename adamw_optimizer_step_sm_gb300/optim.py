@@ -1,5 +1,9 @@
-"""``AnyPrecisionAdamW``: a ``torch.optim.Optimizer`` whose step is one call
-into the adamw_sm library (``adamw_step_device``) per parameter group.
+"""``AnyPrecisionAdamW`` and ``MasterWeightAdamW``: ``torch.optim``
+optimizers whose step is one call into the adamw_sm library
+(``adamw_step_device``) per parameter group.  ``MasterWeightAdamW`` is the
+fp32-master update (see its docstring); the rest of this note is about
+``AnyPrecisionAdamW`` and holds for both where it concerns the layout and
+the step.
 
 It takes the options the pure-bf16 recipe passes to its optimizer ("[pure
 bf16 training] w/ AnyPrecisionAdamW and Kahan summation", "Train from
@@ -62,7 +66,12 @@ def storage_mode(use_kahan_summation: bool, momentum_dtype: torch.dtype,
 
 
 class _GroupBuffers:
-    """A group's flat buffers, views, plan and device-side step state."""
+    """A group's flat buffers, views, plan and device-side step state.
+
+    The plan's param and aux streams depend on the mode: the model's bf16
+    parameters and the compensation (any precision); an fp32 master the
+    optimizer owns and the model's bf16 parameters as output (fp32 master);
+    the model's bf16 parameters and an int16 remainder (bf16 + remainder)."""
 
     def __init__(self, params, mode: int):
         dts = A.buffer_dtypes(mode)
@@ -74,15 +83,31 @@ class _GroupBuffers:
             n += -(-k // _ALIGN) * _ALIGN
         n = max(n, 1)
         flat = lambda dt: None if dt is None else torch.zeros(n, dtype=dt, device=dev)
-        self.grad, self.exp_avg, self.exp_avg_sq, self.comp = (flat(torch.bfloat16), flat(dts[2]),
-                                                              flat(dts[3]), flat(dts[4]))
         view = lambda buf, p, o: None if buf is None else buf[o:o + p.numel()].view(p.shape)
+        self.grad, self.exp_avg, self.exp_avg_sq = flat(torch.bfloat16), flat(dts[2]), flat(dts[3])
         self.grads = [view(self.grad, p, o) for p, o in zip(params, offs)]
         self.exp_avgs = [view(self.exp_avg, p, o) for p, o in zip(params, offs)]
         self.exp_avg_sqs = [view(self.exp_avg_sq, p, o) for p, o in zip(params, offs)]
-        self.comps = [view(self.comp, p, o) for p, o in zip(params, offs)]
-        self.plan = A.Plan(params, self.grads, self.exp_avgs, self.exp_avg_sqs,
-                           self.comps if self.comp is not None else None, mode, norm=True)
+        self.master, self.masters = None, [None] * len(params)
+        self.comp, self.comps = None, [None] * len(params)
+        if mode == A.MODE_MIXED_FP32_MASTER:
+            # the fp32 master starts as the model's bf16 values, exactly
+            self.master = flat(torch.float32)
+            self.masters = [view(self.master, p, o) for p, o in zip(params, offs)]
+            for m, p in zip(self.masters, params):
+                m.copy_(p.detach())
+            plan_p, plan_aux = self.masters, list(params)
+        elif mode == A.MODE_MIXED_BF16_REMAINDER:
+            # remainder 0: the master equals the model's bf16 values
+            self.comp = flat(torch.int16)
+            self.comps = [view(self.comp, p, o) for p, o in zip(params, offs)]
+            plan_p, plan_aux = list(params), self.comps
+        else:
+            self.comp = flat(dts[4])
+            self.comps = [view(self.comp, p, o) for p, o in zip(params, offs)]
+            plan_p, plan_aux = list(params), (self.comps if self.comp is not None else None)
+        self.plan = A.Plan(plan_p, self.grads, self.exp_avgs, self.exp_avg_sqs, plan_aux, mode,
+                           norm=True)
         self.step = torch.zeros(1, dtype=torch.int64, device=dev)
         self.grad_norm = torch.zeros(1, dtype=torch.float64, device=dev)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -90,19 +115,18 @@ class _GroupBuffers:
         self.hp_key = None
 
 
-class AnyPrecisionAdamW(torch.optim.Optimizer):
-    def __init__(self, params, lr: float = 2e-4, betas=(0.9, 0.95), eps: float = 1e-8,
-                 weight_decay: float = 0.1, use_kahan_summation: bool = True,
-                 momentum_dtype: torch.dtype = torch.bfloat16,
-                 variance_dtype: torch.dtype = torch.bfloat16,
-                 compensation_buffer_dtype: torch.dtype = torch.bfloat16,
-                 max_grad_norm: float = 0.0, track_grad_norm: bool = False):
+class _FlatAdamW(torch.optim.Optimizer):
+    """The shared machinery: flat buffers per group, one device-resident
+    library step per group, checkpoints into the optimizer's own buffers."""
+    _aux_name = "compensation"
+
+    def __init__(self, params, mode: int, lr: float, betas, eps: float, weight_decay: float,
+                 max_grad_norm: float, track_grad_norm: bool):
         if not lr >= 0.0 or not eps > 0.0 or not weight_decay >= 0.0:
             raise ValueError("want lr >= 0, eps > 0 and weight_decay >= 0")
         if not (0.0 <= betas[0] < 1.0 and 0.0 <= betas[1] < 1.0):
             raise ValueError("want betas in [0, 1)")
-        self.mode = storage_mode(use_kahan_summation, momentum_dtype, variance_dtype,
-                                 compensation_buffer_dtype)
+        self.mode = mode
         self.track_grad_norm = track_grad_norm
         defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
                         max_grad_norm=max_grad_norm)
@@ -123,8 +147,8 @@ class AnyPrecisionAdamW(torch.optim.Optimizer):
             for p in params:
                 if not p.is_cuda or p.dtype != torch.bfloat16 or not p.is_contiguous() \
                         or p.device != dev:
-                    raise TypeError("AnyPrecisionAdamW steps contiguous bf16 CUDA parameters "
-                                    "of one device")
+                    raise TypeError(f"{type(self).__name__} steps contiguous bf16 CUDA "
+                                    "parameters of one device")
             with torch.cuda.device(dev):
                 b = _GroupBuffers(params, self.mode)
             for k, (p, g) in enumerate(zip(params, b.grads)):
@@ -134,8 +158,10 @@ class AnyPrecisionAdamW(torch.optim.Optimizer):
                 st = self.state[p]
                 st["exp_avg"] = b.exp_avgs[k]
                 st["exp_avg_sq"] = b.exp_avg_sqs[k]
+                if b.master is not None:
+                    st["master"] = b.masters[k]
                 if b.comp is not None:
-                    st["compensation"] = b.comps[k]
+                    st[self._aux_name] = b.comps[k]
                 st["step"] = b.step
             self._buffers[key] = b
         return b
@@ -157,7 +183,7 @@ class AnyPrecisionAdamW(torch.optim.Optimizer):
             for k, (p, g) in enumerate(zip(group["params"], b.grads)):
                 if p.grad is None:
                     raise RuntimeError(f"parameter {k} of a group has no gradient; "
-                                       "AnyPrecisionAdamW steps every parameter")
+                                       f"{type(self).__name__} steps every parameter")
                 if p.grad.data_ptr() != g.data_ptr():
                     g.copy_(p.grad)
                     p.grad = g
@@ -221,9 +247,55 @@ class AnyPrecisionAdamW(torch.optim.Optimizer):
                 s = saved.get(idx)
                 if s is None:
                     continue
-                for name in ("exp_avg", "exp_avg_sq", "compensation"):
+                for name in ("exp_avg", "exp_avg_sq", "compensation", "master", "remainder"):
                     if name in s and name in self.state[p]:
                         self.state[p][name].copy_(s[name])
                 if "step" in s:
                     b.step.copy_(torch.as_tensor(s["step"]).reshape(1))
             b.hp_key = None
+
+
+class AnyPrecisionAdamW(_FlatAdamW):
+    """Pure-bf16 AdamW with the recipe's options: bf16 parameters, each of
+    momentum, variance and Kahan compensation bf16 or fp32, Kahan summation
+    on or off (the recipe's values are the defaults).  State per parameter:
+    exp_avg, exp_avg_sq, compensation (with Kahan summation), step."""
+
+    def __init__(self, params, lr: float = 2e-4, betas=(0.9, 0.95), eps: float = 1e-8,
+                 weight_decay: float = 0.1, use_kahan_summation: bool = True,
+                 momentum_dtype: torch.dtype = torch.bfloat16,
+                 variance_dtype: torch.dtype = torch.bfloat16,
+                 compensation_buffer_dtype: torch.dtype = torch.bfloat16,
+                 max_grad_norm: float = 0.0, track_grad_norm: bool = False):
+        mode = storage_mode(use_kahan_summation, momentum_dtype, variance_dtype,
+                            compensation_buffer_dtype)
+        super().__init__(params, mode, lr, betas, eps, weight_decay, max_grad_norm,
+                         track_grad_norm)
+
+
+class MasterWeightAdamW(_FlatAdamW):
+    """AdamW on bf16 model parameters with an fp32 master: the update the
+    distributed Adam of "Distributed optimizer support for BERT" (NeMo PR
+    #5305, "Usage": distributed_fused_adam) applies to each data-parallel
+    shard, here over one process's parameters.  fp32 m and v; every step
+    updates the master and writes the bf16 parameters from it (round to
+    nearest even).
+
+    ``master="fp32"``: the optimizer keeps an fp32 master copy (state
+    ``master``), 12 B/param of optimizer state.  ``master="remainder"``: the
+    master is the model's bf16 parameter plus an int16 remainder of its bit
+    pattern (state ``remainder``; the "16-bit master param" of the page's
+    memory estimate), 10 B/param, the same trajectory bit for bit (the bf16
+    parameter is then the master rounded to nearest with ties away from
+    zero).  Defaults are torch.optim.AdamW's; the pages give none for this
+    update."""
+
+    def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
+                 weight_decay: float = 0.01, master: str = "fp32", max_grad_norm: float = 0.0,
+                 track_grad_norm: bool = False):
+        modes = {"fp32": A.MODE_MIXED_FP32_MASTER, "remainder": A.MODE_MIXED_BF16_REMAINDER}
+        if master not in modes:
+            raise ValueError('master must be "fp32" or "remainder"')
+        self._aux_name = "remainder"
+        super().__init__(params, modes[master], lr, betas, eps, weight_decay, max_grad_norm,
+                         track_grad_norm)

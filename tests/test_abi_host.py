@@ -320,3 +320,15 @@ def test_partition_properties_on_random_lists():
         for k, offs in heads.items():
             head = min(offs)
             assert all((o - head) % step == 0 for o in offs), (case, k, step, sorted(offs)[:5])
+
+
+def test_master_weight_optimizer_validates_its_options():
+    import torch
+    from adamw_optimizer_step_sm_gb300 import optim as OPT
+    bf = torch.bfloat16
+    with pytest.raises(ValueError):
+        OPT.MasterWeightAdamW([torch.zeros(2, dtype=bf)], master="fp16")
+    with pytest.raises(ValueError):
+        OPT.MasterWeightAdamW([torch.zeros(2, dtype=bf)], eps=0.0)
+    with pytest.raises(TypeError):   # bf16 CUDA model parameters only
+        OPT.MasterWeightAdamW([torch.zeros(2, dtype=torch.float32)])

@@ -234,3 +234,86 @@ def test_tensor_lr_works_and_out_of_range_values_are_refused():
     opt.param_groups[0]["betas"] = (0.9, 1.0)
     with pytest.raises(A.AdamWError):
         opt.step()
+
+
+class _MasterOracle:
+    """The same parameters as host arrays for the fp32-master (mode 1) or
+    bf16 + remainder (mode 2) oracle steps."""
+
+    def __init__(self, params, remainder: bool):
+        self.o = O.load()
+        self.mode = 2 if remainder else 1
+        p16 = [H.to_u16(p.detach()).reshape(-1).copy() for p in params]
+        n = [p.numel() for p in params]
+        if remainder:
+            self.tens = [[q, None, np.zeros(k, np.float32), np.zeros(k, np.float32),
+                          np.zeros(k, np.int16)] for q, k in zip(p16, n)]
+        else:
+            self.tens = [[(q.astype(np.uint32) << 16).view(np.float32).copy(), None,
+                          np.zeros(k, np.float32), np.zeros(k, np.float32), q.copy()]
+                         for q, k in zip(p16, n)]
+        self.t = 0
+
+    def step(self, grads, hp):
+        for e, g in zip(self.tens, grads):
+            e[1] = H.to_u16(g).reshape(-1).copy()
+        skipped, norm = self.o.list_step([tuple(e) for e in self.tens], self.mode, hp, self.t + 1)
+        if not skipped:
+            self.t += 1
+        return skipped, norm
+
+    def check(self, opt, params):
+        for k, p in enumerate(params):
+            st, e = opt.state[p], self.tens[k]
+            model = e[0] if self.mode == 2 else e[4]
+            assert np.array_equal(H.to_u16(p.detach()).reshape(-1), model), f"param {k}"
+            assert np.array_equal(H.to_np(st["exp_avg"]).reshape(-1).view(np.uint8), e[2].view(np.uint8))
+            assert np.array_equal(H.to_np(st["exp_avg_sq"]).reshape(-1).view(np.uint8), e[3].view(np.uint8))
+            if self.mode == 1:
+                assert np.array_equal(H.to_np(st["master"]).reshape(-1).view(np.uint8), e[0].view(np.uint8))
+            else:
+                assert np.array_equal(H.to_np(st["remainder"]).reshape(-1), e[4])
+
+
+@pytest.mark.parametrize("master", ["fp32", "remainder"])
+@pytest.mark.parametrize("clip", [0.0, 0.05])
+def test_master_weight_optimizer_matches_the_oracle(master, clip):
+    params = _params()
+    opt = OPT.MasterWeightAdamW(params, master=master, max_grad_norm=clip, lr=2e-4,
+                                betas=(0.9, 0.95), weight_decay=0.1)
+    ref = _MasterOracle(params, master == "remainder")
+    for k in range(1, 6):
+        opt.zero_grad()
+        gs = _grad(k, inf_at=3 if clip else None)
+        for p, g in zip(params, gs):
+            p.grad.copy_(g)
+        opt.step()
+        skipped, norm = ref.step(gs, _hp(opt.param_groups[0]))
+        torch.cuda.synchronize()
+        assert int(opt.last_nonfinite[0].item()) == int(skipped)
+        assert skipped == (clip > 0 and k == 3)
+        assert int(opt.state[params[0]]["step"].item()) == ref.t
+    ref.check(opt, params)
+
+
+def test_master_weight_modes_keep_the_same_trajectory():
+    """The bf16 + remainder master is the fp32 master exactly: after the same
+    steps the fp32 master of one optimizer equals (bf16 parameter, remainder)
+    of the other, joined."""
+    pa, pb = _params(), _params()
+    oa = OPT.MasterWeightAdamW(pa, master="fp32", max_grad_norm=1.0)
+    ob = OPT.MasterWeightAdamW(pb, master="remainder", max_grad_norm=1.0)
+    for k in range(1, 6):
+        for p, q, g in zip(pa, pb, _grad(k)):
+            p.grad.copy_(g)
+            q.grad.copy_(g)
+        oa.step()
+        ob.step()
+    torch.cuda.synchronize()
+    o = O.load()
+    for p, q in zip(pa, pb):
+        joined = o.join_master(H.to_u16(q.detach()).reshape(-1), H.to_np(ob.state[q]["remainder"]).reshape(-1))
+        master = H.to_np(oa.state[p]["master"]).reshape(-1)
+        assert np.array_equal(joined.view(np.uint32), master.view(np.uint32))
+        for name in ("exp_avg", "exp_avg_sq"):
+            assert torch.equal(oa.state[p][name], ob.state[q][name])
