@@ -317,3 +317,43 @@ def test_master_weight_modes_keep_the_same_trajectory():
         assert np.array_equal(joined.view(np.uint32), master.view(np.uint32))
         for name in ("exp_avg", "exp_avg_sq"):
             assert torch.equal(oa.state[p][name], ob.state[q][name])
+
+
+@pytest.mark.parametrize("master", ["fp32", "remainder"])
+def test_master_weight_backward_and_checkpoint(master):
+    """Real backward passes accumulate into the optimizer's gradient buffer,
+    and a checkpoint taken after two steps continues bit for bit in a fresh
+    optimizer over a copy of the model."""
+    torch.manual_seed(1)
+    make = lambda: torch.nn.Sequential(torch.nn.Linear(64, 96), torch.nn.GELU(),
+                                       torch.nn.Linear(96, 8)).cuda().to(torch.bfloat16)
+    ma = make()
+    mb = make()
+    mb.load_state_dict(ma.state_dict())
+    oa = OPT.MasterWeightAdamW(ma.parameters(), master=master, max_grad_norm=1.0)
+    xs = [torch.randn(16, 64, device="cuda", dtype=torch.bfloat16) for _ in range(5)]
+    ptrs = [p.grad.data_ptr() for p in ma.parameters()]
+    for x in xs[:2]:
+        oa.zero_grad()
+        ma(x).float().pow(2).mean().backward()
+        assert [p.grad.data_ptr() for p in ma.parameters()] == ptrs
+        oa.step()
+    buf = io.BytesIO()
+    torch.save({"model": ma.state_dict(), "opt": oa.state_dict()}, buf)
+    buf.seek(0)
+    ck = torch.load(buf, weights_only=False)
+    mb.load_state_dict(ck["model"])
+    ob = OPT.MasterWeightAdamW(mb.parameters(), master=master, max_grad_norm=1.0)
+    ob.load_state_dict(ck["opt"])
+    for x in xs[2:]:
+        for m, o in ((ma, oa), (mb, ob)):
+            o.zero_grad()
+            m(x).float().pow(2).mean().backward()
+            o.step()
+    torch.cuda.synchronize()
+    for p, q in zip(ma.parameters(), mb.parameters()):
+        assert torch.equal(p.view(torch.int16), q.view(torch.int16))
+        for name in oa.state[p]:
+            if name != "step":
+                assert torch.equal(oa.state[p][name].view(torch.uint8), ob.state[q][name].view(torch.uint8))
+    assert oa.state[next(ma.parameters())]["step"].item() == ob.state[next(mb.parameters())]["step"].item() == 5
