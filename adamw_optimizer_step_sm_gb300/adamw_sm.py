@@ -342,11 +342,20 @@ class Plan:
                                             | (0 if fuse else PLAN_NO_FUSE))
         self.device = dev
         self.info = adamw_plan_get_info(self.handle)
+        self.last_nonfinite = None
 
     def step(self, hp: adamw_hparams_t, step: int, grad_norm=None, nonfinite=None,
              stream=None) -> None:
+        """One step at t = ``step``.  A clipped step (hp.max_grad_norm > 0)
+        needs a non-finite flag; without ``nonfinite`` it goes to the plan's
+        own int32 device tensor ``last_nonfinite`` (1: the step was skipped,
+        so the caller must pass the same ``step`` again)."""
         import torch
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if nonfinite is None and hp.max_grad_norm > 0:
+            if self.last_nonfinite is None:
+                self.last_nonfinite = torch.zeros(1, dtype=torch.int32, device=self.device)
+            nonfinite = self.last_nonfinite
         adamw_step(self.handle, hp, step,
                    grad_norm.data_ptr() if grad_norm is not None else 0,
                    nonfinite.data_ptr() if nonfinite is not None else 0,

@@ -387,6 +387,10 @@ extern "C" int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t 
     int rc = make_scalars(hp, step, &s);
     if (rc != ADAMW_OK) return rc;
     const bool clip = hp->max_grad_norm > 0.0f;
+    // A clipped step can be skipped; without the flag the caller could not
+    // tell, would advance t past a step that wrote nothing, and every later
+    // bias correction would be off by one step.
+    if (clip && !d_nonfinite) return ADAMW_ERR_INVALID_ARG;
     const bool need_norm = clip || d_grad_norm != nullptr;
     if (need_norm && !(plan->flags & ADAMW_PLAN_NORM)) return ADAMW_ERR_NO_NORM;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -206,13 +206,15 @@ int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_tensors,
  * d_grad_norm (nullable, device fp64): receives the global gradient L2 norm.
  *   Clipping computes it anyway; without clipping a non-NULL d_grad_norm
  *   costs one extra read of every gradient (and needs ADAMW_PLAN_NORM).
- * d_nonfinite (nullable, device int32): receives 1 if any gradient element is
- *   inf or NaN, else 0.  With clipping on, a 1 means the step wrote nothing.
- *   Without clipping the state is still updated (non-finite values propagate)
- *   and the flag only reports it.
- * Errors: INVALID_ARG (NULL plan/hp, step < 1, hyperparameter out of range),
- * NO_NORM (clipping on a plan made without ADAMW_PLAN_NORM), CUDA (launch
- * failure).  An error return launches nothing. */
+ * d_nonfinite (device int32): receives 1 if any gradient element is inf or
+ *   NaN, else 0.  Required when clipping (hp->max_grad_norm > 0): a 1 then
+ *   means the step wrote nothing, and the caller must pass the same step
+ *   next time.  Nullable without clipping; the state is then still updated
+ *   (non-finite values propagate) and the flag only reports it.
+ * Errors: INVALID_ARG (NULL plan/hp, step < 1, hyperparameter out of range,
+ * clipping with d_nonfinite NULL), NO_NORM (clipping on a plan made without
+ * ADAMW_PLAN_NORM), CUDA (launch failure).  An error return launches
+ * nothing. */
 int adamw_step(adamw_plan_t plan, const adamw_hparams_t* hp, int64_t step,
                double* d_grad_norm, int32_t* d_nonfinite,
                adamw_stream_t stream);
@@ -322,13 +324,16 @@ int adamw_step_scalars(const adamw_hparams_t* hp, int64_t step, float out5[5]);
 
 /* One step over a tensor table the caller already holds in DEVICE memory
  * (d_table: n_tensors adamw_tensor_t entries, read during the call).  The
- * table is copied to the host (the call waits for `stream` to reach that
- * copy) and the plan built for it is kept in a cache of up to 8 plans keyed
- * by the table's bytes, the mode and the current device, so passing the same
- * table every step builds the plan (and allocates) once.  Other arguments and
- * errors as adamw_plan_create and adamw_step (cached plans carry the norm
- * workspace, so clipping is always available).  Thread-safe with respect to
- * the cache; the buffers named by a cached table must outlive its use. */
+ * table is copied to the host, so unlike adamw_step this call BLOCKS the
+ * host until `stream` has reached that copy (one device-to-host read of the
+ * table per call); the step itself is then queued asynchronously.  The plan
+ * built for the table is kept in a cache of up to 8 plans keyed by the
+ * table's bytes, the mode and the current device, so passing the same table
+ * every step builds the plan (and allocates) once.  Other arguments and
+ * errors as adamw_plan_create and adamw_step (d_nonfinite is required when
+ * clipping; cached plans carry the norm workspace, so clipping is always
+ * available).  Thread-safe with respect to the cache; the buffers named by a
+ * cached table must outlive its use. */
 int adamw_step_table(const adamw_tensor_t* d_table, int32_t n_tensors, int32_t mode,
                      const adamw_hparams_t* hp, int64_t step, double* d_grad_norm,
                      int32_t* d_nonfinite, adamw_stream_t stream);

@@ -340,6 +340,41 @@ def test_api_errors_on_gpu():
     plan.close()
 
 
+@pytest.mark.parametrize("fuse", [True, False])
+def test_clipped_step_without_a_flag_is_refused_before_any_launch(fuse):
+    """A clipped step may be skipped, so it must report the non-finite flag:
+    adamw_step refuses it without one (INVALID_ARG) and writes nothing; the
+    Plan wrapper then supplies its own flag tensor."""
+    w = _small("clipflag", sizes=[1000, 70001], mode=W.MODE_MIXED, max_grad_norm=1.0)
+    gpu = H.GpuSide(w)
+    if not fuse:
+        gpu.plan.close()
+        v = gpu.st.views
+        gpu.plan = A.Plan(v(gpu.st.param), v(gpu.g), v(gpu.st.exp_avg), v(gpu.st.exp_avg_sq),
+                          v(gpu.st.aux), w.mode, norm=True, fuse=False)
+    assert gpu.plan.info.fused == (1 if fuse else 0)
+    gpu.set_grad(1)
+    before = [H.to_np(x).copy() for x in (gpu.st.param, gpu.st.exp_avg, gpu.st.exp_avg_sq, gpu.st.aux)]
+    hp = A.hparams(**w.hparams())
+    with pytest.raises(A.AdamWError) as e:
+        A.adamw_step(gpu.plan.handle, hp, 1, gpu.norm.data_ptr(), 0,
+                     torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == A.ADAMW_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    after = [H.to_np(x) for x in (gpu.st.param, gpu.st.exp_avg, gpu.st.exp_avg_sq, gpu.st.aux)]
+    for a, b in zip(before, after):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    # the wrapper's default flag: a step with an inf is skipped and says so
+    gpu.g[3] = float("inf")
+    gpu.plan.step(hp, 1)
+    torch.cuda.synchronize()
+    assert gpu.plan.last_nonfinite is not None and int(gpu.plan.last_nonfinite.item()) == 1
+    # without clipping the flag stays optional
+    A.adamw_step(gpu.plan.handle, A.hparams(), 1, 0, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    gpu.plan.close()
+
+
 def test_copy_probe_copies():
     src = torch.randint(-2**31, 2**31 - 1, (1 << 22,), dtype=torch.int32, device="cuda")
     dst = torch.zeros_like(src)
