@@ -28,6 +28,13 @@ constexpr int kVec = 8;
 #define ADAMW_FUSED_MAX_GRAD_MB 160
 #endif
 constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
+// Elements of its update share whose state (all streams but g) each CTA of
+// the fused clipped step asks L2 for before its norm pass, so that DRAM keeps
+// streaming through the norm pass and the grid barrier (0: none).
+#ifndef ADAMW_FUSED_PREFETCH
+#define ADAMW_FUSED_PREFETCH 8192
+#endif
+constexpr int64_t kFusedPrefetchElems = ADAMW_FUSED_PREFETCH;
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.
 constexpr int64_t kMinElemsPerCta = int64_t(kBlock) * kVec;
@@ -104,9 +111,18 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 #ifndef ADAMW_CUT_ALIGN
 #define ADAMW_CUT_ALIGN 2048
 #endif
+// Granule of the per-CTA quotas: every CTA of the interleaved partition gets
+// the same number of elements to within this many (measured on GB300, the
+// 13.85M-element shard on 304 CTAs was 7 % slower when the quotas went by
+// whole 8K tiles, five tiles for some CTAs and six for others).
+#ifndef ADAMW_BALANCE_ALIGN
+#define ADAMW_BALANCE_ALIGN 256
+#endif
 constexpr int64_t kTileElems = ADAMW_TILE_ELEMS;
 constexpr int64_t kCutAlign = ADAMW_CUT_ALIGN;
+constexpr int64_t kBalanceAlign = ADAMW_BALANCE_ALIGN;
 static_assert(kCutAlign % kVec == 0 && kTileElems % kCutAlign == 0, "tile cut alignment");
+static_assert(kBalanceAlign % kVec == 0 && kCutAlign % kBalanceAlign == 0, "balance granule");
 
 // Output of the norm finalize kernel, read by the clipped update.
 struct NormOut {
@@ -132,6 +148,21 @@ struct StepRecord {
     int32_t skip;
     int32_t pad_[2];
 };
+
+// The per-step scalars of one (hyperparameters, t), remembered on the device
+// by the device-resident step: the first CTA to finish step t computes the
+// scalars of t + 1 into slot (t + 1) & 1 while the others still stream, so
+// that the next step reads them instead of computing them again.  `key` is
+// the bit pattern of the six hyperparameters and of t; `valid` is 0 in a
+// slot never written.  A slot that does not match is recomputed, so the
+// record only saves time, never changes a result.
+struct ScalarMemo {
+    uint32_t key[8];
+    StepScalars s;
+    int32_t valid;
+    int32_t pad_[6];
+};
+static_assert(sizeof(ScalarMemo) == 96, "memo layout");
 
 // Kernel flavours: plain step, clipped step (reads the norm finalize's
 // output, skips on non-finite), plain step that also reports non-finite g.
@@ -178,11 +209,26 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
 // The grid a list of `total` elements gets when at most `max_grid` CTAs fit.
 int32_t choose_grid(int64_t total, int32_t max_grid);
 
-// Tile size of the update kernel's partition for a list of `total` elements
-// on `grid` CTAs (0: contiguous ranges): the multiple of kVec nearest above
-// total / (k * grid), k = the whole number of kTileElems tiles per CTA
-// nearest to total / (grid * kTileElems).
+// Nominal tile of the update kernel's partition for a list of `total`
+// elements on `grid` CTAs: kTileElems when every CTA gets at least two
+// tiles, else 0 (contiguous ranges).
 int64_t update_tile_elems(int64_t total, int32_t grid);
+
+// Sizes of the interleaved partition's tiles.  With k rounds (the whole
+// number nearest to total / (grid * tile_elems)), tile j belongs to CTA
+// j % grid in round j / grid.  Each CTA's quota is total / grid rounded to
+// kBalanceAlign elements (quotas differ by one granule at most); a CTA's k
+// tiles are that quota's whole kCutAlign units shared out as evenly as the
+// rounds allow (earlier rounds take the extra units), and its last-round
+// tile also takes the quota's leftover granules.  Sizes are in the flattened
+// list; the cuts themselves still move to each tensor's alignment grid.
+struct TileSchedule {
+    int32_t grid;
+    int64_t k = 1, base = 0, extra = 0;
+    TileSchedule(int64_t total, int32_t grid, int64_t tile_elems);
+    int64_t size(int64_t j) const;
+    bool last_round(int64_t j) const { return j / grid >= k - 1; }
+};
 
 // Every buffer the mode uses can be dereferenced by `device` (device_access.cpp).
 int check_device_access(const adamw_tensor_t* table, int32_t n, int32_t mode, int device);

@@ -43,7 +43,10 @@ __global__ void __launch_bounds__(kBlock)
 norm_partial_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin,
                     double* __restrict__ partial, int32_t* __restrict__ flag) {
-    norm_partial_cta(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], partial, flag);
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    pdl_trigger();
+    pdl_wait();
+    norm_partial_cta(chunks, c0, c1, partial, flag);
 }
 
 // Stage 2: fixed-order fp64 sum of the partials, norm, clip coefficient.
@@ -51,11 +54,13 @@ __global__ void __launch_bounds__(kBlock)
 norm_finalize_kernel(const double* __restrict__ partial, const int32_t* __restrict__ flag,
                      int32_t n, float max_grad_norm, NormOut* __restrict__ out,
                      double* __restrict__ user_norm, int32_t* __restrict__ user_flag) {
+    pdl_trigger();
+    pdl_wait();
     double x = 0.0;
     bool bad = false;
     for (int32_t i = threadIdx.x; i < n; i += kBlock) {
-        x += partial[i];
-        bad |= flag[i] != 0;
+        x += __ldcg(partial + i);
+        bad |= __ldcg(flag + i) != 0;
     }
     const double tot = block_sum(x);
     const int any = __syncthreads_or(bad);
@@ -77,25 +82,38 @@ norm_finalize_kernel(const double* __restrict__ partial, const int32_t* __restri
 // One CTA, before the update: finalises the norm when n_partials > 0 (the
 // same fixed-order reduction as norm_finalize_kernel), reads the
 // hyperparameters and the applied-step counter from device memory, decides
-// whether the step is skipped, writes the StepRecord, advances the counter
-// for an applied step, and fills the caller's outputs (flag -1 for invalid
-// hyperparameters).
+// whether the step is skipped, takes the scalars from the plan's memo or
+// computes them (warps 0 and 1, one half each), writes the StepRecord,
+// advances the counter for an applied step, and fills the caller's outputs
+// (flag -1 for invalid hyperparameters).
 __global__ void __launch_bounds__(kBlock)
 step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
                      StepRecord* __restrict__ rec, const double* __restrict__ partial,
                      const int32_t* __restrict__ flag, int32_t n_partials, int32_t clip,
                      NormOut* __restrict__ nout, double* __restrict__ user_norm,
-                     int32_t* __restrict__ user_flag) {
+                     int32_t* __restrict__ user_flag, const ScalarMemo* __restrict__ memo) {
+    __shared__ StepScalars s_sh;
+    __shared__ adamw_hparams_t hp_sh;
+    __shared__ int skip_sh, hit_sh, any_sh;
+    __shared__ int64_t t_sh;
+    __shared__ double norm_sh;
+    __shared__ float coef_sh;
+    pdl_trigger();
+    pdl_wait();
     double x = 0.0;
     bool bad = false;
     for (int32_t i = threadIdx.x; i < n_partials; i += kBlock) {
-        x += partial[i];
-        bad |= flag[i] != 0;
+        x += __ldcg(partial + i);
+        bad |= __ldcg(flag + i) != 0;
     }
     const double tot = block_sum(x);
     const int any = __syncthreads_or(bad);
+    adamw_hparams_t hp;
+    int64_t t = 0;
+    StepScalars s;
+    bool hit = false;
+    if (threadIdx.x < 32) hit = memo_fetch_warp(d_hp, d_step, memo, &hp, &t, &s);
     if (threadIdx.x == 0) {
-        const adamw_hparams_t hp = *d_hp;
         const bool valid = hparams_valid_dev(hp);
         const double norm = sqrt(tot);
         float coef = 1.0f;
@@ -104,22 +122,34 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
             if (c > 1.0) c = 1.0;
             coef = float(c);
         }
+        const int skip = !valid ? 2 : (clip && any) ? 1 : 0;
+        hit_sh = skip ? 1 : hit;
+        if (!skip && hit) s_sh = s;
+        hp_sh = hp;
+        skip_sh = skip;
+        t_sh = t;
+        norm_sh = norm;
+        coef_sh = coef;
+        any_sh = any;
+    }
+    __syncthreads();
+    if (!hit_sh) make_scalars_cta(hp_sh, t_sh, &s_sh);
+    if (threadIdx.x == 0) {
         StepRecord r{};
-        r.skip = !valid ? 2 : (clip && any) ? 1 : 0;
-        r.coef = coef;
+        r.skip = skip_sh;
+        r.coef = coef_sh;
         if (!r.skip) {
-            const int64_t t = *d_step + 1;
-            make_scalars_dev(hp, t, &r.s);
-            *d_step = t;
+            r.s = s_sh;
+            *d_step = t_sh;
         }
         *rec = r;
         if (n_partials > 0) {
-            nout->norm = norm;
-            nout->coef = coef;
-            nout->nonfinite = any;
-            if (user_norm) *user_norm = norm;
+            nout->norm = norm_sh;
+            nout->coef = coef_sh;
+            nout->nonfinite = any_sh;
+            if (user_norm) *user_norm = norm_sh;
         }
-        if (user_flag) *user_flag = !valid ? -1 : (n_partials > 0 ? any : 0);
+        if (user_flag) *user_flag = skip_sh == 2 ? -1 : (n_partials > 0 ? any_sh : 0);
     }
 }
 
@@ -128,7 +158,10 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
 __global__ void lr_linear_warmup_kernel(adamw_hparams_t* __restrict__ d_hp,
                                         const int64_t* __restrict__ d_step, float base_lr,
                                         int64_t warmup, int64_t total) {
-    const int64_t k = *d_step;  // applied updates before this one
+    if (threadIdx.x != 0) return;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t k = __ldcg(d_step);  // applied updates before this one
     double f;
     if (k < warmup) {
         f = __ddiv_rn(double(k), double(warmup > 1 ? warmup : 1));
@@ -245,13 +278,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 cudaError_t launch_norm(const adamw_plan* P, float max_grad_norm, double* user_norm,
                         int32_t* user_flag, cudaStream_t st) {
-    norm_partial_kernel<<<P->nrm.grid, kBlock, 0, st>>>(P->nrm.chunks, P->nrm.cta_begin,
-                                                        P->partial, P->flag);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(norm_partial_kernel, P->nrm.grid, st, P->nrm.chunks,
+                                  P->nrm.cta_begin, P->partial, P->flag);
     if (e != cudaSuccess) return e;
-    norm_finalize_kernel<<<1, kBlock, 0, st>>>(P->partial, P->flag, P->nrm.grid, max_grad_norm,
-                                               P->norm, user_norm, user_flag);
-    return cudaGetLastError();
+    return launch_kernel(norm_finalize_kernel, 1, st, P->partial, P->flag, P->nrm.grid,
+                         max_grad_norm, P->norm, user_norm, user_flag);
 }
 
 }  // namespace
@@ -333,6 +364,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
     const size_t o_a = off; off = align_up(off + sizeof(unsigned long long), 256);
     const size_t o_d = off; off = align_up(off + 2 * sizeof(uint32_t), 256);
+    const size_t o_m = off; off = align_up(off + 2 * sizeof(ScalarMemo), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;
@@ -352,6 +384,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->arrivals = reinterpret_cast<unsigned long long*>(b + o_a);
     P->done = reinterpret_cast<unsigned int*>(b + o_d);
     P->flagword = reinterpret_cast<int32_t*>(b + o_d + sizeof(uint32_t));
+    P->memo = reinterpret_cast<ScalarMemo*>(b + o_m);
     P->fused = fused;
 #if ADAMW_CHECK_BOUNDS
     for (ChunkPtr& c : cp) c.status = P->status;
@@ -475,15 +508,15 @@ extern "C" int adamw_step_device(adamw_plan_t plan, const adamw_hparams_t* d_hp,
         return cuda_ok(e, "update launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
     }
     const bool norm_pass = want_norm && plan->nrm.grid > 0;
-    if (norm_pass) {
-        norm_partial_kernel<<<plan->nrm.grid, kBlock, 0, st>>>(plan->nrm.chunks, plan->nrm.cta_begin,
-                                                               plan->partial, plan->flag);
-        if (!cuda_ok(cudaGetLastError(), "norm launch")) return ADAMW_ERR_CUDA;
-    }
-    step_prologue_kernel<<<1, kBlock, 0, st>>>(d_hp, d_step, plan->rec, plan->partial, plan->flag,
-                                               norm_pass ? plan->nrm.grid : 0, clip ? 1 : 0,
-                                               plan->norm, d_grad_norm, d_nonfinite);
-    if (!cuda_ok(cudaGetLastError(), "prologue launch")) return ADAMW_ERR_CUDA;
+    if (norm_pass &&
+        !cuda_ok(launch_kernel(norm_partial_kernel, plan->nrm.grid, st, plan->nrm.chunks,
+                               plan->nrm.cta_begin, plan->partial, plan->flag), "norm launch"))
+        return ADAMW_ERR_CUDA;
+    if (!cuda_ok(launch_kernel(step_prologue_kernel, 1, st, d_hp, d_step, plan->rec, plan->partial,
+                               plan->flag, norm_pass ? plan->nrm.grid : 0, clip ? 1 : 0, plan->norm,
+                               d_grad_norm, d_nonfinite, plan->memo),
+                 "prologue launch"))
+        return ADAMW_ERR_CUDA;
     if (want_norm && !norm_pass && d_grad_norm &&
         !cuda_ok(cudaMemsetAsync(d_grad_norm, 0, sizeof(double), st), "memset"))
         return ADAMW_ERR_CUDA;
@@ -500,9 +533,10 @@ extern "C" int adamw_lr_linear_warmup_device(adamw_hparams_t* d_hp, const int64_
                                              adamw_stream_t stream) {
     if (!d_hp || !d_step || warmup < 0 || total < 0 || !std::isfinite(base_lr))
         return ADAMW_ERR_INVALID_ARG;
-    lr_linear_warmup_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        d_hp, d_step, base_lr, warmup, total);
-    return cuda_ok(cudaGetLastError(), "schedule launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
+    // one thread of a kBlock launch does the work
+    return cuda_ok(launch_kernel(lr_linear_warmup_kernel, 1, reinterpret_cast<cudaStream_t>(stream),
+                                 d_hp, d_step, base_lr, warmup, total),
+                   "schedule launch") ? ADAMW_OK : ADAMW_ERR_CUDA;
 }
 
 extern "C" int adamw_plan_device_status(adamw_plan_t plan, int32_t* out) {
@@ -616,21 +650,30 @@ extern "C" int adamw_copy_probe(void* dst, const void* src, int64_t bytes, adamw
 //
 // adamw_grad_norm_noalloc is adamw_grad_norm for callers that cannot allocate
 // device memory.  Instead of a plan's cudaMalloc'd workspace it uses one
-// file-scope __device__ array (the uploaded tensor list, the per-CTA partials
-// and flags, and the finalize record), so a call allocates nothing.  Every GPU
-// that loads this library holds the array until the process exits.
+// file-scope __device__ array (the tensor list, the per-CTA partials and
+// flags, and the finalize record), so a call allocates nothing.  Every GPU
+// that loads this library holds the array until the process exits.  The
+// list reaches the device as kernel launch parameters, which the runtime
+// copies when the launch is made, so the caller's table is not read after
+// the call returns.
 
 namespace {
+
+// One tensor of the no-alloc list on the device.
+struct NoAllocEntry {
+    const uint16_t* grad;
+    int64_t numel;
+};
 
 constexpr int kNoAllocMaxCtas = 1024;
 constexpr size_t kNoAllocTableOff = 0;
 constexpr size_t kNoAllocPartialOff =
-    (sizeof(adamw_tensor_t) * ADAMW_NOALLOC_MAX_TENSORS + 255) / 256 * 256;
+    (sizeof(NoAllocEntry) * ADAMW_NOALLOC_MAX_TENSORS + 255) / 256 * 256;
 constexpr size_t kNoAllocFlagOff = kNoAllocPartialOff + sizeof(double) * kNoAllocMaxCtas;
 constexpr size_t kNoAllocOutOff = kNoAllocFlagOff + sizeof(int32_t) * kNoAllocMaxCtas;
 constexpr size_t kNoAllocBytes = (kNoAllocOutOff + sizeof(NormOut) + 255) / 256 * 256;
 
-// The scratch (about 208 KiB).  Host code never uses this name as an address:
+// The scratch (about 76 KiB).  Host code never uses this name as an address:
 // on the host it is only a stand-in; noalloc_device() asks the runtime for the
 // device address.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
@@ -646,22 +689,60 @@ struct NoAllocDevice {
 std::mutex g_noalloc_mu;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
+// Up to CAP entries of the list, passed by value as the parameters of one
+// launch (the large form is just under the 32 KiB parameter limit).
+template <int CAP>
+struct NoAllocPiece {
+    int32_t first, count;
+    const uint16_t* grad[CAP];
+    int64_t numel[CAP];
+};
+constexpr int kNoAllocSmallPiece = 128;
+constexpr int kNoAllocLargePiece = 2000;
+static_assert(sizeof(NoAllocPiece<kNoAllocLargePiece>) <= 32764, "launch parameter limit");
+
+// Writes one piece of the list into the scratch's table.
+template <int CAP>
+__global__ void __launch_bounds__(kBlock)
+noalloc_table_kernel(const __grid_constant__ NoAllocPiece<CAP> piece, NoAllocEntry* __restrict__ table) {
+    pdl_trigger();
+    pdl_wait();
+    for (int32_t i = threadIdx.x; i < piece.count; i += kBlock)
+        table[piece.first + i] = NoAllocEntry{piece.grad[i], piece.numel[i]};
+}
+
+template <int CAP>
+cudaError_t upload_noalloc_piece(const adamw_tensor_t* host_table, int32_t first, int32_t count,
+                                 NoAllocEntry* table, cudaStream_t st) {
+    NoAllocPiece<CAP> piece;
+    piece.first = first;
+    piece.count = count;
+    for (int32_t i = 0; i < count; ++i) {
+        piece.grad[i] = static_cast<const uint16_t*>(host_table[first + i].grad);
+        piece.numel[i] = host_table[first + i].numel;
+    }
+    return launch_kernel(noalloc_table_kernel<CAP>, 1, st, piece, table);
+}
+
 // Stage 1 without a chunk table: tensor by tensor in list order, every thread
 // of the grid takes a fixed share of each tensor (an element of the head that
 // 16-byte aligns g, vectors strided by the whole grid, an element of the
 // tail).  Sums as in norm_partial_kernel: error-free fp32 groups of exact
 // squares, an fp64 recomputation for threads whose groups leave the safe range.
 __global__ void __launch_bounds__(kBlock)
-norm_partial_noalloc_kernel(const adamw_tensor_t* __restrict__ table, int32_t n,
+norm_partial_noalloc_kernel(const NoAllocEntry* __restrict__ table, int32_t n,
                             double* __restrict__ partial, int32_t* __restrict__ flag) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t gt = int64_t(blockIdx.x) * kBlock + threadIdx.x;
     const int64_t T = int64_t(gridDim.x) * kBlock;
     constexpr int U = 4;
 
     auto walk = [&](auto vec, auto elem, auto after_iter) {
         for (int32_t k = 0; k < n; ++k) {
-            const uint16_t* g = static_cast<const uint16_t*>(table[k].grad);
-            const int64_t len = table[k].numel;
+            const uint16_t* g = reinterpret_cast<const uint16_t*>(
+                __ldcg(reinterpret_cast<const unsigned long long*>(&table[k].grad)));
+            const int64_t len = __ldcg(&table[k].numel);
             if (len <= 0) continue;
             int64_t h = int64_t((16 - (reinterpret_cast<uintptr_t>(g) & 15)) & 15) >> 1;
             if (h > len) h = len;
@@ -782,20 +863,34 @@ extern "C" int adamw_grad_norm_noalloc(const adamw_tensor_t* host_table, int32_t
     if (rc != ADAMW_OK) return rc;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    adamw_tensor_t* table = reinterpret_cast<adamw_tensor_t*>(d.base + kNoAllocTableOff);
+    NoAllocEntry* table = reinterpret_cast<NoAllocEntry*>(d.base + kNoAllocTableOff);
     double* partial = reinterpret_cast<double*>(d.base + kNoAllocPartialOff);
     int32_t* flag = reinterpret_cast<int32_t*>(d.base + kNoAllocFlagOff);
     NormOut* out = reinterpret_cast<NormOut*>(d.base + kNoAllocOutOff);
     // Every CTA writes its partial and flag and the finalize writes the
     // record on every call, so nothing in the scratch has to start at zero.
-    if (n_tensors > 0 &&
-        !cuda_ok(cudaMemcpyAsync(table, host_table, sizeof(adamw_tensor_t) * size_t(n_tensors),
-                                 cudaMemcpyHostToDevice, st), "cudaMemcpyAsync(table)"))
+    // The list goes in the launch parameters of one or more small kernels
+    // (copied by the runtime when each launch is made).
+    for (int32_t first = 0; first < n_tensors;) {
+        const int32_t left = n_tensors - first;
+        const cudaError_t e =
+            left <= kNoAllocSmallPiece
+                ? upload_noalloc_piece<kNoAllocSmallPiece>(host_table, first, left, table, st)
+                : upload_noalloc_piece<kNoAllocLargePiece>(
+                      host_table, first, left < kNoAllocLargePiece ? left : kNoAllocLargePiece,
+                      table, st);
+        if (!cuda_ok(e, "table launch")) return ADAMW_ERR_CUDA;
+        first += left <= kNoAllocSmallPiece ? left
+                 : (left < kNoAllocLargePiece ? left : kNoAllocLargePiece);
+    }
+    if (!cuda_ok(launch_kernel(norm_partial_noalloc_kernel, d.grid, st,
+                               static_cast<const NoAllocEntry*>(table), n_tensors, partial, flag),
+                 "norm launch"))
         return ADAMW_ERR_CUDA;
-    norm_partial_noalloc_kernel<<<d.grid, kBlock, 0, st>>>(table, n_tensors, partial, flag);
-    if (!cuda_ok(cudaGetLastError(), "norm launch")) return ADAMW_ERR_CUDA;
-    norm_finalize_kernel<<<1, kBlock, 0, st>>>(partial, flag, d.grid, 0.0f, out, d_grad_norm,
-                                               d_nonfinite);
-    if (!cuda_ok(cudaGetLastError(), "finalize launch")) return ADAMW_ERR_CUDA;
+    if (!cuda_ok(launch_kernel(norm_finalize_kernel, 1, st, static_cast<const double*>(partial),
+                               static_cast<const int32_t*>(flag), d.grid, 0.0f, out, d_grad_norm,
+                               d_nonfinite),
+                 "finalize launch"))
+        return ADAMW_ERR_CUDA;
     return ADAMW_OK;
 }

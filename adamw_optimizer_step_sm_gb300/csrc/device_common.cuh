@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 
@@ -77,6 +78,17 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
     *q = v;
 #endif
 }
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization (launch.h), so it may start while
+// the kernel before it in the stream is still running: it may read only what
+// no earlier kernel writes (the plan's chunk table) before pdl_wait(), which
+// returns once every earlier kernel has finished and its writes are visible.
+// pdl_trigger() lets the next kernel launch before this one ends (it waits
+// in pdl_wait() all the same).  Both are no-ops for a kernel launched
+// without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 __device__ __forceinline__ bool bf16x2_nonfinite(uint32_t w) {
     return ((w & 0x7f80u) == 0x7f80u) || ((w & 0x7f800000u) == 0x7f800000u);
@@ -190,6 +202,12 @@ struct UpdateTuning {
 #else
     static constexpr int kMinBlocks = kB;
 #endif
+    // The one-launch device step runs on the update's grid, so it must reach
+    // the same occupancy.  Left to itself it does in every mode but bf16
+    // without compensation, whose update fits 64 registers (4 CTAs per SM)
+    // and whose device step would take 70.
+    static constexpr int kSelfMinBlocks =
+        (kMinBlocks == 0 && MODE == ADAMW_MODE_BF16_PLAIN) ? 4 : kMinBlocks;
 };
 
 template <int K, int U>
@@ -820,6 +838,7 @@ __device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t 
 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
 #define ADAMW_UPDATE_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kMinBlocks)
+#define ADAMW_SELF_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kSelfMinBlocks)
 
 // One chunk descriptor, read through the read-only path.
 __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
@@ -839,10 +858,10 @@ __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
 #endif
 }
 
-#if ADAMW_CHECK_BOUNDS
 // Bytes per element of stream s (param, grad, exp_avg, exp_avg_sq, aux) in
 // storage mode MODE, 0 for a stream the mode does not use; written out here
-// independently of the host planner's table, so the check cross-checks it.
+// independently of the host planner's table, so the bounds check
+// cross-checks it.
 template <int MODE>
 __device__ constexpr int stream_bytes(int s) {
     if (MODE >= ADAMW_MODE_ANYPREC) {
@@ -857,6 +876,7 @@ __device__ constexpr int stream_bytes(int s) {
     return 2;
 }
 
+#if ADAMW_CHECK_BOUNDS
 // Whether the chunk's `len` elements lie inside its tensor's buffers, for
 // every stream of MODE selected by `mask` (bit s = stream s).  A chunk that
 // does not is reported in the plan's status word; the caller skips it.
@@ -878,14 +898,12 @@ __device__ __forceinline__ bool chunk_in_bounds(const ChunkPtr& c, int64_t len, 
 #endif
 
 // ---- the CTA's share of the update: chunks [c0, c1), each chunk's
-// descriptor fetched one ahead.
+// descriptor fetched one ahead; `cur` holds chunk c0 already (when c0 < c1).
 template <int MODE, int K>
-__device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
-                                           int32_t c1, const StepScalars& s, float coef,
-                                           bool& bad) {
+__device__ __forceinline__ void update_cta_from(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                                int32_t c1, ChunkPtr cur, const StepScalars& s,
+                                                float coef, bool& bad) {
     constexpr int kU = UpdateTuning<MODE>::kUnroll;
-    ChunkPtr cur;
-    if (c0 < c1) cur = load_chunk(chunks + c0);
     for (int32_t ci = c0; ci < c1; ++ci) {
         ChunkPtr nxt = cur;
         if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
@@ -919,6 +937,15 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
         }
         cur = nxt;
     }
+}
+
+template <int MODE, int K>
+__device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                           int32_t c1, const StepScalars& s, float coef,
+                                           bool& bad) {
+    ChunkPtr cur;
+    if (c0 < c1) cur = load_chunk(chunks + c0);
+    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad);
 }
 
 // Error-free fp32 accumulation of non-negative terms: s + e is the exact sum
@@ -1068,6 +1095,38 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
     }
 }
 
+// Asks L2 for the first `budget` elements of the CTA's update chunks
+// [c0, c1) of every stream the update reads except g (which the norm pass
+// just brought in): p (or the master), m, v and the aux stream where the
+// mode reads it.  One prefetch per 128-byte line, every address inside its
+// buffer; a hint only, so it changes no result.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+template <int MODE>
+__device__ __forceinline__ void prefetch_update_state(const ChunkPtr* __restrict__ chunks,
+                                                      int32_t c0, int32_t c1, int64_t budget) {
+    constexpr bool kReadsAux = MODE != ADAMW_MODE_MIXED_FP32_MASTER && stream_bytes<MODE>(4) != 0;
+    for (int32_t ci = c0; ci < c1 && budget > 0; ++ci) {
+        const ChunkPtr ch = load_chunk(chunks + ci);
+        int64_t len = ch.len2 >> 1;
+        if (len > budget) len = budget;
+        budget -= len;
+        const void* ptr[4] = {ch.p, ch.m, ch.v, ch.a};
+        const int es[4] = {stream_bytes<MODE>(0), stream_bytes<MODE>(2), stream_bytes<MODE>(3),
+                           stream_bytes<MODE>(4)};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k == 3 && !kReadsAux) continue;
+            const char* b = static_cast<const char*>(ptr[k]);
+            const int64_t bytes = len * es[k];
+            for (int64_t off = int64_t(threadIdx.x) * 128; off < bytes; off += int64_t(kBlock) * 128)
+                prefetch_l2(b + off);
+        }
+    }
+}
+
 // ---- device-resident step path ----
 
 // beta^t by binary exponentiation, lowest bit of t first, one IEEE fp64
@@ -1089,20 +1148,116 @@ __device__ bool hparams_valid_dev(const adamw_hparams_t& hp) {
            hp.beta1 < 1.0f && hp.beta2 >= 0.0f && hp.beta2 < 1.0f;
 }
 
-// The host planner's make_scalars, operation for operation.
+// The host planner's make_scalars, operation for operation, in two halves
+// that share nothing, so that two warps can evaluate them at once: part 0
+// the beta1 side (step_size, omb1) plus the values copied or derived from lr,
+// eps, weight_decay and max_grad_norm; part 1 the beta2 side (sbc2, omb2).
+__device__ __noinline__ void make_scalars_part(const adamw_hparams_t& hp, int64_t t, int part,
+                                  StepScalars* out) {
+    if (part == 0) {
+        const double b1 = hp.beta1;
+        const double bc1 = __dsub_rn(1.0, beta_power_dev(b1, t));
+        out->beta1 = hp.beta1;
+        out->omb1 = __double2float_rn(__dsub_rn(1.0, b1));
+        out->step_size = __double2float_rn(__ddiv_rn(double(hp.lr), bc1));
+        out->eps = hp.eps;
+        out->lrwd = __double2float_rn(__dmul_rn(double(hp.lr), double(hp.weight_decay)));
+        out->max_grad_norm = hp.max_grad_norm;
+    } else {
+        const double b2 = hp.beta2;
+        const double bc2 = __dsub_rn(1.0, beta_power_dev(b2, t));
+        out->beta2 = hp.beta2;
+        out->omb2 = __double2float_rn(__dsub_rn(1.0, b2));
+        out->sbc2 = __double2float_rn(__dsqrt_rn(bc2));
+    }
+}
+
 __device__ void make_scalars_dev(const adamw_hparams_t& hp, int64_t t, StepScalars* out) {
-    const double b1 = hp.beta1, b2 = hp.beta2;
-    const double bc1 = __dsub_rn(1.0, beta_power_dev(b1, t));
-    const double bc2 = __dsub_rn(1.0, beta_power_dev(b2, t));
-    out->beta1 = hp.beta1;
-    out->beta2 = hp.beta2;
-    out->omb1 = __double2float_rn(__dsub_rn(1.0, b1));
-    out->omb2 = __double2float_rn(__dsub_rn(1.0, b2));
-    out->step_size = __double2float_rn(__ddiv_rn(double(hp.lr), bc1));
-    out->sbc2 = __double2float_rn(__dsqrt_rn(bc2));
-    out->eps = hp.eps;
-    out->lrwd = __double2float_rn(__dmul_rn(double(hp.lr), double(hp.weight_decay)));
-    out->max_grad_norm = hp.max_grad_norm;
+    make_scalars_part(hp, t, 0, out);
+    make_scalars_part(hp, t, 1, out);
+}
+
+// Scalar memo (ScalarMemo): the key of (hp, t), and a lookup.
+__device__ __forceinline__ void memo_key(const adamw_hparams_t& hp, int64_t t, uint32_t k[8]) {
+    k[0] = __float_as_uint(hp.lr);
+    k[1] = __float_as_uint(hp.beta1);
+    k[2] = __float_as_uint(hp.beta2);
+    k[3] = __float_as_uint(hp.eps);
+    k[4] = __float_as_uint(hp.weight_decay);
+    k[5] = __float_as_uint(hp.max_grad_norm);
+    k[6] = uint32_t(uint64_t(t));
+    k[7] = uint32_t(uint64_t(t) >> 32);
+}
+
+// Reads the hyperparameters, the applied-step counter and both memo slots
+// with one load (or two) per lane of the calling warp -- one round trip to
+// L2, few registers per lane; all were written by earlier kernels, so the
+// reads go around L1 -- then picks the slot of t = *d_step + 1.  Every lane
+// of the warp must call it; every lane gets *hp, *t and the result: whether
+// the slot holds the scalars of (*hp, t), which are then in *out.
+__device__ __forceinline__ bool memo_fetch_warp(const adamw_hparams_t* __restrict__ d_hp,
+                                                const int64_t* __restrict__ d_step,
+                                                const ScalarMemo* __restrict__ memo,
+                                                adamw_hparams_t* hp, int64_t* t, StepScalars* out) {
+    // words: [0, 6) hp, [6, 8) the counter, then kSlot words of each slot
+    constexpr int kSlot = int((offsetof(ScalarMemo, valid) + sizeof(int32_t)) / sizeof(uint32_t));
+    constexpr int kTotal = 8 + 2 * kSlot;
+    static_assert(kTotal <= 64, "two words per lane");
+    constexpr int kKey = int(offsetof(ScalarMemo, key) / sizeof(uint32_t));
+    constexpr int kS = int(offsetof(ScalarMemo, s) / sizeof(uint32_t));
+    constexpr int kValid = int(offsetof(ScalarMemo, valid) / sizeof(uint32_t));
+    const int lane = threadIdx.x & 31;
+    auto addr = [&](int i) -> const uint32_t* {
+        if (i < 6) return reinterpret_cast<const uint32_t*>(d_hp) + i;
+        if (i < 8) return reinterpret_cast<const uint32_t*>(d_step) + (i - 6);
+        const int j = i - 8;
+        return reinterpret_cast<const uint32_t*>(memo + j / kSlot) + j % kSlot;
+    };
+    const uint32_t w0 = __ldcg(addr(lane));
+    const uint32_t w1 = (32 + lane < kTotal) ? __ldcg(addr(32 + lane)) : 0u;
+    auto word = [&](int i) {  // word i of the concatenation, i the same in every lane
+        return i < 32 ? __shfl_sync(0xffffffffu, w0, i) : __shfl_sync(0xffffffffu, w1, i - 32);
+    };
+    uint32_t h[6];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) h[i] = word(i);
+    memcpy(hp, h, sizeof(h));
+    *t = int64_t(uint64_t(word(6)) | (uint64_t(word(7)) << 32)) + 1;
+    const int base = 8 + int(*t & 1) * kSlot;
+    uint32_t k[8];
+    memo_key(*hp, *t, k);
+    bool hit = word(base + kValid) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hit &= word(base + kKey + i) == k[i];
+    uint32_t sw[sizeof(StepScalars) / sizeof(uint32_t)];
+#pragma unroll
+    for (int i = 0; i < int(sizeof(sw) / sizeof(uint32_t)); ++i) sw[i] = word(base + kS + i);
+    if (hit) memcpy(out, sw, sizeof(StepScalars));
+    return hit;
+}
+
+// Computes the scalars of (hp, t) with warps 0 and 1 of the CTA (one half
+// each, see make_scalars_part) into shared *sh; every thread of the CTA
+// must call it, and it ends with a barrier.
+__device__ __forceinline__ void make_scalars_cta(const adamw_hparams_t& hp, int64_t t,
+                                                 StepScalars* sh) {
+    if (threadIdx.x == 0) make_scalars_part(hp, t, 0, sh);
+    else if (threadIdx.x == 32) make_scalars_part(hp, t, 1, sh);
+    __syncthreads();
+}
+
+// Writes the scalars of (hp, t), already in *s, into their memo slot (one
+// thread; the scalars first, then the key, then the valid word).
+__device__ __forceinline__ void memo_store(ScalarMemo* memo, const adamw_hparams_t& hp, int64_t t,
+                                           const StepScalars& s) {
+    ScalarMemo* m = memo + (t & 1);
+    uint32_t k[8];
+    memo_key(hp, t, k);
+    m->valid = 0;
+    m->s = s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m->key[i] = k[i];
+    m->valid = 1;
 }
 
 // ---- fused clipped step (one cooperative launch) ----

@@ -16,17 +16,24 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
                     const NormOut* __restrict__ norm, int32_t* __restrict__ report,
                     const StepRecord* __restrict__ rec) {
+    // the chunk table is written once, when the plan is made: read the first
+    // descriptor before waiting for the kernel this one may overlap
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    ChunkPtr cur;
+    if (c0 < c1) cur = load_chunk(chunks + c0);
+    pdl_trigger();
+    pdl_wait();
     float coef = 1.0f;
     if (DEV) {
-        if (rec->skip) return;        // skipped step: no writes at all
+        if (__ldcg(&rec->skip)) return;   // skipped step: no writes at all
         s = rec->s;
         coef = rec->coef;
     } else if (K == kClip) {
-        if (norm->nonfinite) return;  // skipped step: no writes at all
+        if (__ldcg(&norm->nonfinite)) return;  // skipped step: no writes at all
         coef = norm->coef;
     }
     bool bad = false;
-    update_cta<MODE, K>(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], s, coef, bad);
+    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad);
     if (K == kReport) {
         if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
     }
@@ -34,44 +41,70 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
 
 // ---- device-resident step without a norm pass: one launch ----
 //
-// Every CTA reads the hyperparameters and the step counter itself and
-// computes the scalars (the host planner's fp64 operations); the last CTA to
-// finish -- found with an arrival counter -- advances the counter and writes
-// the non-finite flag, so no CTA can read a counter that was already
-// advanced.  Invalid hyperparameters: nothing is updated, the flag is -1.
+// Thread 0 of every CTA reads the hyperparameters and the step counter and
+// looks up the scalars of t = *d_step + 1 in the plan's two-slot memo; on a
+// miss warps 0 and 1 compute them (the host planner's fp64 operations, two
+// independent halves at once).  The first CTA to finish its share computes
+// the scalars of t + 1 into the memo while the others still stream (so a
+// run of steps with unchanged hyperparameters computes each step's scalars
+// off the critical path); the last CTA to finish -- found with an arrival
+// counter -- advances the counter and writes the non-finite flag, so no CTA
+// can read a counter that was already advanced.  Invalid hyperparameters:
+// nothing is updated, the flag is -1.
 template <int MODE, int K>
-__global__ void ADAMW_UPDATE_BOUNDS(MODE)
+__global__ void ADAMW_SELF_BOUNDS(MODE)
 adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
                          const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
                          unsigned int* __restrict__ done, int32_t* __restrict__ flagword,
-                         int32_t* __restrict__ user_flag) {
+                         int32_t* __restrict__ user_flag, ScalarMemo* __restrict__ memo) {
     __shared__ StepScalars s_sh;
-    __shared__ int valid_sh;
+    __shared__ adamw_hparams_t hp_sh;
+    __shared__ int valid_sh, hit_sh;
     __shared__ int64_t t_sh;
-    if (threadIdx.x == 0) {
-        const adamw_hparams_t hp = *d_hp;
-        const int valid = hparams_valid_dev(hp);
-        const int64_t t = __ldcg(d_step) + 1;
-        if (valid) make_scalars_dev(hp, t, &s_sh);
-        valid_sh = valid;
-        t_sh = t;
+    __shared__ unsigned int ticket_sh;
+    const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
+    ChunkPtr cur;
+    if (c0 < c1) cur = load_chunk(chunks + c0);
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x < 32) {
+        adamw_hparams_t hp;
+        int64_t t;
+        StepScalars s;
+        const bool hit = memo_fetch_warp(d_hp, d_step, memo, &hp, &t, &s);
+        if (threadIdx.x == 0) {
+            const int valid = hparams_valid_dev(hp);
+            hit_sh = valid && hit;
+            if (valid && hit) s_sh = s;
+            hp_sh = hp;
+            valid_sh = valid;
+            t_sh = t;
+        }
     }
     __syncthreads();
+    if (valid_sh && !hit_sh) make_scalars_cta(hp_sh, t_sh, &s_sh);
     bool bad = false;
-    if (valid_sh)
-        update_cta<MODE, K>(chunks, cta_begin[blockIdx.x], cta_begin[blockIdx.x + 1], s_sh, 1.0f,
-                            bad);
+    if (valid_sh) update_cta_from<MODE, K>(chunks, c0, c1, cur, s_sh, 1.0f, bad);
     const int any = (K == kReport) ? __syncthreads_or(bad) : 0;
     if (threadIdx.x == 0) {
         if (any) atomicOr(flagword, 1);
         __threadfence();
-        if (atomicAdd(done, 1u) == gridDim.x - 1) {  // the last CTA
-            __threadfence();
-            const int32_t f = atomicExch(flagword, 0);
-            if (valid_sh) *d_step = t_sh;
-            if (user_flag) *user_flag = valid_sh ? f : -1;
-            *done = 0;
-        }
+        ticket_sh = atomicAdd(done, 1u);
+    }
+    __syncthreads();
+    const unsigned int ticket = ticket_sh;
+    if (ticket == 0 && valid_sh) {
+        // the first CTA done: the next step's scalars, for the memo
+        __shared__ StepScalars next_sh;
+        make_scalars_cta(hp_sh, t_sh + 1, &next_sh);
+        if (threadIdx.x == 0) memo_store(memo, hp_sh, t_sh + 1, next_sh);
+    }
+    if (threadIdx.x == 0 && ticket == gridDim.x - 1) {  // the last CTA
+        __threadfence();
+        const int32_t f = atomicExch(flagword, 0);
+        if (valid_sh) *d_step = t_sh;
+        if (user_flag) *user_flag = valid_sh ? f : -1;
+        *done = 0;
     }
 }
 
@@ -86,6 +119,12 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         int32_t* __restrict__ user_flag, unsigned long long* __restrict__ arrivals,
                         int32_t* __restrict__ status) {
     __shared__ int passed;
+    pdl_wait();
+    // the first elements of the state this CTA updates after the barrier,
+    // fetched into L2 while the norm pass and the barrier run
+    if (kFusedPrefetchElems > 0)
+        prefetch_update_state<MODE>(upd_chunks, upd_begin[blockIdx.x], upd_begin[blockIdx.x + 1],
+                                    kFusedPrefetchElems);
     norm_partial_cta(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1], partial, flag);
     if (threadIdx.x == 0) {
         __threadfence();

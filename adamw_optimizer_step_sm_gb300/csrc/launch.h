@@ -43,9 +43,34 @@ struct adamw_plan {
     unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
     unsigned int* done = nullptr;  // finished CTAs of a one-launch device step
     int32_t* flagword = nullptr;   // its non-finite flag, collected across CTAs
+    adamw::ScalarMemo* memo = nullptr;  // two slots, see ScalarMemo
 };
 
 namespace adamw {
+
+// Every kernel of the library is launched with programmatic stream
+// serialization (programmatic dependent launch): it may begin while the
+// kernel before it in the stream finishes, and waits (griddepcontrol.wait)
+// before it touches memory that kernel may write.  This hides the launch gap
+// between back-to-back steps.  ADAMW_PDL=0 at build time launches plainly.
+#ifndef ADAMW_PDL
+#define ADAMW_PDL 1
+#endif
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(unsigned(kBlock));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ADAMW_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // The launchers of one storage mode.  Every pointer is set.
 struct ModeOps {

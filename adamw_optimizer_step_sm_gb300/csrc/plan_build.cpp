@@ -159,17 +159,31 @@ int32_t choose_grid(int64_t total, int32_t max_grid) {
 int64_t update_tile_elems(int64_t total, int32_t grid) {
     if (kTileElems <= 0 || grid <= 0) return 0;
     if (total < 2 * int64_t(grid) * kTileElems) return 0;
-    // k tiles per CTA, k the nearest whole number to total / (grid * tile);
-    // the tile then stretches (or shrinks) so that k * grid tiles cover the
-    // list: every CTA gets k tiles, and no CTA a (k+1)-th one.
-#if ADAMW_TILE_BALANCE
-    const int64_t per_row = int64_t(grid) * kTileElems;
-    const int64_t k = (total + per_row / 2) / per_row;
-    const int64_t t = (total + k * grid - 1) / (k * grid);
-    return (t + kCutAlign - 1) / kCutAlign * kCutAlign;
-#else
     return kTileElems;
-#endif
+}
+
+TileSchedule::TileSchedule(int64_t total, int32_t grid_, int64_t tile_elems) : grid(grid_) {
+    // k rounds, the whole number nearest to total / (grid * tile_elems)
+    const int64_t per_row = int64_t(grid) * tile_elems;
+    k = (total + per_row / 2) / per_row;
+    if (k < 1) k = 1;
+    // each CTA's quota in units of kBalanceAlign elements, equal to one unit
+    const int64_t units = (total + kBalanceAlign - 1) / kBalanceAlign;
+    base = units / grid;
+    extra = units % grid;
+    // no round without a cut-aligned unit for every CTA
+    const int64_t min_whole = base / (kCutAlign / kBalanceAlign);
+    if (k > min_whole) k = min_whole > 1 ? min_whole : 1;
+}
+
+int64_t TileSchedule::size(int64_t j) const {
+    const int64_t r = j / grid, b = j % grid;
+    const int64_t q = base + (b < extra ? 1 : 0);          // quota, balance units
+    constexpr int64_t per_cut = kCutAlign / kBalanceAlign;
+    const int64_t whole = q / per_cut, rest = q % per_cut;  // cut-aligned units + leftover
+    int64_t sz = (whole / k + (r < whole % k ? 1 : 0)) * kCutAlign;
+    if (r == k - 1) sz += rest * kBalanceAlign;
+    return sz;
 }
 
 int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
@@ -232,23 +246,30 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
 #endif
     if (tile_elems > 0) {
         // Interleaved: cut the flattened list (all segments in order) into
-        // tiles of tile_elems and deal them round-robin to the CTAs, so that
+        // tiles of about tile_elems and deal them round-robin to the CTAs, so that
         // at any moment the whole grid streams one narrow window of each
         // buffer.  A tile that spans a tensor boundary is several chunks of
         // one CTA.  A cut inside a vector body moves up to the next multiple
         // of kCutAlign elements from the body's start (a whole number of
         // 16-byte vectors; coarser alignment keeps warps' accesses on whole
         // cache lines) and the next tile is shorter by as much.
+        // Tile j (round j / grid, CTA j % grid) is sched.size(j) long, so
+        // every CTA's tiles add up to the same quota within kBalanceAlign
+        // elements.  Cuts that end a tile of the last round move up to
+        // kBalanceAlign only (there the quota's leftover is taken), all
+        // others to kCutAlign.
+        const TileSchedule sched(P.total, grid, tile_elems);
         std::vector<ChunkDev> pieces;
         std::vector<int32_t> owner;
-        int64_t flat = 0, boundary = tile_elems, tile = 0;
+        int64_t flat = 0, tile = 0, boundary = sched.size(0);
         for (const Seg& s : segs) {
             int64_t pos = 0;
             while (pos < s.len) {
                 int64_t take = s.len - pos;
                 if (take > boundary - flat) {
                     take = boundary - flat;
-                    if (s.vec) take = (pos + take + kCutAlign - 1) / kCutAlign * kCutAlign - pos;
+                    const int64_t align = sched.last_round(tile) ? kBalanceAlign : kCutAlign;
+                    if (s.vec) take = (pos + take + align - 1) / align * align - pos;
                     if (take > s.len - pos) take = s.len - pos;
                 }
                 pieces.push_back({s.k, s.vec, s.off + pos, take});
@@ -257,7 +278,7 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
                 flat += take;
                 while (flat >= boundary) {
                     ++tile;
-                    boundary += tile_elems;
+                    boundary += sched.size(tile);
                 }
             }
         }

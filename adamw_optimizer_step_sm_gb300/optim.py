@@ -108,6 +108,10 @@ class _GroupBuffers:
             plan_p, plan_aux = list(params), (self.comps if self.comp is not None else None)
         self.plan = A.Plan(plan_p, self.grads, self.exp_avgs, self.exp_avg_sqs, plan_aux, mode,
                            norm=True)
+        # the version counter of each model parameter when its master was
+        # last made to agree with it (the library's own writes to the
+        # parameter do not move the counter; a load or an in-place op does)
+        self.versions = [p._version for p in params]
         self.step = torch.zeros(1, dtype=torch.int64, device=dev)
         self.grad_norm = torch.zeros(1, dtype=torch.float64, device=dev)
         self.nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -171,6 +175,39 @@ class _FlatAdamW(torch.optim.Optimizer):
         if hasattr(self, "_buffers"):
             self._buffers_of(self.param_groups[-1])
 
+    # -- the master copy (MasterWeightAdamW) ----------------------------------
+    def _sync_master(self, b: _GroupBuffers, k: int, p, force: bool) -> None:
+        """Makes parameter k's master agree with the model parameter p again.
+        fp32 master: kept when p is its round-to-nearest-even bf16 value
+        (the parameter was reloaded with what this optimizer wrote), else
+        replaced by p's value.  Remainder: set to zero (the master is p)."""
+        if b.master is not None:
+            m = b.masters[k]
+            if force or not torch.equal(m.to(torch.bfloat16), p.detach()):
+                m.copy_(p.detach())
+        elif self.mode == A.MODE_MIXED_BF16_REMAINDER:
+            b.comps[k].zero_()
+        b.versions[k] = p._version
+
+    def _check_masters(self, group, b: _GroupBuffers) -> None:
+        if self.mode not in (A.MODE_MIXED_FP32_MASTER, A.MODE_MIXED_BF16_REMAINDER):
+            return
+        for k, p in enumerate(group["params"]):
+            if p._version != b.versions[k]:
+                self._sync_master(b, k, p, force=False)
+
+    @torch.no_grad()
+    def sync_master(self) -> None:
+        """Re-derives every master copy from the model's current bf16
+        parameters (fp32 master = the parameter's value; remainder = 0).
+        ``step`` does this by itself for a parameter changed in place (a
+        model ``load_state_dict``, ``p.copy_``); call it after changing a
+        parameter through ``p.data``, which ``step`` cannot see."""
+        for group in self.param_groups:
+            b = self._buffers_of(group)
+            for k, p in enumerate(group["params"]):
+                self._sync_master(b, k, p, force=True)
+
     # -- the step -----------------------------------------------------------
     @torch.no_grad()
     def step(self, closure=None):
@@ -180,6 +217,7 @@ class _FlatAdamW(torch.optim.Optimizer):
                 loss = closure()
         for group in self.param_groups:
             b = self._buffers_of(group)
+            self._check_masters(group, b)
             for k, (p, g) in enumerate(zip(group["params"], b.grads)):
                 if p.grad is None:
                     raise RuntimeError(f"parameter {k} of a group has no gradient; "
@@ -243,15 +281,25 @@ class _FlatAdamW(torch.optim.Optimizer):
                 if name in sg:
                     group[name] = tuple(sg[name]) if name == "betas" else sg[name]
             b = self._buffers_of(group)
-            for idx, p in zip(sg["params"], group["params"]):
-                s = saved.get(idx)
-                if s is None:
-                    continue
+            master_key = {A.MODE_MIXED_FP32_MASTER: "master",
+                          A.MODE_MIXED_BF16_REMAINDER: "remainder"}.get(self.mode)
+            for k, (idx, p) in enumerate(zip(sg["params"], group["params"])):
+                s = saved.get(idx) or {}
                 for name in ("exp_avg", "exp_avg_sq", "compensation", "master", "remainder"):
                     if name in s and name in self.state[p]:
                         self.state[p][name].copy_(s[name])
                 if "step" in s:
                     b.step.copy_(torch.as_tensor(s["step"]).reshape(1))
+                if master_key is not None:
+                    if master_key in s:
+                        # the loaded master is authoritative for the model's
+                        # parameter as it stands now
+                        b.versions[k] = p._version
+                    else:
+                        # a state saved without this optimizer's master (by
+                        # another optimizer, or another master layout)
+                        with torch.no_grad():
+                            self._sync_master(b, k, p, force=True)
             b.hp_key = None
 
 
@@ -280,6 +328,16 @@ class MasterWeightAdamW(_FlatAdamW):
     shard, here over one process's parameters.  fp32 m and v; every step
     updates the master and writes the bf16 parameters from it (round to
     nearest even).
+
+    The master starts as the model's values when the optimizer is built.  A
+    parameter changed in place afterwards (``model.load_state_dict``,
+    ``p.copy_``) is seen at the next ``step`` by its version counter: the
+    fp32 master is kept if the parameter is still its bf16 rounding (the
+    same checkpoint loaded into both), else re-taken from the parameter; the
+    remainder is reset to zero.  ``load_state_dict`` takes the saved master
+    when the state has one and re-derives it from the parameter when not.
+    A change made through ``p.data`` bypasses the counter: call
+    ``sync_master()`` after it.
 
     ``master="fp32"``: the optimizer keeps an fp32 master copy (state
     ``master``), 12 B/param of optimizer state.  ``master="remainder"``: the

@@ -324,6 +324,38 @@ def copy_ceiling(device, nbytes: int = 4 << 30, reps: int = 5) -> dict:
     return out
 
 
+def host_link_ceiling(device, nbytes: int, reps: int = 3) -> dict:
+    """Host-to-device bandwidth over the CPU-GPU link for nbytes from pinned
+    host memory: cudaMemcpyAsync, and the library's copy kernel reading the
+    pinned buffer in place (zero copy).  Bytes = nbytes (what crosses the
+    link); best of reps."""
+    nbytes = (nbytes + 15) // 16 * 16
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    for name, fn in (("memcpy_h2d", lambda: dst.copy_(host, non_blocking=True)),
+                     ("zero_copy_read", lambda: A.adamw_copy_probe(dst.data_ptr(), host.data_ptr(),
+                                                                   nbytes, stream.cuda_stream))):
+        fn()
+        torch.cuda.synchronize(device)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        out[name] = nbytes / best / 1e9
+    del host, dst
+    torch.cuda.empty_cache()
+    out["ceiling"] = max(out["memcpy_h2d"], out["zero_copy_read"])
+    out["bytes"] = nbytes
+    return out
+
+
 def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
     """The same metric end to end: every step copies that step's bf16
     gradients from pinned host memory, runs the step and reads the non-finite
@@ -416,9 +448,13 @@ def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
     }
     name = max(out, key=lambda k: out[k]["value"])
     best = out[name]
+    link = host_link_ceiling(device, int(N * 2))
+    link_gbs = N * 2 / (best["ms_per_step"] / 1e3) / 1e9
     return {"value": best["value"], "unit": UNIT, "h2d_bytes_per_step": int(N * 2),
             "d2h_bytes_per_step": 4, "ms_per_step": best["ms_per_step"], "steps": k_e2e,
-            "path": described[name], "paths": out, "_t": state["t"]}
+            "path": described[name], "paths": out,
+            "link_gbs": link_gbs, "link_ceiling_gbs": link,
+            "frac_of_link": link_gbs / link["ceiling"], "_t": state["t"]}
 
 
 def run_gpu(args):
@@ -458,7 +494,8 @@ def run_gpu(args):
 
     t = 0
     for i in range(args.warmup):
-        plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None)
+        plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None,
+                               nonfinite=flag if clip else None)
         t += 1
     torch.cuda.synchronize(device)
     barrier(world)
@@ -471,30 +508,55 @@ def run_gpu(args):
 
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # args.reps repetitions of args.steps steps each.  Large lists: the steps
+    # of a repetition run back to back between two events (no event between
+    # steps, so consecutive launches may overlap their ramp as they do in
+    # training).  L2-resident lists: each step between its own events, after
+    # the flush.
+    rep_s = []
     torch.cuda.synchronize(device)
     barrier(world)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for r in range(args.reps):
         if flush:
-            flush_buf.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        plans[(args.warmup + i) % n_grad].step(hp, t + 1, grad_norm=norm if clip else None)
-        ev[i][1].record(stream)
-        t += 1
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for i in range(args.steps):
+                flush_buf.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                plans[(args.warmup + i) % n_grad].step(hp, t + 1, grad_norm=norm if clip else None,
+                                                       nonfinite=flag if clip else None)
+                ev[i][1].record(stream)
+                t += 1
+            torch.cuda.synchronize(device)
+            rep_s.append(sum(a.elapsed_time(b) / 1e3 for a, b in ev))
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                plans[(args.warmup + i) % n_grad].step(hp, t + 1, grad_norm=norm if clip else None,
+                                                       nonfinite=flag if clip else None)
+                t += 1
+            e1.record(stream)
+            e1.synchronize()
+            rep_s.append(e0.elapsed_time(e1) / 1e3)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - wall0
     barrier(world)
     clk = clocks.stop()
 
-    per_step = [a.elapsed_time(b) / 1e3 for a, b in ev]
-    span = sum(per_step) if flush else ev[0][0].elapsed_time(ev[-1][1]) / 1e3
-    span_max = reduce_max(span, world, device)
+    # the slowest rank's time of each repetition, then the median repetition
+    rep_s = [reduce_max(x, world, device) for x in rep_s]
+    span_max = statistics.median(rep_s)
     ms_per_step = span_max / args.steps * 1e3
     value = world * N * args.steps / span_max
-    avg_launch = sum(per_step) / len(per_step)
+    # one update launch per step (or one norm + update sequence with
+    # clipping): the average launch is the step time
+    avg_launch = span_max / args.steps
     achieved = bpp * N / avg_launch / 1e9
+    repetitions = {"n": len(rep_s), "ms_per_step_median": ms_per_step,
+                   "ms_per_step_min": min(rep_s) / args.steps * 1e3,
+                   "ms_per_step_max": max(rep_s) / args.steps * 1e3}
 
     extra = {}
     if flush:
@@ -504,7 +566,8 @@ def run_gpu(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(args.steps):
-            plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None)
+            plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None,
+                                   nonfinite=flag if clip else None)
             t += 1
         e1.record(stream)
         e1.synchronize()
@@ -556,6 +619,7 @@ def run_gpu(args):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "fused_clipped_step": bool(plans[0].info.fused),
         },
+        "repetitions": repetitions,
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
@@ -567,17 +631,22 @@ def run_gpu(args):
         **extra,
         "frac_of_copy_ceiling": (achieved / ceiling["ceiling"]) if ceiling else None,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": args.reps * args.steps * launches_per_step,
         "clocks": clk,
         "wall_s_timed": wall,
     }
     if cpu_arrays is not None:
         thr = host_threads()
         val, secs, used = oracle_throughput(w_bench, N, 1, thr, cpu_arrays)
+        n1 = min(N, args.ref_sample // 4)
+        val1, secs1, _ = oracle_throughput(w_bench, n1, 1, 1)
         out["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": used, "kind": "oracle",
                                "sample": f"one step over the whole {w.name} list "
                                          f"({N} params, the same drawn inputs), {secs:.2f} s "
-                                         f"on {used} threads"}
+                                         f"on {used} threads",
+                               "single_thread": {"value": val1, "unit": UNIT, "cores": 1,
+                                                 "sample": f"one step over the first {n1} "
+                                                           f"params of the list, {secs1:.2f} s"}}
     for p in plans:
         p.close()
     if rank == 0:
@@ -620,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--grad-buffers", type=int, default=4)
+    ap.add_argument("--reps", type=int, default=5,
+                    help="timed repetitions of --steps steps; the median is reported")
     ap.add_argument("--ref-sample", type=int, default=1 << 28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -359,11 +359,14 @@ int adamw_copy_probe(void* dst, const void* src, int64_t bytes,
  * fails or fragments that pool), and code that must not synchronise the
  * device (cudaMalloc and cudaFree may).  It needs no plan (plan creation
  * allocates) and allocates nothing: its scratch is a fixed file-scope device
- * array of about 208 KiB in this library, which every GPU that loads the
+ * array of about 76 KiB in this library, which every GPU that loads the
  * library keeps until the process exits.  The source pages have no
  * counterpart; this is a utility of this library.
- * host_table: host array of n_tensors entries, read during the call only; only
- *   .grad (device bf16, 2-byte aligned) and .numel are used.
+ * host_table: host array of n_tensors entries (pageable or pinned), read
+ *   during the call only: the entries travel to the device as kernel launch
+ *   parameters, which the runtime copies when the launch is made, so the
+ *   array may be changed or freed as soon as the call returns.  Only .grad
+ *   (device bf16, 2-byte aligned) and .numel are used.
  * d_grad_norm (nullable, device fp64) and d_nonfinite (nullable, device
  *   int32) receive the norm and the flag, as in adamw_grad_norm.
  * The first call on a device sets that device up (looks up the scratch

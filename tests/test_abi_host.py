@@ -90,19 +90,26 @@ def test_interleaved_tiles_cut_on_4k_boundaries_and_balance(sizes, grid):
     """Interleaved tiles are cut in the flattened list at multiples of 2048
     elements from each tensor's start (4 KB of a bf16 stream: measured, such
     cuts stream 1-2 % faster than 8K tiles cut per tensor and 18 % faster
-    than cuts on 16-byte boundaries), stretched to the multiple of 2048 that
-    deals every CTA the same number of tiles where the list allows it: no CTA
-    carries more than one tile beyond the mean, and on long lists the loads
-    agree to 1 %."""
+    than cuts on 16-byte boundaries), except the cuts that end a tile of the
+    last round, which fall on multiples of 256 so that every CTA's quota is
+    the same to 256 elements: at most one such cut per CTA, and on a single
+    tensor no CTA carries more than 256 elements beyond the mean."""
     entries = [_fake(i << 34, n, 1) for i, n in enumerate(sizes)]
     chunks = _check_partition(entries, 1, grid)
     load = np.zeros(grid, np.int64)
+    off_grid = 0
     for c in chunks:
         load[c.cta] += c.len
-        assert c.offset % 2048 == 0, "cut off the 2048-element grid"
+        assert c.offset % 256 == 0, "cut off the 256-element grid"
+        off_grid += c.offset % 2048 != 0
+    assert off_grid <= grid, (off_grid, grid)
     total = sum(sizes)
-    longest = max(c.len for c in chunks)
-    assert load.max() - total / grid <= longest, (load.max(), total / grid)
+    if len(sizes) == 1:
+        assert load.max() - total / grid <= 256, (load.max(), total / grid)
+        assert total / grid - load.min() <= 512, (load.min(), total / grid)
+    else:
+        # each tensor's own cut grid moves a cut by up to 2047 elements
+        assert load.max() - total / grid <= 2048 * len(sizes) + 256, (load.max(), total / grid)
     if total / grid >= 100 * 8192:
         assert load.max() <= 1.01 * total / grid, (load.max(), total / grid)
 
@@ -290,7 +297,8 @@ def test_partition_properties_on_random_lists():
     a random grid from 1 to 1216): every element lands in exactly one chunk,
     chunks come in CTA order, vector chunks start 16-byte aligned in every
     stream, and interleaved cuts inside a vector body fall on the
-    2048-element grid from the body's start."""
+    2048-element grid from the body's start (256 for the one cut per CTA
+    that ends its last tile)."""
     rng = np.random.default_rng(2024)
     modes = [0, 1, 2, 3, 4] + list(A.ANYPREC_MODES)
     for case in range(200):
@@ -310,16 +318,22 @@ def test_partition_properties_on_random_lists():
         grid = int(rng.integers(1, 1217))
         chunks = _check_partition(entries, mode, grid)
         # cuts inside a vector body: on the 2048-element grid of the body
-        # (interleaved partition) or on whole vectors (contiguous ranges)
+        # (interleaved partition; the last round's tile ends on its
+        # 256-element grid, at most one per CTA) or on whole vectors
+        # (contiguous ranges)
         interleaved = int(sizes.sum()) >= 2 * grid * 8192
-        step = 2048 if interleaved else 8
+        step = 256 if interleaved else 8
         heads = {}
         for c in chunks:
             if c.vec:
                 heads.setdefault(c.tensor, []).append(c.offset)
+        coarse = 0
         for k, offs in heads.items():
             head = min(offs)
             assert all((o - head) % step == 0 for o in offs), (case, k, step, sorted(offs)[:5])
+            coarse += sum((o - head) % 2048 != 0 for o in offs)
+        if interleaved:
+            assert coarse <= grid, (case, coarse, grid)
 
 
 def test_master_weight_optimizer_validates_its_options():

@@ -156,13 +156,14 @@ def test_anyprec_step_table_matches_a_plan(mode):
     A.adamw_step_table_cache_clear()
     norm_a = torch.zeros(1, dtype=torch.float64, device="cuda")
     norm_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    flag_b = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     for k in (1, 2, 3):
         a.set_grad(k)
         g.copy_(a.g)
         a.plan.step(hp, k, grad_norm=norm_a)
-        A.adamw_step_table(d_table.data_ptr(), len(entries), w.mode, hp, k, norm_b.data_ptr(), 0,
-                           stream)
+        A.adamw_step_table(d_table.data_ptr(), len(entries), w.mode, hp, k, norm_b.data_ptr(),
+                           flag_b.data_ptr(), stream)
     torch.cuda.synchronize()
     assert A.adamw_step_table_cache_clear() == 1
     _same_state(a.st, b)

@@ -33,5 +33,7 @@ def test_bench_prints_one_line_with_the_whole_contract(capsys):
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["sample"]
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] == 4
+    # five timed repetitions of four one-launch steps
+    assert d["repetitions"]["n"] == 5
+    assert d["gpu_launches"] == 5 * 4
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])

@@ -357,3 +357,93 @@ def test_master_weight_backward_and_checkpoint(master):
             if name != "step":
                 assert torch.equal(oa.state[p][name].view(torch.uint8), ob.state[q][name].view(torch.uint8))
     assert oa.state[next(ma.parameters())]["step"].item() == ob.state[next(mb.parameters())]["step"].item() == 5
+
+
+@pytest.mark.parametrize("master", ["fp32", "remainder"])
+def test_master_follows_weights_loaded_after_the_optimizer(master):
+    """Build the optimizer, then load other weights into the model (as a
+    model load_state_dict does, in place): the next step starts from the
+    loaded weights, exactly as the oracle started from them."""
+    params = _params(seed=3)
+    opt = OPT.MasterWeightAdamW(params, master=master, lr=2e-4, betas=(0.9, 0.95),
+                                weight_decay=0.1, max_grad_norm=1.0)
+    loaded = _params(seed=11)
+    with torch.no_grad():
+        for p, q in zip(params, loaded):
+            p.copy_(q)
+    ref = _MasterOracle(loaded, master == "remainder")
+    for k in range(1, 4):
+        gs = _grad(k)
+        for p, g in zip(params, gs):
+            p.grad.copy_(g)
+        opt.step()
+        ref.step(gs, _hp(opt.param_groups[0]))
+    torch.cuda.synchronize()
+    ref.check(opt, params)
+
+
+@pytest.mark.parametrize("master", ["fp32", "remainder"])
+def test_state_without_a_master_rederives_it_from_the_model(master):
+    """A checkpoint whose state has no master (saved by an optimizer without
+    one) loads its moments and step count; the master is taken from the
+    model's parameters as they are then."""
+    params = _params(seed=3)
+    opt = OPT.MasterWeightAdamW(params, master=master, lr=2e-4, betas=(0.9, 0.95),
+                                weight_decay=0.1)
+    for k in range(1, 3):
+        for p, g in zip(params, _grad(k)):
+            p.grad.copy_(g)
+        opt.step()
+    sd = opt.state_dict()
+    key = "master" if master == "fp32" else "remainder"
+    sd["state"] = {i: {n: (v.clone() if torch.is_tensor(v) else v) for n, v in st.items() if n != key}
+                   for i, st in sd["state"].items()}
+    other = _params(seed=17)
+    with torch.no_grad():
+        for p, q in zip(params, other):
+            p.copy_(q)
+    opt.load_state_dict(sd)
+    ref = _MasterOracle(other, master == "remainder")
+    for kk, p in enumerate(params):
+        ref.tens[kk][2] = H.to_np(opt.state[p]["exp_avg"]).reshape(-1).copy()
+        ref.tens[kk][3] = H.to_np(opt.state[p]["exp_avg_sq"]).reshape(-1).copy()
+    ref.t = int(opt.state[params[0]]["step"].item())
+    assert ref.t == 2
+    for k in range(3, 5):
+        gs = _grad(k)
+        for p, g in zip(params, gs):
+            p.grad.copy_(g)
+        opt.step()
+        ref.step(gs, _hp(opt.param_groups[0]))
+    torch.cuda.synchronize()
+    ref.check(opt, params)
+
+
+def test_fp32_master_survives_loading_the_model_after_the_optimizer():
+    """Restoring a checkpoint in the other order (optimizer state first, then
+    the same checkpoint's model weights) keeps the loaded fp32 master: the
+    model's bf16 values are its rounding, so nothing is re-derived and the
+    run continues bit for bit."""
+    torch.manual_seed(2)
+    make = lambda: torch.nn.Linear(96, 80).cuda().to(torch.bfloat16)
+    ma = make()
+    oa = OPT.MasterWeightAdamW(ma.parameters(), master="fp32")
+    xs = [torch.randn(16, 96, device="cuda", dtype=torch.bfloat16) for _ in range(4)]
+    for x in xs[:2]:
+        oa.zero_grad()
+        ma(x).float().pow(2).mean().backward()
+        oa.step()
+    ck = {"model": {k: v.clone() for k, v in ma.state_dict().items()}, "opt": oa.state_dict()}
+    mb = make()
+    ob = OPT.MasterWeightAdamW(mb.parameters(), master="fp32")
+    ob.load_state_dict(ck["opt"])
+    mb.load_state_dict(ck["model"])
+    for x in xs[2:]:
+        for m, o in ((ma, oa), (mb, ob)):
+            o.zero_grad()
+            m(x).float().pow(2).mean().backward()
+            o.step()
+    torch.cuda.synchronize()
+    for p, q in zip(ma.parameters(), mb.parameters()):
+        assert torch.equal(oa.state[p]["master"], ob.state[q]["master"])
+        assert torch.equal(p.view(torch.int16), q.view(torch.int16))
