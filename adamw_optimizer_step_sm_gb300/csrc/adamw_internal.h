@@ -28,13 +28,7 @@ constexpr int kVec = 8;
 #define ADAMW_FUSED_MAX_GRAD_MB 160
 #endif
 constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
-// Elements of its update share whose state (all streams but g) each CTA of
-// the fused clipped step asks L2 for before its norm pass, so that DRAM keeps
-// streaming through the norm pass and the grid barrier (0: none).
-#ifndef ADAMW_FUSED_PREFETCH
-#define ADAMW_FUSED_PREFETCH 8192
-#endif
-constexpr int64_t kFusedPrefetchElems = ADAMW_FUSED_PREFETCH;
+
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.
 constexpr int64_t kMinElemsPerCta = int64_t(kBlock) * kVec;

@@ -764,26 +764,26 @@ norm_partial_noalloc_kernel(const NoAllocEntry* __restrict__ table, int32_t n,
         }
     };
 
-    Sum2F32 grp;
+    Sum2F32x2 grp;
     double acc = 0.0;
     float err = 0.0f;
     bool in_range = true;
     uint32_t nz = 0;
+    auto add_word = [&](uint32_t w) {
+        const uint64_t x = bf16x2_to_f2(w);
+        grp.add(f2_mul(x, x));
+    };
     walk(
         [&](const uint4& w) {
             nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
-            grp.add(sq(bf16_lo(w.x)));
-            grp.add(sq(bf16_hi(w.x)));
-            grp.add(sq(bf16_lo(w.y)));
-            grp.add(sq(bf16_hi(w.y)));
-            grp.add(sq(bf16_lo(w.z)));
-            grp.add(sq(bf16_hi(w.z)));
-            grp.add(sq(bf16_lo(w.w)));
-            grp.add(sq(bf16_hi(w.w)));
+            add_word(w.x);
+            add_word(w.y);
+            add_word(w.z);
+            add_word(w.w);
         },
         [&](uint16_t hb) {
             nz |= hb & 0x7fffu;
-            grp.add(sq(from_bf16(hb)));
+            add_word(hb);   // the high lane adds an exact zero
             in_range &= grp.flush(acc, err);
         },
         [&]() { in_range &= grp.flush(acc, err); });

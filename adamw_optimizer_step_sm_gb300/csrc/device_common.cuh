@@ -948,34 +948,68 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
     update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad);
 }
 
-// Error-free fp32 accumulation of non-negative terms: s + e is the exact sum
-// of everything added since the last flush, up to the rounding of e itself.
-// Squares of bf16 values are exact in fp32 for |g| in [2^-63, 2^64); for
-// a >= b >= 0 the rounding error of a + b is exactly b - ((a + b) - a)
-// (Dekker's Fast2Sum), so no bit of any square is lost; e collects those
-// errors.  A group of at most 64 terms is flushed: s into an fp64 sum, e
-// (at most 2^-18 of s) into an fp32 sum of the errors.
-struct Sum2F32 {
-    float s = 0.0f, e = 0.0f;
-    __device__ __forceinline__ void add(float x) {
-        const float a = fmaxf(s, x), b = fminf(s, x);
-        const float t = __fadd_rn(a, b);
-        e = __fadd_rn(e, __fsub_rn(b, __fsub_rn(t, a)));
+// Error-free fp32 accumulation of non-negative terms.  Squares of bf16 values
+// are exact in fp32 for |g| in [2^-63, 2^64); a group of terms is summed in
+// fp32 with the exact rounding error of every addition collected on the
+// side (so no bit of any square is lost), and flushed: its sum into an fp64
+// total, its collected error (at most 2^-18 of the sum) into an fp32 sum of
+// the errors.  Sum2F32x2 below does this on two lanes at once.
+__device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
+
+// Packed fp32x2 arithmetic (two IEEE round-to-nearest operations in one
+// instruction on sm_100 and later): a 64-bit value holds two floats, lane 0
+// in the low word.
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// The two bf16 of a 32-bit word as a packed pair of floats (exact).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+    return uint64_t(w << 16) | (uint64_t(w & 0xffff0000u) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t x) { return __uint_as_float(uint32_t(x)); }
+__device__ __forceinline__ float f2_hi(uint64_t x) { return __uint_as_float(uint32_t(x >> 32)); }
+
+// That accumulation on two interleaved streams of terms at once, one per
+// lane of a packed pair, with Knuth's TwoSum (t = s + x; b = t - s; error =
+// (s - (t - b)) + (x - b), exact for any two floats without overflow), which
+// needs no ordering of its operands (so it packs, and a NaN term stays in
+// the sum, where the flush's range check sees it).  Per lane: s + e is the
+// exact sum of the lane's terms since the last flush, up to the rounding of
+// e itself; groups of at most 32 terms per lane.
+struct Sum2F32x2 {
+    uint64_t s = 0, e = 0;
+    __device__ __forceinline__ void add(uint64_t x) {
+        const uint64_t t = f2_add(s, x);
+        const uint64_t b = f2_sub(t, s);
+        e = f2_add(e, f2_add(f2_sub(s, f2_sub(t, b)), f2_sub(x, b)));
         s = t;
     }
-    // Adds the group to (acc, err) and restarts it; false when the group left
-    // the range where squares are exact and sums finite.
+    // Adds both lanes' groups to (acc, err) (lane 0 first) and restarts
+    // them; false when a group left the range where squares are exact and
+    // sums finite.
     __device__ __forceinline__ bool flush(double& acc, float& err) {
-        const bool ok = s < 0x1p100f;   // also false for inf and NaN
-        acc += double(s);
-        err = __fadd_rn(err, e);
-        s = 0.0f;
-        e = 0.0f;
+        const float s0 = f2_lo(s), s1 = f2_hi(s);
+        const bool ok = s0 < 0x1p100f && s1 < 0x1p100f;   // also false for inf and NaN
+        acc += double(s0);
+        acc += double(s1);
+        err = __fadd_rn(__fadd_rn(err, f2_lo(e)), f2_hi(e));
+        s = 0;
+        e = 0;
         return ok;
     }
 };
-
-__device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
 
 // Walks the g elements of one CTA's chunks that belong to this thread, in a
 // fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
@@ -1028,37 +1062,38 @@ __device__ __forceinline__ double block_sum(double x) {
 }
 
 // Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
-// same partition as the update (so the result depends only on the plan).
-// Fast path: error-free fp32 group sums of the exact squares, flushed every
-// 64 elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny,
-// inf or NaN gradients) recomputes its elements in fp64, which also decides
-// the non-finite flag.
+// norm's own partition (so the result depends only on the plan).
+// Fast path: error-free fp32 group sums of the exact squares, two lanes
+// packed (the low and the high bf16 of each word), flushed every 64
+// elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny, inf or
+// NaN gradients) recomputes its elements in fp64, which also decides the
+// non-finite flag.
 // The CTA's partial sum of squares and non-finite flag, written to
 // partial[blockIdx.x] and flag[blockIdx.x].
 __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                                  int32_t c1, double* __restrict__ partial,
                                                  int32_t* __restrict__ flag) {
-    Sum2F32 grp;
+    Sum2F32x2 grp;
     double acc = 0.0;
     float err = 0.0f;
     bool in_range = true;
     uint32_t nz = 0;
+    auto add_word = [&](uint32_t w) {
+        const uint64_t x = bf16x2_to_f2(w);
+        grp.add(f2_mul(x, x));
+    };
     for_thread_grads<8>(
         chunks, c0, c1,
         [&](const uint4& w) {
             nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
-            grp.add(sq(bf16_lo(w.x)));
-            grp.add(sq(bf16_hi(w.x)));
-            grp.add(sq(bf16_lo(w.y)));
-            grp.add(sq(bf16_hi(w.y)));
-            grp.add(sq(bf16_lo(w.z)));
-            grp.add(sq(bf16_hi(w.z)));
-            grp.add(sq(bf16_lo(w.w)));
-            grp.add(sq(bf16_hi(w.w)));
+            add_word(w.x);
+            add_word(w.y);
+            add_word(w.z);
+            add_word(w.w);
         },
         [&](uint16_t h) {
             nz |= h & 0x7fffu;
-            grp.add(sq(from_bf16(h)));
+            add_word(h);   // the high lane adds an exact zero
             in_range &= grp.flush(acc, err);
         },
         [&]() { in_range &= grp.flush(acc, err); });
@@ -1092,38 +1127,6 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
     if (threadIdx.x == 0) {
         partial[blockIdx.x] = tot;
         flag[blockIdx.x] = any;
-    }
-}
-
-// Asks L2 for the first `budget` elements of the CTA's update chunks
-// [c0, c1) of every stream the update reads except g (which the norm pass
-// just brought in): p (or the master), m, v and the aux stream where the
-// mode reads it.  One prefetch per 128-byte line, every address inside its
-// buffer; a hint only, so it changes no result.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-template <int MODE>
-__device__ __forceinline__ void prefetch_update_state(const ChunkPtr* __restrict__ chunks,
-                                                      int32_t c0, int32_t c1, int64_t budget) {
-    constexpr bool kReadsAux = MODE != ADAMW_MODE_MIXED_FP32_MASTER && stream_bytes<MODE>(4) != 0;
-    for (int32_t ci = c0; ci < c1 && budget > 0; ++ci) {
-        const ChunkPtr ch = load_chunk(chunks + ci);
-        int64_t len = ch.len2 >> 1;
-        if (len > budget) len = budget;
-        budget -= len;
-        const void* ptr[4] = {ch.p, ch.m, ch.v, ch.a};
-        const int es[4] = {stream_bytes<MODE>(0), stream_bytes<MODE>(2), stream_bytes<MODE>(3),
-                           stream_bytes<MODE>(4)};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (k == 3 && !kReadsAux) continue;
-            const char* b = static_cast<const char*>(ptr[k]);
-            const int64_t bytes = len * es[k];
-            for (int64_t off = int64_t(threadIdx.x) * 128; off < bytes; off += int64_t(kBlock) * 128)
-                prefetch_l2(b + off);
-        }
     }
 }
 

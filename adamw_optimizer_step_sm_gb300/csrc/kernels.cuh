@@ -120,11 +120,6 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         int32_t* __restrict__ status) {
     __shared__ int passed;
     pdl_wait();
-    // the first elements of the state this CTA updates after the barrier,
-    // fetched into L2 while the norm pass and the barrier run
-    if (kFusedPrefetchElems > 0)
-        prefetch_update_state<MODE>(upd_chunks, upd_begin[blockIdx.x], upd_begin[blockIdx.x + 1],
-                                    kFusedPrefetchElems);
     norm_partial_cta(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1], partial, flag);
     if (threadIdx.x == 0) {
         __threadfence();

@@ -245,6 +245,53 @@ def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     gpu.plan.close()
 
 
+@pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
+@pytest.mark.parametrize("path", ["fused", "three_launches", "device"])
+def test_clip_skips_step_with_nan_in_every_path(mode, path):
+    """A NaN gradient under clipping (one element among a million, or the
+    only non-zero one) sets the flag and skips the step in every path, as in
+    the oracle, and the norm reads NaN; the next finite step goes on from the
+    unchanged state."""
+    w = _small("nanskip", mode=mode, max_grad_norm=1.0, steps=3)
+    gpu = H.GpuSide(w)
+    if path != "fused":
+        gpu.plan.close()
+        v = gpu.st.views
+        gpu.plan = A.Plan(v(gpu.st.param), v(gpu.g), v(gpu.st.exp_avg), v(gpu.st.exp_avg_sq),
+                          v(gpu.st.aux), mode, norm=True, fuse=False)
+    assert gpu.plan.info.fused == (1 if path == "fused" else 0)
+    ref = H.OracleRun.from_state(gpu.st)
+    hp_g, hp_o = H.hp_pair(w)
+    d_hp = A.device_hparams(hp_g)
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for k in (1, 2, 3):
+        gpu.set_grad(k)
+        if k == 2:
+            gpu.g[gpu.st.offsets[8] + 4242] = float("nan")
+        if path == "device":
+            gpu.plan.step_device(d_hp, d_step, A.STEP_CLIP, grad_norm=gpu.norm, nonfinite=gpu.flag)
+            torch.cuda.synchronize()
+            skipped = bool(gpu.flag.item())
+        else:
+            skipped = gpu.step(hp_g)
+        oskipped, onorm, obad = ref.step(H.to_u16(gpu.g), hp_o)
+        assert skipped == oskipped == obad == (k == 2), (k, skipped, oskipped, obad)
+        if k == 2:
+            assert np.isnan(gpu.norm.item())
+    if path == "device":
+        assert int(d_step.item()) == 2
+    rep = H.compare_state(gpu, ref)
+    _assert(rep)
+    assert rep.exact == rep.n
+    # a list whose only non-zero gradient is the NaN
+    gpu.g.zero_()
+    gpu.g[7] = float("nan")
+    gpu.plan.grad_norm(gpu.norm, gpu.flag)
+    torch.cuda.synchronize()
+    assert int(gpu.flag.item()) == 1 and np.isnan(gpu.norm.item())
+    gpu.plan.close()
+
+
 @pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan")])
 def test_nonfinite_reported_without_clip(bad):
     """Without clipping the step runs and NaN/inf propagate exactly as in the
