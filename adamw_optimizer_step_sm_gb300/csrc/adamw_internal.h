@@ -28,6 +28,12 @@ constexpr int kVec = 8;
 #define ADAMW_FUSED_MAX_GRAD_MB 160
 #endif
 constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
+// 1: the fused clipped step's norm phase loads g with the evict-last L2
+// policy, so that more of the update phase's second read of g hits L2.
+#ifndef ADAMW_FUSED_KEEP_G
+#define ADAMW_FUSED_KEEP_G 1
+#endif
+constexpr bool kFusedKeepG = ADAMW_FUSED_KEEP_G != 0;
 
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.

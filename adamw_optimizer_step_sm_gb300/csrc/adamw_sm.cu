@@ -363,7 +363,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_r = off; off = align_up(off + sizeof(StepRecord), 256);
     const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
     const size_t o_a = off; off = align_up(off + sizeof(unsigned long long), 256);
-    const size_t o_d = off; off = align_up(off + 2 * sizeof(uint32_t), 256);
+    const size_t o_d = off; off = align_up(off + sizeof(unsigned long long), 256);
     const size_t o_m = off; off = align_up(off + 2 * sizeof(ScalarMemo), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
@@ -382,8 +382,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->rec = reinterpret_cast<StepRecord*>(b + o_r);
     P->status = reinterpret_cast<int32_t*>(b + o_s);
     P->arrivals = reinterpret_cast<unsigned long long*>(b + o_a);
-    P->done = reinterpret_cast<unsigned int*>(b + o_d);
-    P->flagword = reinterpret_cast<int32_t*>(b + o_d + sizeof(uint32_t));
+    P->done = reinterpret_cast<unsigned long long*>(b + o_d);
     P->memo = reinterpret_cast<ScalarMemo*>(b + o_m);
     P->fused = fused;
 #if ADAMW_CHECK_BOUNDS

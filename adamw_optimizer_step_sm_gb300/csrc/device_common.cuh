@@ -70,6 +70,18 @@ __device__ __forceinline__ uint4 ld16(const void* p) {
     return *q;
 #endif
 }
+// A 16-byte load that asks L2 to keep the line (evict-last policy): for g in
+// the fused clipped step's norm phase, which the update phase reads again.
+__device__ __forceinline__ uint4 ld16_keep(const void* p) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+    uint4 r;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(policy));
+    return r;
+}
+
 __device__ __forceinline__ void st16(void* p, uint4 v) {
     uint4* q = reinterpret_cast<uint4*>(p);
 #if ADAMW_ST_POLICY == 1
@@ -1014,7 +1026,7 @@ struct Sum2F32x2 {
 // Walks the g elements of one CTA's chunks that belong to this thread, in a
 // fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
 // after every group of U vectors.
-template <int U, typename FV, typename FE, typename FI>
+template <int U, bool KEEP = false, typename FV, typename FE, typename FI>
 __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ chunks,
                                                  int32_t c0, int32_t c1, FV vec, FE elem,
                                                  FI after_iter) {
@@ -1033,7 +1045,7 @@ __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ ch
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t i = base + int64_t(u) * kBlock;
-                    if (i < nvec) w[u] = ld16(g + i * kVec);
+                    if (i < nvec) w[u] = KEEP ? ld16_keep(g + i * kVec) : ld16(g + i * kVec);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -1070,6 +1082,8 @@ __device__ __forceinline__ double block_sum(double x) {
 // non-finite flag.
 // The CTA's partial sum of squares and non-finite flag, written to
 // partial[blockIdx.x] and flag[blockIdx.x].
+// KEEP: load g with the evict-last L2 policy (the fused step reads it again).
+template <bool KEEP = false>
 __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                                  int32_t c1, double* __restrict__ partial,
                                                  int32_t* __restrict__ flag) {
@@ -1082,7 +1096,7 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
         const uint64_t x = bf16x2_to_f2(w);
         grp.add(f2_mul(x, x));
     };
-    for_thread_grads<8>(
+    for_thread_grads<8, KEEP>(
         chunks, c0, c1,
         [&](const uint4& w) {
             nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;

@@ -48,20 +48,23 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
 // the scalars of t + 1 into the memo while the others still stream (so a
 // run of steps with unchanged hyperparameters computes each step's scalars
 // off the critical path); the last CTA to finish -- found with an arrival
-// counter -- advances the counter and writes the non-finite flag, so no CTA
-// can read a counter that was already advanced.  Invalid hyperparameters:
-// nothing is updated, the flag is -1.
+// counter that also counts the CTAs that saw a non-finite gradient, one
+// atomic per CTA -- advances the counter and writes the non-finite flag, so
+// no CTA can read a counter that was already advanced (each CTA's read of it
+// has returned before its arrival is counted).  The kernel's end publishes
+// the last CTA's writes and the memo.  Invalid hyperparameters: nothing is
+// updated, the flag is -1.
 template <int MODE, int K>
 __global__ void ADAMW_SELF_BOUNDS(MODE)
 adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
                          const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
-                         unsigned int* __restrict__ done, int32_t* __restrict__ flagword,
-                         int32_t* __restrict__ user_flag, ScalarMemo* __restrict__ memo) {
+                         unsigned long long* __restrict__ done, int32_t* __restrict__ user_flag,
+                         ScalarMemo* __restrict__ memo) {
     __shared__ StepScalars s_sh;
     __shared__ adamw_hparams_t hp_sh;
     __shared__ int valid_sh, hit_sh;
     __shared__ int64_t t_sh;
-    __shared__ unsigned int ticket_sh;
+    __shared__ unsigned long long ticket_sh;
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
     ChunkPtr cur;
     if (c0 < c1) cur = load_chunk(chunks + c0);
@@ -86,24 +89,19 @@ adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
     bool bad = false;
     if (valid_sh) update_cta_from<MODE, K>(chunks, c0, c1, cur, s_sh, 1.0f, bad);
     const int any = (K == kReport) ? __syncthreads_or(bad) : 0;
-    if (threadIdx.x == 0) {
-        if (any) atomicOr(flagword, 1);
-        __threadfence();
-        ticket_sh = atomicAdd(done, 1u);
-    }
+    if (threadIdx.x == 0) ticket_sh = atomicAdd(done, 1ull + (any ? (1ull << 32) : 0ull)) + (any ? (1ull << 32) : 0ull);
     __syncthreads();
-    const unsigned int ticket = ticket_sh;
-    if (ticket == 0 && valid_sh) {
+    const unsigned long long ticket = ticket_sh;   // the word with this CTA's arrival
+    const unsigned int arrived = unsigned(ticket & 0xffffffffu);
+    if (arrived == 0 && valid_sh) {
         // the first CTA done: the next step's scalars, for the memo
         __shared__ StepScalars next_sh;
         make_scalars_cta(hp_sh, t_sh + 1, &next_sh);
         if (threadIdx.x == 0) memo_store(memo, hp_sh, t_sh + 1, next_sh);
     }
-    if (threadIdx.x == 0 && ticket == gridDim.x - 1) {  // the last CTA
-        __threadfence();
-        const int32_t f = atomicExch(flagword, 0);
+    if (threadIdx.x == 0 && arrived == gridDim.x - 1) {  // the last CTA
         if (valid_sh) *d_step = t_sh;
-        if (user_flag) *user_flag = valid_sh ? f : -1;
+        if (user_flag) *user_flag = valid_sh ? int32_t((ticket >> 32) != 0) : -1;
         *done = 0;
     }
 }
@@ -119,8 +117,10 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         int32_t* __restrict__ user_flag, unsigned long long* __restrict__ arrivals,
                         int32_t* __restrict__ status) {
     __shared__ int passed;
+    pdl_trigger();
     pdl_wait();
-    norm_partial_cta(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1], partial, flag);
+    norm_partial_cta<kFusedKeepG>(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1],
+                                  partial, flag);
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned long long ticket = atomicAdd(arrivals, 1ull);

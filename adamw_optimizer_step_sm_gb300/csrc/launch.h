@@ -41,8 +41,9 @@ struct adamw_plan {
     int32_t* status = nullptr;         // set by a kernel whose bounded wait ran out
     bool fused = false;                // clipped steps run as one cooperative launch
     unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
-    unsigned int* done = nullptr;  // finished CTAs of a one-launch device step
-    int32_t* flagword = nullptr;   // its non-finite flag, collected across CTAs
+    // one-launch device step: finished CTAs (low 32 bits) and how many of
+    // them saw a non-finite gradient (high 32 bits), in one word
+    unsigned long long* done = nullptr;
     adamw::ScalarMemo* memo = nullptr;  // two slots, see ScalarMemo
 };
 

@@ -421,21 +421,29 @@ def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
         zc_plan.step(hp, state["t"] + 1, grad_norm=norm if clip else None, nonfinite=flag)
         finish_step()
 
+    # each path: args.reps repetitions of k_e2e steps, the median repetition
+    # reported (the host-to-device copies now and then stall for tens of
+    # milliseconds on this host; the median keeps one stall from deciding)
     out = {}
     for name, fn, prime in (("overlapped", overlapped, overlap_prime), ("serial", serial, None),
                             ("zero_copy", zero_copy, None)):
-        torch.cuda.synchronize(device)
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        if prime:
-            prime()
-        for i in range(k_e2e):
-            fn(i)
-        e1.record(stream)
-        e1.synchronize()
-        secs = reduce_max(e0.elapsed_time(e1) / 1e3, world, device)
-        out[name] = {"value": world * N * k_e2e / secs, "ms_per_step": secs / k_e2e * 1e3}
+        reps = []
+        for _ in range(args.reps):
+            torch.cuda.synchronize(device)
+            barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if prime:
+                prime()
+            for i in range(k_e2e):
+                fn(i)
+            e1.record(stream)
+            e1.synchronize()
+            reps.append(reduce_max(e0.elapsed_time(e1) / 1e3, world, device))
+        secs = statistics.median(reps)
+        out[name] = {"value": world * N * k_e2e / secs, "ms_per_step": secs / k_e2e * 1e3,
+                     "ms_per_step_min": min(reps) / k_e2e * 1e3,
+                     "ms_per_step_max": max(reps) / k_e2e * 1e3}
     zc_plan.close()
     torch.cuda.synchronize(device)
     described = {
@@ -452,6 +460,7 @@ def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
     link_gbs = N * 2 / (best["ms_per_step"] / 1e3) / 1e9
     return {"value": best["value"], "unit": UNIT, "h2d_bytes_per_step": int(N * 2),
             "d2h_bytes_per_step": 4, "ms_per_step": best["ms_per_step"], "steps": k_e2e,
+            "repetitions": args.reps,
             "path": described[name], "paths": out,
             "link_gbs": link_gbs, "link_ceiling_gbs": link,
             "frac_of_link": link_gbs / link["ceiling"], "_t": state["t"]}
