@@ -34,6 +34,12 @@ constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
 #define ADAMW_FUSED_KEEP_G 1
 #endif
 constexpr bool kFusedKeepG = ADAMW_FUSED_KEEP_G != 0;
+// Bytes of g (over the whole grid) the fused clipped step asks L2 for before
+// its norm phase, each CTA its share from the start of its norm range.
+#ifndef ADAMW_FUSED_PREFETCH_MB
+#define ADAMW_FUSED_PREFETCH_MB 64
+#endif
+constexpr int64_t kFusedPrefetchBytes = int64_t(ADAMW_FUSED_PREFETCH_MB) << 20;
 
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.

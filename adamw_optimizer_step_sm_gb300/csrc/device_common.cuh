@@ -1144,6 +1144,24 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
     }
 }
 
+// Asks L2 for up to `budget` bytes of g of the CTA's norm chunks [c0, c1):
+// one prefetch per 128-byte line, every address inside its buffer.  The
+// fused clipped step's norm phase is short (each thread makes only a few
+// rounds of loads), so without it the phase is bound by load latency rather
+// than by DRAM; a hint only, it changes no result.
+__device__ __forceinline__ void prefetch_grads_l2(const ChunkPtr* __restrict__ chunks, int32_t c0,
+                                                  int32_t c1, int64_t budget) {
+    for (int32_t ci = c0; ci < c1 && budget > 0; ++ci) {
+        const ChunkPtr ch = load_chunk(chunks + ci);
+        int64_t bytes = (ch.len2 >> 1) * 2;
+        if (bytes > budget) bytes = budget;
+        budget -= bytes;
+        const char* b = static_cast<const char*>(ch.g);
+        for (int64_t off = int64_t(threadIdx.x) * 128; off < bytes; off += int64_t(kBlock) * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
+    }
+}
+
 // ---- device-resident step path ----
 
 // beta^t by binary exponentiation, lowest bit of t first, one IEEE fp64
@@ -1286,7 +1304,13 @@ __device__ __forceinline__ void memo_store(ScalarMemo* memo, const adamw_hparams
 // The barrier is a monotonic 64-bit arrival counter: the CTA whose ticket is
 // t waits until the counter reaches the next multiple of the grid.  The wait
 // is bounded: a CTA that gives up sets *status and returns without updating.
-constexpr uint32_t kBarrierSpins = 1u << 21;   // about a second with the sleeps
+#ifndef ADAMW_BARRIER_SLEEP_NS
+#define ADAMW_BARRIER_SLEEP_NS 64
+#endif
+constexpr uint32_t kBarrierSleepNs = ADAMW_BARRIER_SLEEP_NS;
+// rounds of the bounded wait: about a second, each round a sleep and one
+// load from L2 (a few hundred nanoseconds)
+constexpr uint32_t kBarrierSpins = uint32_t(1000000000ull / (kBarrierSleepNs + 256));
 
 __device__ __forceinline__ unsigned long long load_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
