@@ -34,12 +34,7 @@ constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
 #define ADAMW_FUSED_KEEP_G 1
 #endif
 constexpr bool kFusedKeepG = ADAMW_FUSED_KEEP_G != 0;
-// Bytes of g (over the whole grid) the fused clipped step asks L2 for before
-// its norm phase, each CTA its share from the start of its norm range.
-#ifndef ADAMW_FUSED_PREFETCH_MB
-#define ADAMW_FUSED_PREFETCH_MB 64
-#endif
-constexpr int64_t kFusedPrefetchBytes = int64_t(ADAMW_FUSED_PREFETCH_MB) << 20;
+
 
 // Fewest elements a CTA is given before the grid is shrunk (one vector per
 // thread), so tiny lists do not launch idle CTAs.
@@ -124,6 +119,16 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 #ifndef ADAMW_BALANCE_ALIGN
 #define ADAMW_BALANCE_ALIGN 256
 #endif
+// 1: the fused clipped step is a cooperative launch; 0: an ordinary one.
+#ifndef ADAMW_FUSED_COOP
+#define ADAMW_FUSED_COOP 1
+#endif
+// 1: the norm pass takes the update's round-robin tile partition on its own
+// grid; 0: one contiguous range per CTA.
+#ifndef ADAMW_NORM_INTERLEAVE
+#define ADAMW_NORM_INTERLEAVE 1
+#endif
+constexpr bool kNormInterleave = ADAMW_NORM_INTERLEAVE != 0;
 constexpr int64_t kTileElems = ADAMW_TILE_ELEMS;
 constexpr int64_t kCutAlign = ADAMW_CUT_ALIGN;
 constexpr int64_t kBalanceAlign = ADAMW_BALANCE_ALIGN;

@@ -332,7 +332,10 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
         chunk_pointers(host_table, mode, part, &cp);
     }
     if (grid_norm > 0) {
-        rc = build_partition(host_table, n_tensors, mode, grid_norm, 0, &part_norm);
+        // the norm pass reads g in round-robin tiles like the update (the
+        // whole grid in one narrow window of g), or in contiguous ranges
+        rc = build_partition(host_table, n_tensors, mode, grid_norm,
+                             kNormInterleave ? update_tile_elems(total, grid_norm) : 0, &part_norm);
         if (rc != ADAMW_OK) return rc;
         chunk_pointers(host_table, mode, part_norm, &cp_norm);
     }

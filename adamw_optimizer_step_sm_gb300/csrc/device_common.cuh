@@ -1144,24 +1144,6 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
     }
 }
 
-// Asks L2 for up to `budget` bytes of g of the CTA's norm chunks [c0, c1):
-// one prefetch per 128-byte line, every address inside its buffer.  The
-// fused clipped step's norm phase is short (each thread makes only a few
-// rounds of loads), so without it the phase is bound by load latency rather
-// than by DRAM; a hint only, it changes no result.
-__device__ __forceinline__ void prefetch_grads_l2(const ChunkPtr* __restrict__ chunks, int32_t c0,
-                                                  int32_t c1, int64_t budget) {
-    for (int32_t ci = c0; ci < c1 && budget > 0; ++ci) {
-        const ChunkPtr ch = load_chunk(chunks + ci);
-        int64_t bytes = (ch.len2 >> 1) * 2;
-        if (bytes > budget) bytes = budget;
-        budget -= bytes;
-        const char* b = static_cast<const char*>(ch.g);
-        for (int64_t off = int64_t(threadIdx.x) * 128; off < bytes; off += int64_t(kBlock) * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
-    }
-}
-
 // ---- device-resident step path ----
 
 // beta^t by binary exponentiation, lowest bit of t first, one IEEE fp64

@@ -119,9 +119,6 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
     __shared__ int passed;
     pdl_trigger();
     pdl_wait();
-    if (kFusedPrefetchBytes > 0)
-        prefetch_grads_l2(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1],
-                          kFusedPrefetchBytes / gridDim.x);
     norm_partial_cta<kFusedKeepG>(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1],
                                   partial, flag);
     if (threadIdx.x == 0) {
