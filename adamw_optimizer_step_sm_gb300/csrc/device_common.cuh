@@ -968,6 +968,10 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
 // the errors.  Sum2F32x2 below does this on two lanes at once.
 __device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
 
+// Rounds of 8 vectors (64 elements, 32 per lane) between flushes of the
+// norm's error-free groups into fp64.
+constexpr int kNormFlushRounds = 4;
+
 // Packed fp32x2 arithmetic (two IEEE round-to-nearest operations in one
 // instruction on sm_100 and later): a 64-bit value holds two floats, lane 0
 // in the low word.
@@ -999,7 +1003,8 @@ __device__ __forceinline__ float f2_hi(uint64_t x) { return __uint_as_float(uint
 // needs no ordering of its operands (so it packs, and a NaN term stays in
 // the sum, where the flush's range check sees it).  Per lane: s + e is the
 // exact sum of the lane's terms since the last flush, up to the rounding of
-// e itself; groups of at most 32 terms per lane.
+// e itself (relative 2^-24 of an e that is itself at most 2^-17 of s for the
+// 128 terms per lane of a group); the group length only bounds that.
 struct Sum2F32x2 {
     uint64_t s = 0, e = 0;
     __device__ __forceinline__ void add(uint64_t x) {
@@ -1008,15 +1013,19 @@ struct Sum2F32x2 {
         e = f2_add(e, f2_add(f2_sub(s, f2_sub(t, b)), f2_sub(x, b)));
         s = t;
     }
-    // Adds both lanes' groups to (acc, err) (lane 0 first) and restarts
-    // them; false when a group left the range where squares are exact and
-    // sums finite.
+    // Adds both lanes' groups to (acc, err) and restarts them: the two lane
+    // sums are joined exactly in fp32 (TwoSum again; its error goes to err
+    // with the lanes' own), so the slow fp64 unit sees one conversion and
+    // one addition per flush.  False when a group left the range where
+    // squares are exact and sums finite.
     __device__ __forceinline__ bool flush(double& acc, float& err) {
         const float s0 = f2_lo(s), s1 = f2_hi(s);
         const bool ok = s0 < 0x1p100f && s1 < 0x1p100f;   // also false for inf and NaN
-        acc += double(s0);
-        acc += double(s1);
-        err = __fadd_rn(__fadd_rn(err, f2_lo(e)), f2_hi(e));
+        const float t = __fadd_rn(s0, s1);
+        const float b = __fsub_rn(t, s0);
+        const float e01 = __fadd_rn(__fsub_rn(s0, __fsub_rn(t, b)), __fsub_rn(s1, b));
+        acc += double(t);
+        err = __fadd_rn(err, __fadd_rn(__fadd_rn(f2_lo(e), f2_hi(e)), e01));
         s = 0;
         e = 0;
         return ok;
@@ -1076,7 +1085,7 @@ __device__ __forceinline__ double block_sum(double x) {
 // Stage 1 of the global norm: one fp64 partial and one flag per CTA, over the
 // norm's own partition (so the result depends only on the plan).
 // Fast path: error-free fp32 group sums of the exact squares, two lanes
-// packed (the low and the high bf16 of each word), flushed every 64
+// packed (the low and the high bf16 of each word), flushed every 256
 // elements.  A thread whose groups leave [2^-100, 2^100) (huge, tiny, inf or
 // NaN gradients) recomputes its elements in fp64, which also decides the
 // non-finite flag.
@@ -1092,6 +1101,7 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
     float err = 0.0f;
     bool in_range = true;
     uint32_t nz = 0;
+    int rounds = 0;
     auto add_word = [&](uint32_t w) {
         const uint64_t x = bf16x2_to_f2(w);
         grp.add(f2_mul(x, x));
@@ -1110,7 +1120,12 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
             add_word(h);   // the high lane adds an exact zero
             in_range &= grp.flush(acc, err);
         },
-        [&]() { in_range &= grp.flush(acc, err); });
+        [&]() {
+            if (++rounds == kNormFlushRounds) {   // 8 x 32 elements between flushes
+                rounds = 0;
+                in_range &= grp.flush(acc, err);
+            }
+        });
     in_range &= grp.flush(acc, err);
     double tot = acc + double(err);
     bool bad = false;
