@@ -119,6 +119,16 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 #ifndef ADAMW_BALANCE_ALIGN
 #define ADAMW_BALANCE_ALIGN 256
 #endif
+// The norm pass's resident CTAs per SM (its grid is that times the SMs) and
+// 16-byte vectors of g in flight per thread.
+#ifndef ADAMW_NORM_CTAS
+#define ADAMW_NORM_CTAS 4
+#endif
+#ifndef ADAMW_NORM_UNROLL
+#define ADAMW_NORM_UNROLL 8
+#endif
+constexpr int kNormCtas = ADAMW_NORM_CTAS;
+constexpr int kNormUnroll = ADAMW_NORM_UNROLL;
 // 1: the fused clipped step is a cooperative launch; 0 (measured 2 us
 // faster per step on the 13.85M shard): an ordinary one, with programmatic
 // serialization.  Its grid never exceeds what the device holds at once (the

@@ -39,8 +39,9 @@ using namespace adamw;
 
 namespace {
 
-// Four CTAs per SM (64 registers): the occupancy the norm's grid is sized by.
-__global__ void __launch_bounds__(kBlock, 4)
+// kNormCtas CTAs per SM (four: 64 registers), the occupancy the norm's grid
+// is sized by.
+__global__ void __launch_bounds__(kBlock, kNormCtas)
 norm_partial_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin,
                     double* __restrict__ partial, int32_t* __restrict__ flag) {
@@ -308,7 +309,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     int occ = di.occ[var][kPlain];
     for (int k = 0; k < 3; ++k) occ = occ < di.occ[var][k] ? occ : di.occ[var][k];
     if (occ < 1) occ = 1;
-    const int occ_norm = di.occ_norm > 0 ? di.occ_norm : 1;
+    int occ_norm = di.occ_norm > 0 ? di.occ_norm : 1;
+    if (occ_norm > kNormCtas) occ_norm = kNormCtas;
 
     int64_t total = 0;
     for (int32_t k = 0; k < n_tensors; ++k) total += host_table[k].numel;

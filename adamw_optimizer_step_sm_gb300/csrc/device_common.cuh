@@ -70,11 +70,15 @@ __device__ __forceinline__ uint4 ld16(const void* p) {
     return *q;
 #endif
 }
-// A 16-byte load that asks L2 to keep the line (evict-last policy): for g in
-// the fused clipped step's norm phase, which the update phase reads again.
-__device__ __forceinline__ uint4 ld16_keep(const void* p) {
+// A 16-byte load that asks L2 to keep the line (the evict-last policy made
+// by keep_policy()): for g in the fused clipped step's norm phase, which the
+// update phase reads again.
+__device__ __forceinline__ uint64_t keep_policy() {
     uint64_t policy;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+__device__ __forceinline__ uint4 ld16_keep(const void* p, uint64_t policy) {
     uint4 r;
     asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
@@ -968,9 +972,9 @@ __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, 
 // the errors.  Sum2F32x2 below does this on two lanes at once.
 __device__ __forceinline__ float sq(float x) { return __fmul_rn(x, x); }
 
-// Rounds of 8 vectors (64 elements, 32 per lane) between flushes of the
-// norm's error-free groups into fp64.
-constexpr int kNormFlushRounds = 4;
+// Rounds of kNormUnroll vectors between flushes of the norm's error-free
+// groups into fp64: 256 elements (128 per lane).
+constexpr int kNormFlushRounds = 32 / kNormUnroll > 0 ? 32 / kNormUnroll : 1;
 
 // Packed fp32x2 arithmetic (two IEEE round-to-nearest operations in one
 // instruction on sm_100 and later): a 64-bit value holds two floats, lane 0
@@ -1039,6 +1043,7 @@ template <int U, bool KEEP = false, typename FV, typename FE, typename FI>
 __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ chunks,
                                                  int32_t c0, int32_t c1, FV vec, FE elem,
                                                  FI after_iter) {
+    const uint64_t policy = KEEP ? keep_policy() : 0;
     for (int32_t ci = c0; ci < c1; ++ci) {
         const ChunkPtr ch = load_chunk(chunks + ci);
         const uint16_t* g = static_cast<const uint16_t*>(ch.g);
@@ -1054,7 +1059,7 @@ __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ ch
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t i = base + int64_t(u) * kBlock;
-                    if (i < nvec) w[u] = KEEP ? ld16_keep(g + i * kVec) : ld16(g + i * kVec);
+                    if (i < nvec) w[u] = KEEP ? ld16_keep(g + i * kVec, policy) : ld16(g + i * kVec);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -1106,7 +1111,7 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
         const uint64_t x = bf16x2_to_f2(w);
         grp.add(f2_mul(x, x));
     };
-    for_thread_grads<8, KEEP>(
+    for_thread_grads<kNormUnroll, KEEP>(
         chunks, c0, c1,
         [&](const uint4& w) {
             nz |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
@@ -1121,7 +1126,7 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
             in_range &= grp.flush(acc, err);
         },
         [&]() {
-            if (++rounds == kNormFlushRounds) {   // 8 x 32 elements between flushes
+            if (++rounds == kNormFlushRounds) {   // 256 elements between flushes
                 rounds = 0;
                 in_range &= grp.flush(acc, err);
             }
