@@ -1039,13 +1039,14 @@ struct Sum2F32x2 {
 // Walks the g elements of one CTA's chunks that belong to this thread, in a
 // fixed order: vec(w) gets 8 packed bf16, elem(h) one bf16, after_iter() runs
 // after every group of U vectors.
+// `pre`, when set, is chunk c0 already loaded.
 template <int U, bool KEEP = false, typename FV, typename FE, typename FI>
 __device__ __forceinline__ void for_thread_grads(const ChunkPtr* __restrict__ chunks,
                                                  int32_t c0, int32_t c1, FV vec, FE elem,
-                                                 FI after_iter) {
+                                                 FI after_iter, const ChunkPtr* pre = nullptr) {
     const uint64_t policy = KEEP ? keep_policy() : 0;
     for (int32_t ci = c0; ci < c1; ++ci) {
-        const ChunkPtr ch = load_chunk(chunks + ci);
+        const ChunkPtr ch = (pre && ci == c0) ? *pre : load_chunk(chunks + ci);
         const uint16_t* g = static_cast<const uint16_t*>(ch.g);
         const int64_t len = ch.len2 >> 1;
 #if ADAMW_CHECK_BOUNDS
@@ -1097,10 +1098,12 @@ __device__ __forceinline__ double block_sum(double x) {
 // The CTA's partial sum of squares and non-finite flag, written to
 // partial[blockIdx.x] and flag[blockIdx.x].
 // KEEP: load g with the evict-last L2 policy (the fused step reads it again).
+// `pre`, when set, is chunk c0 already loaded.
 template <bool KEEP = false>
 __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                                  int32_t c1, double* __restrict__ partial,
-                                                 int32_t* __restrict__ flag) {
+                                                 int32_t* __restrict__ flag,
+                                                 const ChunkPtr* pre = nullptr) {
     Sum2F32x2 grp;
     double acc = 0.0;
     float err = 0.0f;
@@ -1130,7 +1133,8 @@ __device__ __forceinline__ void norm_partial_cta(const ChunkPtr* __restrict__ ch
                 rounds = 0;
                 in_range &= grp.flush(acc, err);
             }
-        });
+        },
+        pre);
     in_range &= grp.flush(acc, err);
     double tot = acc + double(err);
     bool bad = false;

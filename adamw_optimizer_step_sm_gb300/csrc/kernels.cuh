@@ -117,10 +117,13 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         int32_t* __restrict__ user_flag, unsigned long long* __restrict__ arrivals,
                         int32_t* __restrict__ status) {
     __shared__ int passed;
+    // the chunk tables are written once, when the plan is made
+    const int32_t n0 = nrm_begin[blockIdx.x], n1 = nrm_begin[blockIdx.x + 1];
+    ChunkPtr first;
+    if (n0 < n1) first = load_chunk(nrm_chunks + n0);
     pdl_trigger();
     pdl_wait();
-    norm_partial_cta<kFusedKeepG>(nrm_chunks, nrm_begin[blockIdx.x], nrm_begin[blockIdx.x + 1],
-                                  partial, flag);
+    norm_partial_cta<kFusedKeepG>(nrm_chunks, n0, n1, partial, flag, n0 < n1 ? &first : nullptr);
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned long long ticket = atomicAdd(arrivals, 1ull);
