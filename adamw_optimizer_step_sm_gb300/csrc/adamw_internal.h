@@ -18,14 +18,15 @@ constexpr int kBlock = ADAMW_BLOCK;
 // Elements per vector: 8 bf16 = one 16-byte load; 8 fp32 = two.
 constexpr int kVec = 8;
 // Largest gradient list (MiB of bf16 gradients) whose clipped steps run as
-// one fused launch.  Measured on GB300 with the fp32-master mode: the fused
-// step saves about 6 us up to 40M parameters (the update re-reads g from
-// L2) and still 2-3 us at 56M and 80M (launches saved), but at 1.3B it is
-// 0.7 % slower (its norm pass runs on the update grid, half the CTAs of the
-// norm pass's own grid).  160 MiB = 80M parameters, the largest size
-// measured as a win.
+// one fused launch.  Measured on GB300 with the fp32-master mode, every
+// kernel launched with programmatic dependent launch (median us per step,
+// fused / three launches): 2M parameters 24.7 / 27.5, 4M 34.1 / 36.0, 8M
+// 49.4 / 50.5, 13.85M 70.6 / 71.9, then 24M 117.5 / 116.7, 40M 190.4 /
+// 187.9, 80M 373.3 / 371.0: the three launches overlap their ramps, and the
+// fused norm phase runs on the update's grid (half the norm kernel's CTAs).
+// 32 MiB = 16.7M parameters, between the last win and the first loss.
 #ifndef ADAMW_FUSED_MAX_GRAD_MB
-#define ADAMW_FUSED_MAX_GRAD_MB 160
+#define ADAMW_FUSED_MAX_GRAD_MB 32
 #endif
 constexpr int64_t kFusedMaxGradBytes = int64_t(ADAMW_FUSED_MAX_GRAD_MB) << 20;
 // 1: the fused clipped step's norm phase loads g with the evict-last L2

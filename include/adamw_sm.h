@@ -187,7 +187,7 @@ typedef struct {
  * CTAs per SM, fewer for small lists), uploads the tensor table and the chunk
  * table, and (with ADAMW_PLAN_NORM) builds the norm kernel's own partition
  * and allocates the norm workspace.  With ADAMW_PLAN_NORM, a list whose
- * gradients take at most 160 MiB (80M parameters) runs its clipped steps as
+ * gradients take at most 32 MiB (16.7M parameters) runs its clipped steps as
  * one cooperative launch: norm partials, a bounded grid barrier, and the
  * update reading g again (from L2 where it fits) (unless ADAMW_PLAN_NO_FUSE;
  * adamw_plan_info_t.fused says which).  The norm is the same either way.
