@@ -101,6 +101,7 @@ def load_peaks() -> dict:
 
 
 KERNEL_SOURCES = ("adamw_internal.h", "device_common.cuh", "kernels.cuh", "launch.h",
+                  "adamw_sm.cu", "plan_build.cpp",
                   "update_mode.inc", "update_m0.cu", "update_m1.cu", "update_m2.cu",
                   "update_m3.cu", "update_m4.cu", "update_m17.cu", "update_m19.cu",
                   "update_m20.cu", "update_m21.cu", "update_m22.cu", "update_m23.cu",
@@ -108,7 +109,8 @@ KERNEL_SOURCES = ("adamw_internal.h", "device_common.cuh", "kernels.cuh", "launc
 
 
 def kernel_source_hash() -> str:
-    """Hash of the files that define the kernels and their data layout."""
+    """Hash of the files that define the kernels, their launches and the
+    partition (what decides the DRAM traffic of a launch)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "adamw_optimizer_step_sm_gb300", "csrc")
