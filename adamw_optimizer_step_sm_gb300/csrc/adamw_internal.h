@@ -130,6 +130,36 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 #endif
 constexpr int kNormCtas = ADAMW_NORM_CTAS;
 constexpr int kNormUnroll = ADAMW_NORM_UNROLL;
+// 1: the update's last rounds (about kDynSharePct percent of the list) are
+// not dealt to CTAs but cut into tiles of kTileElems that the CTAs claim
+// with an atomic counter once their own tiles are done, so that CTAs on SMs
+// that stream faster take more of them.  Measured on GB300 before this, the
+// CTAs of one launch with equal work ended up to 8 % apart (the 1.3B list:
+// 3.29 to 3.58 ms, median 3.41), SM to SM.
+#ifndef ADAMW_DYN_TAIL
+#define ADAMW_DYN_TAIL 1
+#endif
+#ifndef ADAMW_DYN_SHARE_PCT
+#define ADAMW_DYN_SHARE_PCT 12
+#endif
+// Lists of fewer rounds keep every tile dealt: there one tile is a large part
+// of a CTA's work and the claims cost more than they even out (measured,
+// fp32 master: the 13.85M shard, 6 rounds, 0.5 % slower with claims, 8 %
+// with claims of whole tiles; 8M, 3 rounds, 5 % slower; bf16 Kahan lists of
+// 40M to 80M, 11 to 21 rounds, 2 to 3 % faster).
+#ifndef ADAMW_DYN_MIN_ROUNDS
+#define ADAMW_DYN_MIN_ROUNDS 8
+#endif
+// 1: the claimable tiles shrink towards the end of the list (each about the
+// work left over twice the grid, between kCutAlign and kTileElems), so the
+// last claims are short and the CTAs end closer together.
+#ifndef ADAMW_DYN_GUIDED
+#define ADAMW_DYN_GUIDED 1
+#endif
+constexpr bool kDynTail = ADAMW_DYN_TAIL != 0 && !ADAMW_BULK;
+constexpr int kDynSharePct = ADAMW_DYN_SHARE_PCT;
+constexpr int64_t kDynMinRounds = ADAMW_DYN_MIN_ROUNDS;
+constexpr bool kDynGuided = ADAMW_DYN_GUIDED != 0;
 // 1: the fused clipped step is a cooperative launch; 0 (measured 2 us
 // faster per step on the 13.85M shard): an ordinary one, with programmatic
 // serialization.  Its grid never exceeds what the device holds at once (the
@@ -184,6 +214,24 @@ struct ScalarMemo {
 };
 static_assert(sizeof(ScalarMemo) == 96, "memo layout");
 
+// The plan's claim-and-arrival word of the update partition, one 64-bit
+// atomic word: bits 0-23 count the claims of last-round pieces, bits 24-43
+// the CTAs that have finished (the last one to arrive zeroes the word for
+// the next launch), bits 44-63 the CTAs that saw a non-finite gradient (the
+// one-launch device step's flag).
+constexpr unsigned long long kSyncClaim = 1ull;
+constexpr unsigned long long kSyncArrive = 1ull << 24;
+constexpr unsigned long long kSyncFlagged = 1ull << 44;
+constexpr unsigned long long kSyncClaimMask = kSyncArrive - 1;
+constexpr unsigned long long kSyncArriveMask = (kSyncFlagged - 1) & ~kSyncClaimMask;
+
+// Where the claimable last-round chunks are, for the kernels.
+struct DynTail {
+    int32_t begin;                  // index of the first claimable chunk
+    int32_t n;                      // how many (0: none, no claims, no arrivals)
+    unsigned long long* sync;       // the claim-and-arrival word
+};
+
 // Kernel flavours: plain step, clipped step (reads the norm finalize's
 // output, skips on non-finite), plain step that also reports non-finite g.
 enum Kind { kPlain = 0, kClip = 1, kReport = 2 };
@@ -212,10 +260,14 @@ int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out);
 
 // Splits the list over `grid` CTAs.  chunks are ordered by CTA; cta_begin has
 // grid + 1 entries (chunks of CTA b are [cta_begin[b], cta_begin[b+1])).
+// Chunks of the last round of the interleaved partition may be left to
+// whichever CTA is free (chunk_cta -1): they follow every CTA's own chunks,
+// from index cta_begin[grid], n_dyn of them, and are claimed at run time.
 struct Partition {
     std::vector<ChunkDev> chunks;
     std::vector<int32_t> chunk_cta;
     std::vector<int32_t> cta_begin;
+    int64_t n_dyn = 0;
     int64_t total = 0;
     int64_t scalar_elems = 0;
 };

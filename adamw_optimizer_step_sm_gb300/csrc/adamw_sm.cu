@@ -387,7 +387,8 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     P->rec = reinterpret_cast<StepRecord*>(b + o_r);
     P->status = reinterpret_cast<int32_t*>(b + o_s);
     P->arrivals = reinterpret_cast<unsigned long long*>(b + o_a);
-    P->done = reinterpret_cast<unsigned long long*>(b + o_d);
+    P->sync = reinterpret_cast<unsigned long long*>(b + o_d);
+    P->upd.dyn = DynTail{grid > 0 ? part.cta_begin[size_t(grid)] : 0, int32_t(part.n_dyn), P->sync};
     P->memo = reinterpret_cast<ScalarMemo*>(b + o_m);
     P->fused = fused;
 #if ADAMW_CHECK_BOUNDS
@@ -552,14 +553,18 @@ extern "C" int adamw_plan_device_status(adamw_plan_t plan, int32_t* out) {
                  "cudaMemcpy(status)"))
         return ADAMW_ERR_CUDA;
     if (*out != 0) {
-        // a wait ran out: clear the word and realign the fused-step barrier
-        // counter (no kernel of the plan is running after the synchronise)
+        // a wait ran out: clear the word, realign the fused-step barrier
+        // counter and zero the claim-and-arrival word, which a launch that
+        // gave up may have left part-counted (no kernel of the plan is
+        // running after the synchronise)
         const int32_t zero = 0;
         const unsigned long long start = 0;
         if (!cuda_ok(cudaMemcpy(plan->status, &zero, sizeof(int32_t), cudaMemcpyHostToDevice),
                      "cudaMemcpy(status)") ||
             !cuda_ok(cudaMemcpy(plan->arrivals, &start, sizeof(start), cudaMemcpyHostToDevice),
-                     "cudaMemcpy(arrivals)"))
+                     "cudaMemcpy(arrivals)") ||
+            !cuda_ok(cudaMemcpy(plan->sync, &start, sizeof(start), cudaMemcpyHostToDevice),
+                     "cudaMemcpy(sync)"))
             return ADAMW_ERR_CUDA;
     }
     return ADAMW_OK;

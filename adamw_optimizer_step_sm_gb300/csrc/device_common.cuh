@@ -213,17 +213,29 @@ struct UpdateTuning {
 #else
     static constexpr int kUnroll = kU;
 #endif
+    // Resident CTAs per SM the update kernel reaches with the tuning above
+    // (kB where set; otherwise what its registers allowed when the table was
+    // fitted).  Where the code around the element loop (the claim loop of the
+    // last rounds, the device step's bookkeeping) would cost a CTA per SM,
+    // launch bounds hold this occupancy for the modes at 3 or 4 CTAs per SM
+    // (at 2 the registers leave room, and the kernels keep the code they
+    // were tuned with).
+    static constexpr int kOcc =
+        kB > 0 ? kB
+        : MODE == ADAMW_MODE_BF16_PLAIN ? 4
+        : (MODE == ADAMW_MODE_BF16_KAHAN || MODE == (ADAMW_MODE_ANYPREC | 9) ||
+           MODE == (ADAMW_MODE_ANYPREC | 10)) ? 3
+        : 2;
 #ifdef ADAMW_MIN_BLOCKS
     static constexpr int kMinBlocks = ADAMW_MIN_BLOCKS;
 #else
-    static constexpr int kMinBlocks = kB;
+    static constexpr int kMinBlocks = kOcc >= 3 ? kOcc : kB;
 #endif
     // The one-launch device step runs on the update's grid, so it must reach
-    // the same occupancy.  Left to itself it does in every mode but bf16
-    // without compensation, whose update fits 64 registers (4 CTAs per SM)
-    // and whose device step would take 70.
-    static constexpr int kSelfMinBlocks =
-        (kMinBlocks == 0 && MODE == ADAMW_MODE_BF16_PLAIN) ? 4 : kMinBlocks;
+    // the same occupancy.
+    static constexpr int kSelfMinBlocks = kMinBlocks;
+    // The fused clipped step: the update's own tuning.
+    static constexpr int kFusedMinBlocks = kB;
 };
 
 template <int K, int U>
@@ -855,6 +867,7 @@ __device__ __forceinline__ void remainder_elem_chunk(const ChunkPtr& t, int64_t 
 // The update: CTA b walks chunks [cta_begin[b], cta_begin[b+1]).
 #define ADAMW_UPDATE_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kMinBlocks)
 #define ADAMW_SELF_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kSelfMinBlocks)
+#define ADAMW_FUSED_BOUNDS(MODE) __launch_bounds__(kBlock, UpdateTuning<MODE>::kFusedMinBlocks)
 
 // One chunk descriptor, read through the read-only path.
 __device__ __forceinline__ ChunkPtr load_chunk(const ChunkPtr* c) {
@@ -913,55 +926,90 @@ __device__ __forceinline__ bool chunk_in_bounds(const ChunkPtr& c, int64_t len, 
 }
 #endif
 
-// ---- the CTA's share of the update: chunks [c0, c1), each chunk's
-// descriptor fetched one ahead; `cur` holds chunk c0 already (when c0 < c1).
+// ---- one chunk of the update
+template <int MODE, int K>
+__device__ __forceinline__ void update_chunk(const ChunkPtr& cur, const StepScalars& s, float coef,
+                                             bool& bad) {
+    constexpr int kU = UpdateTuning<MODE>::kUnroll;
+    const int64_t len = cur.len2 >> 1;
+    const bool vec = cur.len2 & 1;
+#if ADAMW_CHECK_BOUNDS
+    if (!chunk_in_bounds<MODE>(cur, len)) return;
+#endif
+    if constexpr (MODE == ADAMW_MODE_BF16_KAHAN) {
+        if (vec) kahan_vec_chunk<K, kU>(cur, len, s, coef, bad);
+        else kahan_elem_chunk<K>(cur, len, s, coef, bad);
+    } else if constexpr (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
+        if (vec) mixed_vec_chunk<K, kU>(cur, len, s, coef, bad);
+        else mixed_elem_chunk<K>(cur, len, s, coef, bad);
+    } else if constexpr (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
+        if (vec) remainder_vec_chunk<K, kU>(cur, len, s, coef, bad);
+        else remainder_elem_chunk<K>(cur, len, s, coef, bad);
+    } else if constexpr (MODE == ADAMW_MODE_BF16_PLAIN) {
+        if (vec) plain_vec_chunk<K, kU>(cur, len, s, coef, bad);
+        else plain_elem_chunk<K>(cur, len, s, coef, bad);
+    } else if constexpr (MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR) {
+        if (vec) kahan_v32_vec_chunk<K, kU>(cur, len, s, coef, bad);
+        else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
+    } else {
+        constexpr int kFlags = MODE & ~ADAMW_MODE_ANYPREC;
+        if (vec) anyprec_vec_chunk<kFlags, K, kU>(cur, len, s, coef, bad);
+        else anyprec_elem_chunk<kFlags, K>(cur, len, s, coef, bad);
+    }
+}
+
+// ---- the CTA's share of the update: its own chunks [c0, c1), each chunk's
+// descriptor fetched one ahead (`cur` holds chunk c0 already when c0 < c1),
+// then claimable chunks until none is left.
 template <int MODE, int K>
 __device__ __forceinline__ void update_cta_from(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                                 int32_t c1, ChunkPtr cur, const StepScalars& s,
-                                                float coef, bool& bad) {
-    constexpr int kU = UpdateTuning<MODE>::kUnroll;
+                                                float coef, bool& bad, const DynTail& dyn) {
     for (int32_t ci = c0; ci < c1; ++ci) {
         ChunkPtr nxt = cur;
         if (ci + 1 < c1) nxt = load_chunk(chunks + ci + 1);
-        const int64_t len = cur.len2 >> 1;
-        const bool vec = cur.len2 & 1;
-#if ADAMW_CHECK_BOUNDS
-        if (!chunk_in_bounds<MODE>(cur, len)) {
-            cur = nxt;
-            continue;
-        }
-#endif
-        if constexpr (MODE == ADAMW_MODE_BF16_KAHAN) {
-            if (vec) kahan_vec_chunk<K, kU>(cur, len, s, coef, bad);
-            else kahan_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if constexpr (MODE == ADAMW_MODE_MIXED_FP32_MASTER) {
-            if (vec) mixed_vec_chunk<K, kU>(cur, len, s, coef, bad);
-            else mixed_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if constexpr (MODE == ADAMW_MODE_MIXED_BF16_REMAINDER) {
-            if (vec) remainder_vec_chunk<K, kU>(cur, len, s, coef, bad);
-            else remainder_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if constexpr (MODE == ADAMW_MODE_BF16_PLAIN) {
-            if (vec) plain_vec_chunk<K, kU>(cur, len, s, coef, bad);
-            else plain_elem_chunk<K>(cur, len, s, coef, bad);
-        } else if constexpr (MODE == ADAMW_MODE_BF16_KAHAN_FP32_VAR) {
-            if (vec) kahan_v32_vec_chunk<K, kU>(cur, len, s, coef, bad);
-            else kahan_v32_elem_chunk<K>(cur, len, s, coef, bad);
-        } else {
-            constexpr int kFlags = MODE & ~ADAMW_MODE_ANYPREC;
-            if (vec) anyprec_vec_chunk<kFlags, K, kU>(cur, len, s, coef, bad);
-            else anyprec_elem_chunk<kFlags, K>(cur, len, s, coef, bad);
-        }
+        update_chunk<MODE, K>(cur, s, coef, bad);
         cur = nxt;
     }
+    if (dyn.n == 0) return;
+    // Claims: thread 0 asks for the next piece when a piece starts and
+    // hands the answer over when it ends, so the atomic's latency overlaps
+    // the piece.  A claim at or past n means the list is done.
+    __shared__ int32_t claim_sh;
+    if (threadIdx.x == 0) claim_sh = int32_t(atomicAdd(dyn.sync, kSyncClaim) & kSyncClaimMask);
+    __syncthreads();
+    int32_t i = claim_sh;
+    while (i < dyn.n) {
+        const ChunkPtr piece = load_chunk(chunks + dyn.begin + i);
+        __syncthreads();   // every thread has read claim_sh
+        unsigned long long next = 0;
+        if (threadIdx.x == 0) next = atomicAdd(dyn.sync, kSyncClaim);
+        update_chunk<MODE, K>(piece, s, coef, bad);
+        if (threadIdx.x == 0) claim_sh = int32_t(next & kSyncClaimMask);
+        __syncthreads();
+        i = claim_sh;
+    }
+}
+
+// The CTA has finished: counts its arrival (and, with `flagged`, that it saw
+// a non-finite gradient) in the claim-and-arrival word; returns the word as
+// it was before, with this arrival and flag added.  The last CTA to arrive
+// zeroes the word.  Thread 0 only.
+__device__ __forceinline__ unsigned long long sync_arrive(unsigned long long* sync, bool flagged,
+                                                          uint32_t grid) {
+    const unsigned long long add = kSyncArrive + (flagged ? kSyncFlagged : 0ull);
+    const unsigned long long w = atomicAdd(sync, add) + add;
+    if (((w & kSyncArriveMask) / kSyncArrive) == grid) *sync = 0;
+    return w;
 }
 
 template <int MODE, int K>
 __device__ __forceinline__ void update_cta(const ChunkPtr* __restrict__ chunks, int32_t c0,
                                            int32_t c1, const StepScalars& s, float coef,
-                                           bool& bad) {
+                                           bool& bad, const DynTail& dyn) {
     ChunkPtr cur;
     if (c0 < c1) cur = load_chunk(chunks + c0);
-    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad);
+    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad, dyn);
 }
 
 // Error-free fp32 accumulation of non-negative terms.  Squares of bf16 values

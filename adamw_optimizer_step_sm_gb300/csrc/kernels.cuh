@@ -15,7 +15,7 @@ __global__ void ADAMW_UPDATE_BOUNDS(MODE)
 adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
                     const NormOut* __restrict__ norm, int32_t* __restrict__ report,
-                    const StepRecord* __restrict__ rec) {
+                    const StepRecord* __restrict__ rec, DynTail dyn) {
     // the chunk table is written once, when the plan is made: read the first
     // descriptor before waiting for the kernel this one may overlap
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
@@ -33,7 +33,8 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
         coef = norm->coef;
     }
     bool bad = false;
-    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad);
+    update_cta_from<MODE, K>(chunks, c0, c1, cur, s, coef, bad, dyn);
+    if (dyn.n > 0 && threadIdx.x == 0) sync_arrive(dyn.sync, false, gridDim.x);
     if (K == kReport) {
         if (__syncthreads_or(bad) && threadIdx.x == 0) *report = 1;
     }
@@ -48,18 +49,18 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
 // the scalars of t + 1 into the memo while the others still stream (so a
 // run of steps with unchanged hyperparameters computes each step's scalars
 // off the critical path); the last CTA to finish -- found with an arrival
-// counter that also counts the CTAs that saw a non-finite gradient, one
-// atomic per CTA -- advances the counter and writes the non-finite flag, so
-// no CTA can read a counter that was already advanced (each CTA's read of it
-// has returned before its arrival is counted).  The kernel's end publishes
-// the last CTA's writes and the memo.  Invalid hyperparameters: nothing is
-// updated, the flag is -1.
+// counter in the plan's claim-and-arrival word, which also counts the CTAs
+// that saw a non-finite gradient, one atomic per CTA -- advances the counter
+// and writes the non-finite flag, so no CTA can read a counter that was
+// already advanced (each CTA's read of it has returned before its arrival
+// is counted).  The kernel's end publishes the last CTA's writes and the
+// memo.  Invalid hyperparameters: nothing is updated, the flag is -1.
 template <int MODE, int K>
 __global__ void ADAMW_SELF_BOUNDS(MODE)
 adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __restrict__ cta_begin,
                          const adamw_hparams_t* __restrict__ d_hp, int64_t* __restrict__ d_step,
-                         unsigned long long* __restrict__ done, int32_t* __restrict__ user_flag,
-                         ScalarMemo* __restrict__ memo) {
+                         int32_t* __restrict__ user_flag, ScalarMemo* __restrict__ memo,
+                         DynTail dyn) {
     __shared__ StepScalars s_sh;
     __shared__ adamw_hparams_t hp_sh;
     __shared__ int valid_sh, hit_sh;
@@ -87,27 +88,26 @@ adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
     __syncthreads();
     if (valid_sh && !hit_sh) make_scalars_cta(hp_sh, t_sh, &s_sh);
     bool bad = false;
-    if (valid_sh) update_cta_from<MODE, K>(chunks, c0, c1, cur, s_sh, 1.0f, bad);
+    if (valid_sh) update_cta_from<MODE, K>(chunks, c0, c1, cur, s_sh, 1.0f, bad, dyn);
     const int any = (K == kReport) ? __syncthreads_or(bad) : 0;
-    if (threadIdx.x == 0) ticket_sh = atomicAdd(done, 1ull + (any ? (1ull << 32) : 0ull)) + (any ? (1ull << 32) : 0ull);
+    if (threadIdx.x == 0) ticket_sh = sync_arrive(dyn.sync, any != 0, gridDim.x);
     __syncthreads();
     const unsigned long long ticket = ticket_sh;   // the word with this CTA's arrival
-    const unsigned int arrived = unsigned(ticket & 0xffffffffu);
+    const unsigned int arrived = unsigned((ticket & kSyncArriveMask) / kSyncArrive) - 1u;
     if (arrived == 0 && valid_sh) {
         // the first CTA done: the next step's scalars, for the memo
         __shared__ StepScalars next_sh;
         make_scalars_cta(hp_sh, t_sh + 1, &next_sh);
         if (threadIdx.x == 0) memo_store(memo, hp_sh, t_sh + 1, next_sh);
     }
-    if (threadIdx.x == 0 && arrived == gridDim.x - 1) {  // the last CTA
+    if (threadIdx.x == 0 && arrived == gridDim.x - 1) {  // the last CTA (it zeroed the word)
         if (valid_sh) *d_step = t_sh;
-        if (user_flag) *user_flag = valid_sh ? int32_t((ticket >> 32) != 0) : -1;
-        *done = 0;
+        if (user_flag) *user_flag = valid_sh ? int32_t(ticket >= kSyncFlagged) : -1;
     }
 }
 
 template <int MODE>
-__global__ void ADAMW_UPDATE_BOUNDS(MODE)
+__global__ void ADAMW_FUSED_BOUNDS(MODE)
 adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         const int32_t* __restrict__ upd_begin,
                         const ChunkPtr* __restrict__ nrm_chunks,
@@ -115,7 +115,7 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
                         double* __restrict__ partial, int32_t* __restrict__ flag,
                         NormOut* __restrict__ nout, double* __restrict__ user_norm,
                         int32_t* __restrict__ user_flag, unsigned long long* __restrict__ arrivals,
-                        int32_t* __restrict__ status) {
+                        int32_t* __restrict__ status, DynTail dyn) {
     __shared__ int passed;
     // the chunk tables are written once, when the plan is made
     const int32_t n0 = nrm_begin[blockIdx.x], n1 = nrm_begin[blockIdx.x + 1];
@@ -168,7 +168,8 @@ adamw_fused_clip_kernel(const ChunkPtr* __restrict__ upd_chunks,
     if (any) return;  // skipped step: no writes
     bool unused = false;
     update_cta<MODE, kClip>(upd_chunks, upd_begin[blockIdx.x], upd_begin[blockIdx.x + 1], s,
-                            coef_sh, unused);
+                            coef_sh, unused, dyn);
+    if (dyn.n > 0 && threadIdx.x == 0) sync_arrive(dyn.sync, false, gridDim.x);
 }
 
 // ------------------------------------------- bulk-copy staged update (A) --

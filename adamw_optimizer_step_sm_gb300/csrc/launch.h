@@ -20,6 +20,7 @@ struct DevPartition {
     int64_t n_chunks = 0;
     adamw::ChunkPtr* chunks = nullptr;
     int32_t* cta_begin = nullptr;
+    adamw::DynTail dyn = {0, 0, nullptr};   // claimable chunks (update partition only)
 };
 
 struct adamw_plan {
@@ -41,9 +42,8 @@ struct adamw_plan {
     int32_t* status = nullptr;         // set by a kernel whose bounded wait ran out
     bool fused = false;                // clipped steps run as one cooperative launch
     unsigned long long* arrivals = nullptr;  // grid-barrier counter of the fused kernel
-    // one-launch device step: finished CTAs (low 32 bits) and how many of
-    // them saw a non-finite gradient (high 32 bits), in one word
-    unsigned long long* done = nullptr;
+    // the update partition's claim-and-arrival word (kSyncClaim ...)
+    unsigned long long* sync = nullptr;
     adamw::ScalarMemo* memo = nullptr;  // two slots, see ScalarMemo
 };
 

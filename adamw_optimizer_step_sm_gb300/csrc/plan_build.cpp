@@ -10,6 +10,7 @@
 // tiles of about 8K elements on 2048-element boundaries of the flattened list
 // and dealt round-robin (the grid sweeps the buffers together), small lists
 // and the norm pass into one contiguous range per CTA.
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -258,43 +259,70 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
         // elements.  Cuts that end a tile of the last round move up to
         // kBalanceAlign only (there the quota's leftover is taken), all
         // others to kCutAlign.
+        //
+        // With kDynTail (and at least kDynMinRounds rounds) the last rounds
+        // (kDynSharePct percent of k, at least one, never all) are not
+        // dealt: from there on the list is cut into tiles (owner -1) that
+        // the CTAs claim at run time, of tile_elems, or with kDynGuided of
+        // the work left over twice the grid, rounded up to kCutAlign and
+        // capped at tile_elems.
         const TileSchedule sched(P.total, grid, tile_elems);
+        const bool dyn = kDynTail && sched.k >= 2 && sched.k >= kDynMinRounds;
+        int64_t claim_rounds = (sched.k * kDynSharePct + 99) / 100;
+        if (claim_rounds < 1) claim_rounds = 1;
+        if (claim_rounds > sched.k - 1) claim_rounds = sched.k - 1;
+        const int64_t n_dealt = dyn ? (sched.k - claim_rounds) * int64_t(grid) : INT64_MAX;
+        const int64_t two_grids = 2 * int64_t(grid);
+        auto size_of = [&](int64_t j, int64_t start) {
+            if (j < n_dealt) return sched.size(j);
+            if (!kDynGuided) return tile_elems;
+            const int64_t left = P.total - start;
+            const int64_t want = left > 0 ? (left + two_grids - 1) / two_grids : 0;
+            const int64_t sz = (want + kCutAlign - 1) / kCutAlign * kCutAlign;
+            return sz < kCutAlign ? kCutAlign : sz > tile_elems ? tile_elems : sz;
+        };
         std::vector<ChunkDev> pieces;
         std::vector<int32_t> owner;
-        int64_t flat = 0, tile = 0, boundary = sched.size(0);
+        int64_t flat = 0, tile = 0, boundary = size_of(0, 0);
         for (const Seg& s : segs) {
             int64_t pos = 0;
             while (pos < s.len) {
                 int64_t take = s.len - pos;
                 if (take > boundary - flat) {
                     take = boundary - flat;
-                    const int64_t align = sched.last_round(tile) ? kBalanceAlign : kCutAlign;
+                    const int64_t align =
+                        (!dyn && sched.last_round(tile)) ? kBalanceAlign : kCutAlign;
                     if (s.vec) take = (pos + take + align - 1) / align * align - pos;
                     if (take > s.len - pos) take = s.len - pos;
                 }
                 pieces.push_back({s.k, s.vec, s.off + pos, take});
-                owner.push_back(int32_t(tile % grid));
+                owner.push_back(tile < n_dealt ? int32_t(tile % grid) : -1);
                 pos += take;
                 flat += take;
                 while (flat >= boundary) {
                     ++tile;
-                    boundary += sched.size(tile);
+                    boundary += size_of(tile, boundary);
                 }
             }
         }
-        std::vector<int64_t> count(size_t(grid) + 1, 0);
-        for (int32_t b : owner) ++count[size_t(b) + 1];
-        for (int32_t b = 0; b < grid; ++b) count[b + 1] += count[b];
+        // every CTA's own chunks in CTA order, then the claimable ones
+        std::vector<int64_t> count(size_t(grid) + 2, 0);
+        for (int32_t b : owner) ++count[size_t(b < 0 ? grid : b) + 1];
+        for (int32_t b = 0; b <= grid; ++b) count[b + 1] += count[b];
         P.chunks.resize(pieces.size());
         P.chunk_cta.resize(pieces.size());
         std::vector<int64_t> fill(count.begin(), count.end() - 1);
         for (size_t j = 0; j < pieces.size(); ++j) {
-            const int32_t b = owner[j];
+            const int32_t b = owner[j] < 0 ? grid : owner[j];
             P.chunks[fill[b]] = pieces[j];
-            P.chunk_cta[fill[b]] = b;
+            P.chunk_cta[fill[b]] = owner[j];
             ++fill[b];
         }
         for (int32_t b = 0; b <= grid; ++b) P.cta_begin[b] = int32_t(count[b]);
+        P.n_dyn = count[size_t(grid) + 1] - count[size_t(grid)];
+        // every claim (one per claimable chunk, plus each CTA's last, empty
+        // one) is counted in the claim field of the sync word
+        if (uint64_t(P.n_dyn) + uint64_t(grid) > kSyncClaimMask) return ADAMW_ERR_TOO_LARGE;
         return ADAMW_OK;
     }
 

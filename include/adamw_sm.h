@@ -178,7 +178,8 @@ typedef struct {
     int32_t vec;     /* 1: 16-byte vector path, 0: element path          */
     int64_t offset;  /* first element, relative to the tensor's base     */
     int64_t len;     /* elements                                         */
-    int32_t cta;     /* CTA that processes the piece                     */
+    int32_t cta;     /* CTA that processes the piece; -1: claimed at run
+                        time by whichever CTA runs out of its own first  */
     int32_t pad_;
 } adamw_chunk_t;
 
@@ -370,12 +371,11 @@ int adamw_copy_probe(void* dst, const void* src, int64_t bytes,
  * d_grad_norm (nullable, device fp64) and d_nonfinite (nullable, device
  *   int32) receive the norm and the flag, as in adamw_grad_norm.
  * The first call on a device sets that device up (looks up the scratch
- * address and the grid size) with it current; make that first call before
- * any stream capture.  All calls share the one scratch array, which keeps the
- * last call's contents (nothing in it needs to start at zero): calls that
- * overlap on the GPU, on any streams, race.  The sum runs in a fixed order
- * for a given device, but not the order of adamw_grad_norm, so the two norms
- * agree to fp64 rounding, not bit for bit.
+ * address and the grid size) with it current.  All calls share the one
+ * scratch array, which keeps the last call's contents (nothing in it needs
+ * to start at zero): calls that overlap on the GPU, on any streams, race.
+ * The sum runs in a fixed order for a given device, but not the order of
+ * adamw_grad_norm, so the two norms agree to fp64 rounding, not bit for bit.
  * Errors: INVALID_ARG (n_tensors < 0, NULL table or grad with numel > 0,
  * numel < 0), TOO_LARGE (n_tensors > ADAMW_NOALLOC_MAX_TENSORS, or a device
  * index of 64 or more), MISALIGNED (odd grad address), CUDA. */

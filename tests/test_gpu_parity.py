@@ -225,6 +225,51 @@ def test_interleaved_partition_over_ragged_tensors(mode, clip, layout):
     assert rep.exact == rep.n
 
 
+def _claimable(gpu: H.GpuSide) -> int:
+    """Chunks of the plan's update partition that CTAs claim at run time."""
+    v = gpu.st.views
+    entries = [tuple(t.data_ptr() if t is not None else 0 for t in ts) + (ts[0].numel(),)
+               for ts in zip(v(gpu.st.param), v(gpu.g), v(gpu.st.exp_avg), v(gpu.st.exp_avg_sq),
+                             v(gpu.st.aux))]
+    return sum(c.cta < 0 for c in A.adamw_plan_chunks(entries, gpu.w.mode, gpu.plan.info.grid))
+
+
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.0), (W.MODE_MIXED, 0.5),
+                                       (W.MODE_REMAINDER, 0.0)])
+def test_claimed_tiles_match_oracle_on_host_and_device_paths(mode, clip):
+    """A list of more than 8 rounds of tiles, whose last rounds are not dealt
+    to CTAs but claimed at run time (ragged tensors, so claimed tiles span
+    tensor boundaries and the pieces shrink towards the end): every element
+    against the oracle over three steps on the host path, and the
+    device-resident step, whose claims share the word with its arrival
+    count, bit-identical to the host path."""
+    sizes = [30_000_001, 7, 6_500_003, 65_537, 1, 4_194_304, 1_048_583]
+    w = _small("claimed", mode=mode, sizes=sizes, max_grad_norm=clip, steps=3)
+    probe = H.GpuSide(w)
+    assert _claimable(probe) > probe.plan.info.grid, "no claimable tiles"
+    probe.plan.close()
+    del probe
+    rep, log = H.run_parity(w, align_elems=1, skew=3)
+    _assert(rep, log)
+    assert rep.exact == rep.n
+    a, b_state, b_plan = _twin(w)
+    hp, _ = H.hp_pair(w)
+    d_hp = A.device_hparams(hp)
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    n_b = torch.zeros(1, dtype=torch.float64, device="cuda")
+    f_b = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k in range(1, 4):
+        a.set_grad(k)
+        a.step(hp)
+        b_plan.step_device(d_hp, d_step, A.STEP_CLIP if clip else 0,
+                           grad_norm=n_b if clip else None, nonfinite=f_b)
+    torch.cuda.synchronize()
+    assert int(d_step.item()) == a.t == 3 and int(f_b.item()) == 0
+    _same_state(a.st, b_state)
+    a.plan.close()
+    b_plan.close()
+
+
 @pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
 def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     w = _small("skip", mode=mode, max_grad_norm=1.0, inf_at=(2, 8, 777), steps=4)
