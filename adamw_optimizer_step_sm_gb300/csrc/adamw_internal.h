@@ -104,6 +104,13 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 #ifndef ADAMW_TILE_ELEMS
 #define ADAMW_TILE_ELEMS 8192
 #endif
+// The nominal tile of lists that would get fewer than kDynMinRounds rounds of
+// ADAMW_TILE_ELEMS: with smaller tiles they get more rounds, and claimable
+// last rounds once those reach kDynMinRounds.  Equal to ADAMW_TILE_ELEMS:
+// one tile size for every list.
+#ifndef ADAMW_SMALL_TILE_ELEMS
+#define ADAMW_SMALL_TILE_ELEMS ADAMW_TILE_ELEMS
+#endif
 // 1: tiles cut in the flattened list and stretched so every CTA gets the
 // same number (cuts inside a tensor at multiples of ADAMW_CUT_ALIGN elements
 // from its vector body's start); 0: fixed tiles cut per tensor.
@@ -168,11 +175,23 @@ constexpr bool kDynGuided = ADAMW_DYN_GUIDED != 0;
 #ifndef ADAMW_FUSED_COOP
 #define ADAMW_FUSED_COOP 0
 #endif
+// Elements by which CTA 0's share of the update partition is short of the
+// others': in the one-launch device step CTA 0 first computes the next
+// step's scalars for the memo (fp64, about 1 us on GB300) while the other
+// CTAs stream, and this keeps it from ending last (on lists of up to ~4096
+// elements per CTA it gets none).  A multiple of kBalanceAlign.
+#ifndef ADAMW_MEMO_RELIEF
+#define ADAMW_MEMO_RELIEF 4096
+#endif
+constexpr int64_t kMemoRelief = ADAMW_MEMO_RELIEF;
 constexpr int64_t kTileElems = ADAMW_TILE_ELEMS;
+constexpr int64_t kSmallTileElems = ADAMW_SMALL_TILE_ELEMS;
 constexpr int64_t kCutAlign = ADAMW_CUT_ALIGN;
 constexpr int64_t kBalanceAlign = ADAMW_BALANCE_ALIGN;
 static_assert(kCutAlign % kVec == 0 && kTileElems % kCutAlign == 0, "tile cut alignment");
+static_assert(kSmallTileElems % kCutAlign == 0 && kSmallTileElems <= kTileElems, "small tile");
 static_assert(kBalanceAlign % kVec == 0 && kCutAlign % kBalanceAlign == 0, "balance granule");
+static_assert(kMemoRelief >= 0 && kMemoRelief % kBalanceAlign == 0, "relief granule");
 
 // Output of the norm finalize kernel, read by the clipped update.
 struct NormOut {
@@ -191,18 +210,22 @@ struct StepScalars {
 // What the device-resident step path (adamw_step_device) decides before the
 // update runs: the scalars of t = *d_step + 1, the clip coefficient, and
 // whether the step is skipped (1: non-finite gradient under clipping,
-// 2: invalid hyperparameters).
+// 2: invalid hyperparameters); with the hyperparameters and t they came
+// from, for the next step's memo.
 struct StepRecord {
     StepScalars s;
     float coef;
     int32_t skip;
-    int32_t pad_[2];
+    adamw_hparams_t hp;
+    int32_t pad_;
+    int64_t t;
 };
 
 // The per-step scalars of one (hyperparameters, t), remembered on the device
-// by the device-resident step: the first CTA to finish step t computes the
-// scalars of t + 1 into slot (t + 1) & 1 while the others still stream, so
-// that the next step reads them instead of computing them again.  `key` is
+// by the device-resident step: CTA 0 of step t's update computes the scalars
+// of t + 1 into slot (t + 1) & 1 first, while the others stream (its share
+// of the list is kMemoRelief elements short for that), so that the next step
+// reads them instead of computing them again.  `key` is
 // the bit pattern of the six hyperparameters and of t; `valid` is 0 in a
 // slot never written.  A slot that does not match is recomputed, so the
 // record only saves time, never changes a result.
@@ -213,6 +236,20 @@ struct ScalarMemo {
     int32_t pad_[6];
 };
 static_assert(sizeof(ScalarMemo) == 96, "memo layout");
+
+// The squares beta^(2^i), i = 0..63, of both betas, as the binary
+// exponentiation computes them (each the previous one squared, rounded to
+// fp64), keyed by the betas' bit patterns; `valid` is 0 until written.  With
+// them beta^t is one multiplication per set bit of t, in the same order and
+// with the same roundings as the exponentiation itself.  It sits in the plan
+// right after the two memo slots; CTA 0 of an update writes and reads it
+// (memo_next), nothing else does.
+struct PowTable {
+    uint32_t b1, b2;
+    int32_t valid;
+    int32_t pad_;
+    double sq[2][64];
+};
 
 // The plan's claim-and-arrival word of the update partition, one 64-bit
 // atomic word: bits 0-23 count the claims of last-round pieces, bits 24-43
@@ -263,6 +300,8 @@ int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out);
 // Chunks of the last round of the interleaved partition may be left to
 // whichever CTA is free (chunk_cta -1): they follow every CTA's own chunks,
 // from index cta_begin[grid], n_dyn of them, and are claimed at run time.
+// CTA 0's share is `relief` elements short of the others' (kMemoRelief for
+// the update partition, 0 for the norm pass's).
 struct Partition {
     std::vector<ChunkDev> chunks;
     std::vector<int32_t> chunk_cta;
@@ -272,7 +311,8 @@ struct Partition {
     int64_t scalar_elems = 0;
 };
 int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
-                    int32_t grid, int64_t tile_elems, Partition* out);
+                    int32_t grid, int64_t tile_elems, Partition* out,
+                    int64_t relief = kMemoRelief);
 
 // Device chunks (pointers offset per stream element size) of a partition.
 void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& P,
@@ -282,22 +322,26 @@ void chunk_pointers(const adamw_tensor_t* table, int32_t mode, const Partition& 
 int32_t choose_grid(int64_t total, int32_t max_grid);
 
 // Nominal tile of the update kernel's partition for a list of `total`
-// elements on `grid` CTAs: kTileElems when every CTA gets at least two
-// tiles, else 0 (contiguous ranges).
+// elements on `grid` CTAs: 0 (contiguous ranges) when a CTA would get fewer
+// than two tiles of kTileElems, kSmallTileElems when it would get fewer than
+// kDynMinRounds, else kTileElems.
 int64_t update_tile_elems(int64_t total, int32_t grid);
 
 // Sizes of the interleaved partition's tiles.  With k rounds (the whole
 // number nearest to total / (grid * tile_elems)), tile j belongs to CTA
-// j % grid in round j / grid.  Each CTA's quota is total / grid rounded to
-// kBalanceAlign elements (quotas differ by one granule at most); a CTA's k
-// tiles are that quota's whole kCutAlign units shared out as evenly as the
-// rounds allow (earlier rounds take the extra units), and its last-round
-// tile also takes the quota's leftover granules.  Sizes are in the flattened
-// list; the cuts themselves still move to each tensor's alignment grid.
+// j % grid in round j / grid.  CTA 0's quota is total / grid less
+// `relief` elements (never below zero; with one CTA, everything); the
+// other CTAs share the rest, each quota rounded to kBalanceAlign elements
+// (theirs differ by one granule at most); a CTA's k tiles are that quota's
+// whole kCutAlign units shared out as evenly as the rounds allow (earlier
+// rounds take the extra units; a short quota leaves some rounds empty), and
+// its last-round tile also takes the quota's leftover granules.  Sizes are
+// in the flattened list; the cuts themselves still move to each tensor's
+// alignment grid.
 struct TileSchedule {
     int32_t grid;
-    int64_t k = 1, base = 0, extra = 0;
-    TileSchedule(int64_t total, int32_t grid, int64_t tile_elems);
+    int64_t k = 1, q0 = 0, base = 0, extra = 0;   // quotas in kBalanceAlign units
+    TileSchedule(int64_t total, int32_t grid, int64_t tile_elems, int64_t relief);
     int64_t size(int64_t j) const;
     bool last_round(int64_t j) const { return j / grid >= k - 1; }
 };

@@ -142,6 +142,8 @@ step_prologue_kernel(const adamw_hparams_t* __restrict__ d_hp, int64_t* __restri
         r.coef = coef_sh;
         if (!r.skip) {
             r.s = s_sh;
+            r.hp = hp_sh;
+            r.t = t_sh;
             *d_step = t_sh;
         }
         *rec = r;
@@ -337,7 +339,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     if (grid_norm > 0) {
         // contiguous ranges (measured faster for the norm pass than the
         // update's round-robin tiles: 56.9 against 62.9 us on OPT-125m)
-        rc = build_partition(host_table, n_tensors, mode, grid_norm, 0, &part_norm);
+        rc = build_partition(host_table, n_tensors, mode, grid_norm, 0, &part_norm, 0);
         if (rc != ADAMW_OK) return rc;
         chunk_pointers(host_table, mode, part_norm, &cp_norm);
     }
@@ -369,7 +371,7 @@ extern "C" int adamw_plan_create(const adamw_tensor_t* host_table, int32_t n_ten
     const size_t o_s = off; off = align_up(off + sizeof(int32_t), 256);
     const size_t o_a = off; off = align_up(off + sizeof(unsigned long long), 256);
     const size_t o_d = off; off = align_up(off + sizeof(unsigned long long), 256);
-    const size_t o_m = off; off = align_up(off + 2 * sizeof(ScalarMemo), 256);
+    const size_t o_m = off; off = align_up(off + 2 * sizeof(ScalarMemo) + sizeof(PowTable), 256);
 
     if (!cuda_ok(cudaMalloc(&P->block, off), "cudaMalloc")) {
         delete P;

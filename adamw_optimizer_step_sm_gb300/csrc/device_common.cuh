@@ -1237,15 +1237,26 @@ __device__ bool hparams_valid_dev(const adamw_hparams_t& hp) {
            hp.beta1 < 1.0f && hp.beta2 >= 0.0f && hp.beta2 < 1.0f;
 }
 
+// The same power from the squares of beta the exponentiation would compute
+// (sq[i] = beta^(2^i)): one multiplication per set bit of t, lowest first,
+// so the same roundings in the same order.
+__device__ double beta_power_sq(const double* sq, int64_t t) {
+    double result = 1.0;
+    for (int i = 0; t > 0; ++i, t >>= 1)
+        if (t & 1) result = __dmul_rn(result, sq[i]);
+    return result;
+}
+
 // The host planner's make_scalars, operation for operation, in two halves
 // that share nothing, so that two warps can evaluate them at once: part 0
 // the beta1 side (step_size, omb1) plus the values copied or derived from lr,
 // eps, weight_decay and max_grad_norm; part 1 the beta2 side (sbc2, omb2).
+// With `sq` (that part's beta's squares) the power takes them from there.
 __device__ __noinline__ void make_scalars_part(const adamw_hparams_t& hp, int64_t t, int part,
-                                  StepScalars* out) {
+                                  StepScalars* out, const double* sq = nullptr) {
     if (part == 0) {
         const double b1 = hp.beta1;
-        const double bc1 = __dsub_rn(1.0, beta_power_dev(b1, t));
+        const double bc1 = __dsub_rn(1.0, sq ? beta_power_sq(sq, t) : beta_power_dev(b1, t));
         out->beta1 = hp.beta1;
         out->omb1 = __double2float_rn(__dsub_rn(1.0, b1));
         out->step_size = __double2float_rn(__ddiv_rn(double(hp.lr), bc1));
@@ -1254,7 +1265,7 @@ __device__ __noinline__ void make_scalars_part(const adamw_hparams_t& hp, int64_
         out->max_grad_norm = hp.max_grad_norm;
     } else {
         const double b2 = hp.beta2;
-        const double bc2 = __dsub_rn(1.0, beta_power_dev(b2, t));
+        const double bc2 = __dsub_rn(1.0, sq ? beta_power_sq(sq, t) : beta_power_dev(b2, t));
         out->beta2 = hp.beta2;
         out->omb2 = __double2float_rn(__dsub_rn(1.0, b2));
         out->sbc2 = __double2float_rn(__dsqrt_rn(bc2));
@@ -1347,6 +1358,54 @@ __device__ __forceinline__ void memo_store(ScalarMemo* memo, const adamw_hparams
 #pragma unroll
     for (int i = 0; i < 8; ++i) m->key[i] = k[i];
     m->valid = 1;
+}
+
+// The next step's scalars into the memo, from the squares table (built
+// here first when the betas changed): warps 0 and 1 read the table's
+// header and both rows in one round trip, then threads 0 and 32 evaluate
+// the two halves at once.  Every thread of the CTA calls it; it ends with a
+// barrier.  Only CTA 0 of a device-resident update calls it, so the table
+// has no other reader or writer while it runs.
+__device__ __noinline__ void memo_next(ScalarMemo* memo, const adamw_hparams_t& hp, int64_t t) {
+    PowTable* tab = reinterpret_cast<PowTable*>(memo + 2);
+    __shared__ double sq_sh[2][64];
+    __shared__ int ok_sh;
+    __shared__ StepScalars next_sh;
+    const uint32_t b1 = __float_as_uint(hp.beta1), b2 = __float_as_uint(hp.beta2);
+    if (threadIdx.x < 64) {
+        const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const double2 v = __ldcg(reinterpret_cast<const double2*>(tab->sq[row]) + lane);
+        sq_sh[row][2 * lane] = v.x;
+        sq_sh[row][2 * lane + 1] = v.y;
+        if (threadIdx.x == 0)
+            ok_sh = __ldcg(&tab->valid) != 0 && __ldcg(&tab->b1) == b1 && __ldcg(&tab->b2) == b2;
+    }
+    __syncthreads();
+    if (!ok_sh) {
+        // new betas: the squares, one row per thread, kept for later steps
+        if ((threadIdx.x & 31) == 0 && threadIdx.x < 64) {
+            double sq = threadIdx.x == 0 ? double(hp.beta1) : double(hp.beta2);
+            double* row = sq_sh[threadIdx.x >> 5];
+            for (int i = 0; i < 64; ++i) {
+                row[i] = sq;
+                sq = __dmul_rn(sq, sq);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            const int row = threadIdx.x >> 6, i = threadIdx.x & 63;
+            tab->sq[row][i] = sq_sh[row][i];
+        }
+        if (threadIdx.x == 0) {
+            tab->b1 = b1;
+            tab->b2 = b2;
+            tab->valid = 1;
+        }
+    }
+    if (threadIdx.x == 0) make_scalars_part(hp, t + 1, 0, &next_sh, sq_sh[0]);
+    else if (threadIdx.x == 32) make_scalars_part(hp, t + 1, 1, &next_sh, sq_sh[1]);
+    __syncthreads();
+    if (threadIdx.x == 0) memo_store(memo, hp, t + 1, next_sh);
 }
 
 // ---- fused clipped step (one cooperative launch) ----

@@ -9,13 +9,15 @@
 namespace {
 
 // DEV: the scalars, clip coefficient and skip decision come from the
-// StepRecord the device-resident step path's prologue wrote.
+// StepRecord the device-resident step path's prologue wrote; CTA 0 also
+// computes the next step's scalars into the memo.
 template <int MODE, int K, bool DEV>
 __global__ void ADAMW_UPDATE_BOUNDS(MODE)
 adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
                     const int32_t* __restrict__ cta_begin, StepScalars s,
                     const NormOut* __restrict__ norm, int32_t* __restrict__ report,
-                    const StepRecord* __restrict__ rec, DynTail dyn) {
+                    const StepRecord* __restrict__ rec, ScalarMemo* __restrict__ memo,
+                    DynTail dyn) {
     // the chunk table is written once, when the plan is made: read the first
     // descriptor before waiting for the kernel this one may overlap
     const int32_t c0 = cta_begin[blockIdx.x], c1 = cta_begin[blockIdx.x + 1];
@@ -24,10 +26,20 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
     pdl_trigger();
     pdl_wait();
     float coef = 1.0f;
-    if (DEV) {
+    if constexpr (DEV) {
         if (__ldcg(&rec->skip)) return;   // skipped step: no writes at all
         s = rec->s;
         coef = rec->coef;
+        if (blockIdx.x == 0) {
+            __shared__ adamw_hparams_t hp_sh;
+            __shared__ int64_t t_sh;
+            if (threadIdx.x == 0) {
+                hp_sh = rec->hp;
+                t_sh = rec->t;
+            }
+            __syncthreads();
+            memo_next(memo, hp_sh, t_sh);
+        }
     } else if (K == kClip) {
         if (__ldcg(&norm->nonfinite)) return;  // skipped step: no writes at all
         coef = norm->coef;
@@ -45,10 +57,11 @@ adamw_update_kernel(const ChunkPtr* __restrict__ chunks,
 // Thread 0 of every CTA reads the hyperparameters and the step counter and
 // looks up the scalars of t = *d_step + 1 in the plan's two-slot memo; on a
 // miss warps 0 and 1 compute them (the host planner's fp64 operations, two
-// independent halves at once).  The first CTA to finish its share computes
-// the scalars of t + 1 into the memo while the others still stream (so a
-// run of steps with unchanged hyperparameters computes each step's scalars
-// off the critical path); the last CTA to finish -- found with an arrival
+// independent halves at once).  CTA 0, whose share of the list is short by
+// about that much work, first computes the scalars of t + 1 into the memo
+// while the others stream (so a run of steps with unchanged
+// hyperparameters computes each step's scalars off the critical path); the
+// last CTA to finish -- found with an arrival
 // counter in the plan's claim-and-arrival word, which also counts the CTAs
 // that saw a non-finite gradient, one atomic per CTA -- advances the counter
 // and writes the non-finite flag, so no CTA can read a counter that was
@@ -87,6 +100,7 @@ adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
     }
     __syncthreads();
     if (valid_sh && !hit_sh) make_scalars_cta(hp_sh, t_sh, &s_sh);
+    if (blockIdx.x == 0 && valid_sh) memo_next(memo, hp_sh, t_sh);
     bool bad = false;
     if (valid_sh) update_cta_from<MODE, K>(chunks, c0, c1, cur, s_sh, 1.0f, bad, dyn);
     const int any = (K == kReport) ? __syncthreads_or(bad) : 0;
@@ -94,12 +108,6 @@ adamw_update_self_kernel(const ChunkPtr* __restrict__ chunks, const int32_t* __r
     __syncthreads();
     const unsigned long long ticket = ticket_sh;   // the word with this CTA's arrival
     const unsigned int arrived = unsigned((ticket & kSyncArriveMask) / kSyncArrive) - 1u;
-    if (arrived == 0 && valid_sh) {
-        // the first CTA done: the next step's scalars, for the memo
-        __shared__ StepScalars next_sh;
-        make_scalars_cta(hp_sh, t_sh + 1, &next_sh);
-        if (threadIdx.x == 0) memo_store(memo, hp_sh, t_sh + 1, next_sh);
-    }
     if (threadIdx.x == 0 && arrived == gridDim.x - 1) {  // the last CTA (it zeroed the word)
         if (valid_sh) *d_step = t_sh;
         if (user_flag) *user_flag = valid_sh ? int32_t(ticket >= kSyncFlagged) : -1;

@@ -159,27 +159,38 @@ int32_t choose_grid(int64_t total, int32_t max_grid) {
 
 int64_t update_tile_elems(int64_t total, int32_t grid) {
     if (kTileElems <= 0 || grid <= 0) return 0;
-    if (total < 2 * int64_t(grid) * kTileElems) return 0;
+    const int64_t row = int64_t(grid) * kTileElems;
+    if (total < 2 * row) return 0;
+    // fewer than kDynMinRounds rounds: the small tile
+    if ((total + row / 2) / row < kDynMinRounds) return kSmallTileElems;
     return kTileElems;
 }
 
-TileSchedule::TileSchedule(int64_t total, int32_t grid_, int64_t tile_elems) : grid(grid_) {
+TileSchedule::TileSchedule(int64_t total, int32_t grid_, int64_t tile_elems, int64_t relief_elems)
+    : grid(grid_) {
     // k rounds, the whole number nearest to total / (grid * tile_elems)
     const int64_t per_row = int64_t(grid) * tile_elems;
     k = (total + per_row / 2) / per_row;
     if (k < 1) k = 1;
-    // each CTA's quota in units of kBalanceAlign elements, equal to one unit
+    // quotas in units of kBalanceAlign elements: CTA 0 short by the relief,
+    // the others equal to one unit
     const int64_t units = (total + kBalanceAlign - 1) / kBalanceAlign;
-    base = units / grid;
-    extra = units % grid;
-    // no round without a cut-aligned unit for every CTA
-    const int64_t min_whole = base / (kCutAlign / kBalanceAlign);
+    if (grid == 1) {
+        q0 = units;
+    } else {
+        const int64_t even = units / grid, relief = relief_elems / kBalanceAlign;
+        q0 = even > relief ? even - relief : 0;
+        base = (units - q0) / (grid - 1);
+        extra = (units - q0) % (grid - 1);
+    }
+    // no round without a cut-aligned unit for every CTA but CTA 0
+    const int64_t min_whole = (grid == 1 ? q0 : base) / (kCutAlign / kBalanceAlign);
     if (k > min_whole) k = min_whole > 1 ? min_whole : 1;
 }
 
 int64_t TileSchedule::size(int64_t j) const {
     const int64_t r = j / grid, b = j % grid;
-    const int64_t q = base + (b < extra ? 1 : 0);          // quota, balance units
+    const int64_t q = b == 0 ? q0 : base + (b - 1 < extra ? 1 : 0);   // quota, balance units
     constexpr int64_t per_cut = kCutAlign / kBalanceAlign;
     const int64_t whole = q / per_cut, rest = q % per_cut;  // cut-aligned units + leftover
     int64_t sz = (whole / k + (r < whole % k ? 1 : 0)) * kCutAlign;
@@ -188,10 +199,12 @@ int64_t TileSchedule::size(int64_t j) const {
 }
 
 int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
-                    int32_t grid, int64_t tile_elems, Partition* out) {
+                    int32_t grid, int64_t tile_elems, Partition* out, int64_t relief) {
     int rc = validate_table(table, n, mode);
     if (rc != ADAMW_OK) return rc;
-    if (!out || grid < 0 || tile_elems < 0 || tile_elems % kVec) return ADAMW_ERR_INVALID_ARG;
+    if (!out || grid < 0 || tile_elems < 0 || tile_elems % kVec || relief < 0 ||
+        relief % kBalanceAlign)
+        return ADAMW_ERR_INVALID_ARG;
     Partition& P = *out;
     P = Partition();
     for (int32_t k = 0; k < n; ++k) P.total += table[k].numel;
@@ -266,7 +279,7 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
         // the CTAs claim at run time, of tile_elems, or with kDynGuided of
         // the work left over twice the grid, rounded up to kCutAlign and
         // capped at tile_elems.
-        const TileSchedule sched(P.total, grid, tile_elems);
+        const TileSchedule sched(P.total, grid, tile_elems, relief);
         const bool dyn = kDynTail && sched.k >= 2 && sched.k >= kDynMinRounds;
         int64_t claim_rounds = (sched.k * kDynSharePct + 99) / 100;
         if (claim_rounds < 1) claim_rounds = 1;
@@ -326,22 +339,29 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
         return ADAMW_OK;
     }
 
-    // Contiguous: an even split of the flattened element space; cuts inside
-    // a vector body fall on multiples of kVec from the body's start so every
-    // chunk of it starts 16-byte aligned.
-    const int64_t target = ((P.total + grid - 1) / grid + kVec - 1) / kVec * kVec;
+    // Contiguous: an even split of the flattened element space, CTA 0's
+    // share `relief` short (never below zero); cuts inside a vector body
+    // fall on multiples of kVec from the body's start so every chunk of it
+    // starts 16-byte aligned.
+    auto round_vec = [](int64_t x) { return (x + kVec - 1) / kVec * kVec; };
+    const int64_t even = round_vec((P.total + grid - 1) / grid);
+    const int64_t target0 = grid == 1 ? P.total : even > relief ? even - relief : 0;
+    const int64_t target =
+        grid == 1 ? P.total : round_vec((P.total - target0 + grid - 2) / (grid - 1));
     int32_t cta = 0;
     int64_t filled = 0;
     for (const Seg& s : segs) {
         int64_t pos = 0;
         while (pos < s.len) {
-            if (filled >= target && cta < grid - 1) {
+            const int64_t want = cta == 0 ? target0 : target;
+            if (filled >= want && cta < grid - 1) {
                 ++cta;
                 filled = 0;
+                continue;
             }
             int64_t take = s.len - pos;
-            if (cta < grid - 1 && take > target - filled) {
-                int64_t cap = target - filled;
+            if (cta < grid - 1 && take > want - filled) {
+                int64_t cap = want - filled;
                 take = s.vec ? (cap + kVec - 1) / kVec * kVec : cap;
                 if (take > s.len - pos) take = s.len - pos;
             }
