@@ -572,17 +572,19 @@ def run_gpu(args):
     extra = {}
     if flush:
         # the same steps back to back with a warm L2, and as one CUDA graph of
-        # device-resident steps (no launch gaps), for context
-        # (median of the repetitions for both; the graph replayed once
-        # untimed first, which uploads it to the device)
+        # device-resident steps (no launch gaps), for context; both on one
+        # plan (one gradient buffer), as a training loop runs them: its
+        # device-step memo then holds each next step's scalars (median of
+        # the repetitions for both; the graph replayed once untimed first,
+        # which uploads it to the device)
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         warm_s = []
         for _ in range(max(1, args.reps)):
             e0.record(stream)
             for i in range(args.steps):
-                plans[i % n_grad].step(hp, t + 1, grad_norm=norm if clip else None,
-                                       nonfinite=flag if clip else None)
+                plans[0].step(hp, t + 1, grad_norm=norm if clip else None,
+                              nonfinite=flag if clip else None)
                 t += 1
             e1.record(stream)
             e1.synchronize()
@@ -590,15 +592,15 @@ def run_gpu(args):
         warm = statistics.median(warm_s)
         extra["warm_l2"] = {"ms_per_step": warm / args.steps * 1e3,
                             "value": N * args.steps / warm,
-                            "how": f"median of {len(warm_s)} x {args.steps} steps launched "
-                                   "from Python"}
+                            "how": f"median of {len(warm_s)} x {args.steps} steps of one plan "
+                                   "launched from Python"}
         d_hp = A.device_hparams(hp, device)
         d_step = torch.full((1,), t, dtype=torch.int64, device=device)
         flags = A.STEP_CLIP if clip else 0
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(args.steps):
-                plans[i % n_grad].step_device(d_hp, d_step, flags, grad_norm=norm if clip else None)
+                plans[0].step_device(d_hp, d_step, flags, grad_norm=norm if clip else None)
         graph.replay()
         torch.cuda.synchronize(device)
         g_all = []
@@ -612,8 +614,8 @@ def run_gpu(args):
         t = int(d_step.item())
         extra["graph_warm_l2"] = {"ms_per_step": g_s / args.steps * 1e3,
                                   "value": N * args.steps / g_s,
-                                  "how": f"{args.steps} device-resident steps in one CUDA graph, "
-                                         f"median of {len(g_all)} replays"}
+                                  "how": f"{args.steps} device-resident steps of one plan in one "
+                                         f"CUDA graph, median of {len(g_all)} replays"}
         del graph
 
     # end to end through the public API, gradients arriving in pinned host
