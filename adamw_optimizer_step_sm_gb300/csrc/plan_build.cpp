@@ -343,17 +343,22 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
     // share `relief` short (never below zero); cuts inside a vector body
     // fall on multiples of kVec from the body's start so every chunk of it
     // starts 16-byte aligned.
-    auto round_vec = [](int64_t x) { return (x + kVec - 1) / kVec * kVec; };
-    const int64_t even = round_vec((P.total + grid - 1) / grid);
-    const int64_t target0 = grid == 1 ? P.total : even > relief ? even - relief : 0;
-    const int64_t target =
-        grid == 1 ? P.total : round_vec((P.total - target0 + grid - 2) / (grid - 1));
+    // Shares in whole vectors: CTA 0's the even share less the relief, the
+    // others' the rest dealt out so that they differ by one vector at most.
+    const int64_t vecs = (P.total + kVec - 1) / kVec;
+    const int64_t even = (vecs + grid - 1) / grid, relief_v = relief / kVec;
+    const int64_t v0 = grid == 1 ? vecs : even > relief_v ? even - relief_v : 0;
+    const int64_t per = grid == 1 ? 0 : (vecs - v0) / (grid - 1);
+    const int64_t extra = grid == 1 ? 0 : (vecs - v0) % (grid - 1);
+    auto want_of = [&](int32_t b) {
+        return (b == 0 ? v0 : per + (b - 1 < extra ? 1 : 0)) * kVec;
+    };
     int32_t cta = 0;
     int64_t filled = 0;
     for (const Seg& s : segs) {
         int64_t pos = 0;
         while (pos < s.len) {
-            const int64_t want = cta == 0 ? target0 : target;
+            const int64_t want = want_of(cta);
             if (filled >= want && cta < grid - 1) {
                 ++cta;
                 filled = 0;

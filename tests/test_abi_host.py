@@ -106,6 +106,29 @@ def test_partition_covers_each_element_once_and_balances():
             _check_partition(entries, mode, grid)
 
 
+@pytest.mark.parametrize("total,grid,cta0", [
+    (1_048_576, 456, 0),                        # contiguous, even share 2300 < 4096: none
+    (4_000_000, 456, 8776 - 4096),              # contiguous, share 8776 (vector-rounded)
+    (13_850_000, 304, None),                    # round-robin tiles, 6 rounds
+    (1_000, 1, 1_000)])                         # one CTA takes everything
+def test_cta0_share_is_short_by_the_memo_relief(total, grid, cta0):
+    """CTA 0 of the update partition gets 4096 elements less than the others
+    (none when its share is smaller), so that the device step's CTA 0 can
+    compute the next step's scalars first; the other CTAs stay balanced."""
+    chunks = _check_partition([_fake(0, total, 0)], 0, grid)
+    load = np.zeros(grid, np.int64)
+    for c in chunks:
+        if c.cta >= 0:
+            load[c.cta] += c.len
+    if cta0 is not None:
+        assert load[0] == cta0, (load[0], cta0)
+    if grid > 1:
+        rest = load[1:]
+        assert rest.max() - rest.min() <= 2048, (rest.min(), rest.max())
+        if cta0 is None:
+            assert abs(rest.mean() - load[0] - 4096) <= 512, (load[0], rest.mean())
+
+
 @pytest.mark.parametrize("sizes,grid", [([13_850_000], 304), ([13_850_000], 456),
                                         ([125_000_007, 3, 9, 1 << 20], 456),
                                         ([1000003] * 40 + [7, 65537], 152),
