@@ -189,9 +189,12 @@ typedef struct {
  * table, and (with ADAMW_PLAN_NORM) builds the norm kernel's own partition
  * and allocates the norm workspace.  With ADAMW_PLAN_NORM, a list whose
  * gradients take at most 32 MiB (16.7M parameters) runs its clipped steps as
- * one cooperative launch: norm partials, a bounded grid barrier, and the
- * update reading g again (from L2 where it fits) (unless ADAMW_PLAN_NO_FUSE;
- * adamw_plan_info_t.fused says which).  The norm is the same either way.
+ * one launch whose grid fits on the device at once: norm partials, a bounded
+ * grid barrier, and the update reading g again (from L2 where it fits)
+ * (unless ADAMW_PLAN_NO_FUSE; adamw_plan_info_t.fused says which).  Either
+ * way the norm is the exact sum of squares up to fp64 rounding; the two
+ * paths group the sum differently (different grids), so their norms may
+ * differ in the last bits.
  * Synchronous (it allocates and copies).  host_table is read during the call
  * only.  On error *out is left NULL and nothing stays allocated.
  * Errors: INVALID_ARG (NULL out or table with n_tensors > 0, n_tensors < 0,

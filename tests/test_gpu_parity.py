@@ -96,8 +96,8 @@ def test_other_anyprecision_options_sampled_full_size(name):
 
 def test_fused_clipped_shard_matches_oracle():
     """A 13.85M-element shard with clipping: each clipped step is one fused
-    cooperative launch (norm, grid barrier, update); bit-identical to the
-    oracle over 20 steps including the skipped step 7."""
+    launch (norm, grid barrier, update); bit-identical to the oracle over 20
+    steps including the skipped step 7."""
     w = W.WORKLOADS["bert55m_shard_mixed_clip"]
     gpu = H.GpuSide(w)
     assert gpu.plan.info.fused == 1
