@@ -138,11 +138,12 @@ static_assert(sizeof(ChunkPtr) == (ADAMW_CHECK_BOUNDS ? 144 : 48), "chunk layout
 constexpr int kNormCtas = ADAMW_NORM_CTAS;
 constexpr int kNormUnroll = ADAMW_NORM_UNROLL;
 // 1: the update's last rounds (about kDynSharePct percent of the list) are
-// not dealt to CTAs but cut into tiles of kTileElems that the CTAs claim
-// with an atomic counter once their own tiles are done, so that CTAs on SMs
-// that stream faster take more of them.  Measured on GB300 before this, the
-// CTAs of one launch with equal work ended up to 8 % apart (the 1.3B list:
-// 3.29 to 3.58 ms, median 3.41), SM to SM.
+// not dealt to CTAs but cut into tiles (at most kTileElems) that the CTAs
+// claim with an atomic counter once their own tiles are done, so that CTAs
+// on SMs that stream faster take more of them.  Measured on GB300: with
+// equal work, the CTAs of one launch ended up to 8 % apart (the 1.3B list:
+// 3.29 to 3.58 ms, median 3.41), SM to SM; with the claims within 4 us of
+// each other, and the step went from 3.57 to 3.46 ms.
 #ifndef ADAMW_DYN_TAIL
 #define ADAMW_DYN_TAIL 1
 #endif
@@ -252,20 +253,21 @@ struct PowTable {
 };
 
 // The plan's claim-and-arrival word of the update partition, one 64-bit
-// atomic word: bits 0-23 count the claims of last-round pieces, bits 24-43
-// the CTAs that have finished (the last one to arrive zeroes the word for
-// the next launch), bits 44-63 the CTAs that saw a non-finite gradient (the
-// one-launch device step's flag).
+// atomic word: bits 0-23 count the claims of the last rounds' pieces, bits
+// 24-43 the CTAs that have finished (the last one to arrive zeroes the word
+// for the next launch), bits 44-63 the CTAs that saw a non-finite gradient
+// (the one-launch device step's flag).
 constexpr unsigned long long kSyncClaim = 1ull;
 constexpr unsigned long long kSyncArrive = 1ull << 24;
 constexpr unsigned long long kSyncFlagged = 1ull << 44;
 constexpr unsigned long long kSyncClaimMask = kSyncArrive - 1;
 constexpr unsigned long long kSyncArriveMask = (kSyncFlagged - 1) & ~kSyncClaimMask;
 
-// Where the claimable last-round chunks are, for the kernels.
+// Where the claimable chunks of the last rounds are, for the kernels.
 struct DynTail {
     int32_t begin;                  // index of the first claimable chunk
-    int32_t n;                      // how many (0: none, no claims, no arrivals)
+    int32_t n;                      // how many (0: none; then only the one-launch
+                                    // device step counts arrivals)
     unsigned long long* sync;       // the claim-and-arrival word
 };
 
@@ -297,7 +299,7 @@ int make_scalars(const adamw_hparams_t* hp, int64_t step, StepScalars* out);
 
 // Splits the list over `grid` CTAs.  chunks are ordered by CTA; cta_begin has
 // grid + 1 entries (chunks of CTA b are [cta_begin[b], cta_begin[b+1])).
-// Chunks of the last round of the interleaved partition may be left to
+// Chunks of the last rounds of the interleaved partition may be left to
 // whichever CTA is free (chunk_cta -1): they follow every CTA's own chunks,
 // from index cta_begin[grid], n_dyn of them, and are claimed at run time.
 // CTA 0's share is `relief` elements short of the others' (kMemoRelief for

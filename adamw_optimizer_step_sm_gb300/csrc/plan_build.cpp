@@ -268,8 +268,9 @@ int build_partition(const adamw_tensor_t* table, int32_t n, int32_t mode,
         // 16-byte vectors; coarser alignment keeps warps' accesses on whole
         // cache lines) and the next tile is shorter by as much.
         // Tile j (round j / grid, CTA j % grid) is sched.size(j) long, so
-        // every CTA's tiles add up to the same quota within kBalanceAlign
-        // elements.  Cuts that end a tile of the last round move up to
+        // every CTA's tiles add up to its quota (CTA 0's `relief` short, the
+        // others' equal) within kBalanceAlign elements.  Cuts that end a
+        // tile of the last round move up to
         // kBalanceAlign only (there the quota's leftover is taken), all
         // others to kCutAlign.
         //

@@ -108,15 +108,46 @@ KERNEL_SOURCES = ("adamw_internal.h", "device_common.cuh", "kernels.cuh", "launc
                   "update_m25.cu", "update_m26.cu", "update_m27.cu")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the files that define the kernels, their launches and the
-    partition (what decides the DRAM traffic of a launch)."""
+def _code_only(text: str) -> str:
+    """C/C++ source with its comments removed and whitespace runs collapsed,
+    string and character literals kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the code (comments and layout left out) of the files that
+    define the kernels, their launches and the partition: what decides the
+    DRAM traffic of a launch.  `read(name)` gives a file's text (default:
+    the working tree's)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "adamw_optimizer_step_sm_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+                return fh.read()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        h.update(_code_only(read(f)).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

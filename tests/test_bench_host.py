@@ -87,8 +87,18 @@ def test_traffic_is_dropped_when_kernel_sources_change(tmp_path, monkeypatch):
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(
         {"x": {"kernel_source_hash": h, "dram_bytes_per_launch": 123}}))
     assert bench.recorded_traffic("x") == 123
+    # a comment or a blank line is not a change of the code
+    (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / bench.KERNEL_SOURCES[0]).write_text(
+        "a // note\n/* block\n comment */\n")
+    assert bench.recorded_traffic("x") == 123
     (tmp_path / "adamw_optimizer_step_sm_gb300" / "csrc" / bench.KERNEL_SOURCES[0]).write_text("b")
     assert bench.recorded_traffic("x") is None
+
+
+def test_code_only_drops_comments_and_layout_but_keeps_literals():
+    src = 'int a = 1; // one\n/* two\n lines */ const char* s = "x // y /* z */";\n  char c = \'/\';'
+    assert bench._code_only(src) == 'int a = 1; const char* s = "x // y /* z */"; char c = \'/\';'
+    assert bench._code_only("a+b") != bench._code_only("a-b")
 
 
 def test_reference_arm_prints_one_json_line(capsys):
