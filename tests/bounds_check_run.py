@@ -16,6 +16,8 @@ from adamw_optimizer_step_sm_gb300 import workloads as W
 
 RAGGED = [1, 7, 8, 9, 4095, 65537, 0, 3, 1000003, 255, 256, 257, 3 * 768, 50272]
 LONG = [3_000_001, 7, 2_500_003, 65_537, 1_999_999, 1, 4_194_304, 257, 1_048_583, 9]
+# more than 8 rounds of tiles: the last rounds are claimed at run time
+CLAIMED = [30_000_001, 7, 6_500_003, 65_537, 1, 4_194_304, 1_048_583]
 
 
 def workload(name, mode, sizes, clip, steps=3):
@@ -90,6 +92,10 @@ def main():
             parity_with_status(workload("long", mode, LONG, clip), (1, 3))
             parity_with_status(workload("long", mode, LONG, clip), (8, 0), device_step=True)
             n += 2
+    for mode in (W.MODE_BF16_KAHAN, W.MODE_MIXED):
+        parity_with_status(workload("claimed", mode, CLAIMED, 0.5, steps=2), (1, 3))
+        parity_with_status(workload("claimed", mode, CLAIMED, 0.0, steps=2), (8, 0), device_step=True)
+        n += 2
     fused = parity_with_status(workload("fused", W.MODE_MIXED, [13_850_000], 1.0), (8, 0))
     assert fused == 1
     n += 1

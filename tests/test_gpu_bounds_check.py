@@ -2,10 +2,11 @@
 memory sanitizer): every kernel checks each chunk against its tensor's
 buffers before touching it.  Builds that variant into a temporary folder
 and runs tests/bounds_check_run.py against it in a child process: every
-storage mode over ragged and long lists, clipped (fused and not) and
-device-resident steps, must run with no chunk refused and bit-identical to
-the oracle; a chunk lengthened past its tensor must be refused, reported in
-the device status word and left unwritten."""
+storage mode over ragged and long lists (also lists whose last rounds are
+claimed at run time), clipped (fused and not) and device-resident steps,
+must run with no chunk refused and bit-identical to the oracle; a chunk
+lengthened past its tensor must be refused, reported in the device status
+word and left unwritten."""
 import os
 import subprocess
 import sys
