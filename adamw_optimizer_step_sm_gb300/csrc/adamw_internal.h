@@ -2,6 +2,7 @@
 // the CUDA kernels (adamw_sm.cu).  Not part of the public ABI.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -251,6 +252,10 @@ struct PowTable {
     int32_t pad_;
     double sq[2][64];
 };
+// memo_next reads the rows 16 bytes at a time from memo + 2 (the memo slots
+// start 256-byte aligned in the plan)
+static_assert((2 * sizeof(ScalarMemo)) % 16 == 0 && offsetof(PowTable, sq) % 16 == 0,
+              "squares table rows 16-byte aligned");
 
 // The plan's claim-and-arrival word of the update partition, one 64-bit
 // atomic word: bits 0-23 count the claims of the last rounds' pieces, bits
