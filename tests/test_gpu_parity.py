@@ -273,6 +273,32 @@ def test_claimed_tiles_match_oracle_on_host_and_device_paths(mode, clip):
     b_plan.close()
 
 
+@pytest.mark.parametrize("mode,clip", [(W.MODE_BF16_KAHAN, 0.5), (W.MODE_MIXED, 0.0),
+                                       (W.MODE_ANYPREC | 7, 0.5)])
+def test_claimed_tiles_over_thousands_of_small_tensors(mode, clip):
+    """The claimed last rounds falling on 2500 small tensors (37 and 1000
+    elements) at the end of a list of more than 8 rounds, on bases skewed so
+    that every tensor has an element-path head: claimed tiles made of many
+    chunks, element-path chunks and pieces shorter than a vector, every
+    element against the oracle."""
+    sizes = [30_000_000, 6_000_001] + [37] * 2000 + [1000] * 500 + [5]
+    w = _small("claimsmall", mode=mode, sizes=sizes, max_grad_norm=clip, steps=2)
+    probe = H.GpuSide(w, "cuda", W.make_state(w, "cuda", 1, 3))
+    v = probe.st.views
+    entries = [tuple(t.data_ptr() if t is not None else 0 for t in ts) + (ts[0].numel(),)
+               for ts in zip(v(probe.st.param), v(probe.g), v(probe.st.exp_avg),
+                             v(probe.st.exp_avg_sq), v(probe.st.aux))]
+    chunks = A.adamw_plan_chunks(entries, mode, probe.plan.info.grid)
+    claimed = {c.tensor for c in chunks if c.cta < 0}
+    assert len(claimed) > 2000 and any(c.cta < 0 and not c.vec for c in chunks), \
+        (len(claimed), "claimed chunks should span the small tensors, element paths included")
+    probe.plan.close()
+    del probe
+    rep, log = H.run_parity(w, align_elems=1, skew=3)
+    _assert(rep, log)
+    assert rep.exact == rep.n
+
+
 @pytest.mark.parametrize("mode", [W.MODE_BF16_KAHAN, W.MODE_MIXED, W.MODE_REMAINDER])
 def test_clip_skips_step_with_inf_and_writes_nothing(mode):
     w = _small("skip", mode=mode, max_grad_norm=1.0, inf_at=(2, 8, 777), steps=4)
