@@ -1,9 +1,10 @@
-"""GPU parity on random lists: 16 seeded cases, each a random storage mode,
+"""GPU parity on random lists: 20 seeded cases, each a random storage mode,
 a random mix of tensor sizes (empty, single-element, sub-vector, ragged and
 multi-million), a random layout (16-byte aligned or skewed bases), with or
-without clipping, and half of them long enough for the interleaved
-partition.  Every element of every buffer after 3 steps must match the
-oracle bit for bit."""
+without clipping; half of the first 16 long enough for the interleaved
+partition, the last 4 long enough (more than 8 rounds of tiles) for its
+last rounds to be claimed at run time.  Every element of every buffer after
+3 steps must match the oracle bit for bit."""
 import numpy as np
 import pytest
 
@@ -36,10 +37,12 @@ def _case(seed: int):
         sizes.append(int(rng.integers(6_000_000, 9_000_000)))
     clip = float(rng.choice([0.0, 0.3, 1.0]))
     layout = (8, 0) if rng.random() < 0.5 else (1, int(rng.integers(1, 8)))
+    if seed >= 16:   # claimed last rounds
+        sizes.insert(int(rng.integers(0, len(sizes) + 1)), int(rng.integers(30_000_000, 40_000_000)))
     return mode, sizes, clip, layout
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(20))
 def test_random_list(seed):
     mode, sizes, clip, layout = _case(seed)
     w = _small(f"random{seed}", mode=mode, sizes=sizes, max_grad_norm=clip, steps=3)
