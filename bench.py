@@ -402,7 +402,10 @@ def run_e2e(args, w, st, grads, plans, hp, clip, t, world, device) -> dict:
                   itself; the kernels read it over NVLink-C2C
     """
     N = w.total
-    k_e2e = max(2, min(args.steps, 10))
+    # as many steps as the timed region (at most 50): the overlapped path's
+    # first copy and last step are not hidden, and a window of more steps
+    # spreads them the way a training run does
+    k_e2e = max(2, min(args.steps, 50))
     stream = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device)
     host_g = [torch.empty(grads[0].numel(), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
